@@ -1,0 +1,9 @@
+"""CPU oracle (test infrastructure; never imported by the product path)."""
+from .ragged_attention import (  # noqa: F401
+    attend,
+    attend_row,
+    pack_indices,
+    pack_rows,
+    pipeline,
+    unpack,
+)
