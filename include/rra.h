@@ -1,0 +1,195 @@
+/*
+ * rra.h -- ragged (token-pruned) bidirectional attention for ViTs, C ABI.
+ *
+ * The operation is the pack -> attend -> unpack pipeline of "Dispatch-Aware
+ * Ragged Attention for Pruned Vision Transformers" (arXiv 2604.15408):
+ *   - abstract: a bidirectional (non-causal) attention kernel run on
+ *     token-pruned ViT sequences (at most 197 tokens at 224 px, 577 at
+ *     384 px) inside a complete pack-attend-unpack pipeline whose outputs
+ *     match padded SDPA;
+ *   - agents-report.net article on the paper, section "方法概覽：
+ *     pack-attend-unpack 流程" (method overview): (1) fused token packing --
+ *     GPU index work yields per-image offsets (cu_seqlens) and destination
+ *     indices, and a vectorised copy gathers surviving tokens into one flat
+ *     buffer; (2) the ragged attention kernel runs directly on that compact
+ *     buffer; (3) unpack writes results back to the original batch positions
+ *     using cu_seqlens.  Section "問題：填充與派遣的瓶頸" (problem) names host
+ *     dispatch as the bottleneck, which the graph plan below addresses.
+ *
+ * Conventions for every entry point:
+ *   - Tensors are device pointers, contiguous, 16-byte aligned (else
+ *     RRA_ERR_MISALIGNED).  Padded tensors are [B, N, H, d] row-major; packed
+ *     tensors are [cap, H, d] with cap = B*N rows, of which the first T (the
+ *     number of kept tokens, known only on the device) are written.
+ *   - d must be 64 (else RRA_ERR_UNSUPPORTED); 1 <= N <= 1024; H >= 1;
+ *     1 <= B <= 65535; B*N*H*d < 2^31.
+ *   - The keep mask is uint8 [B, N]; any nonzero byte keeps the token.
+ *   - Input dtype is RRA_F16 or RRA_BF16; attention outputs may also be
+ *     RRA_F32.  Softmax and both products accumulate in fp32.
+ *   - Ownership: the caller allocates and frees every buffer.  The library
+ *     allocates no device memory, except the CUDA graph owned by an rra_plan.
+ *   - Asynchrony: every call only enqueues work on `stream` (a cudaStream_t;
+ *     NULL is the legacy default stream).  Nothing synchronises and nothing
+ *     is copied device->host, so every call can be captured in a CUDA graph.
+ *   - Errors: argument checks run on the host before anything is launched
+ *     and return a status with nothing enqueued.  A failed launch returns
+ *     RRA_ERR_CUDA.  Inconsistent device-side data (e.g. a cu_seqlens entry
+ *     longer than max_seqlen) never traps: the kernel skips the bad work and
+ *     records a code that rra_get_device_error() reads after the caller syncs.
+ *   - rra_last_error_message() gives a one-line description of the last
+ *     non-OK status returned on the calling thread.
+ */
+#ifndef RRA_H
+#define RRA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define RRA_API __attribute__((visibility("default")))
+#else
+#define RRA_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  RRA_OK = 0,
+  RRA_ERR_INVALID_ARG = 1, /* null pointer, bad size, bad enum          */
+  RRA_ERR_UNSUPPORTED = 2, /* valid but unsupported (d != 64, N > 1024)  */
+  RRA_ERR_MISALIGNED = 3,  /* a tensor pointer not 16-byte aligned       */
+  RRA_ERR_CUDA = 4,        /* a CUDA runtime call or launch failed       */
+  RRA_ERR_DEVICE = 5       /* a kernel recorded a device-side error code */
+} rra_status;
+
+typedef enum { RRA_F16 = 0, RRA_BF16 = 1, RRA_F32 = 2 } rra_dtype;
+
+/* Device-side error codes reported by rra_get_device_error(). */
+enum {
+  RRA_DEVERR_NONE = 0,
+  RRA_DEVERR_SEQ_TOO_LONG = 1,  /* attend: cu_seqlens[b+1]-cu_seqlens[b] > max_seqlen */
+  RRA_DEVERR_SEQ_NEGATIVE = 2,  /* attend: cu_seqlens decreasing                      */
+  RRA_DEVERR_INDEX_RANGE = 3,   /* attend/unpack: src_idx or dst_idx out of range     */
+  RRA_DEVERR_WAIT_TIMEOUT = 4   /* a bounded on-chip wait gave up                     */
+};
+
+/* Bytes of workspace rra_pipeline needs for these sizes (0 on bad args):
+ * cu_seqlens [B+1], dst_idx [B*N], src_idx [B*N] (int32), then packed Q, K, V
+ * [B*N, H, d] in the input dtype, each section 256-byte aligned. */
+RRA_API size_t rra_workspace_bytes(int B, int N, int H, int d, rra_dtype in_dtype);
+
+/* Byte offsets of the sections of that workspace, in the order
+ * cu_seqlens, dst_idx, src_idx, qp, kp, vp (6 entries). */
+RRA_API rra_status rra_workspace_offsets(int B, int N, int H, int d, rra_dtype in_dtype,
+                                         size_t offsets[6]);
+
+/* Fused token packing (method overview, bullet 1), one kernel launch:
+ *   cu_seqlens[b]   = number of kept tokens in images 0..b-1 (cu[B] = T);
+ *   dst_idx[b*N+j]  = packed row of token (b, j), or -1 if it is pruned;
+ *   src_idx[t]      = b*N+j for packed row t (t < T; rows >= T untouched);
+ *   qp/kp/vp[t]     = bit copies of q/k/v[b, j] (all H heads of the token);
+ *   out_zero_fill   = optional [B, N, H, d] tensor of `out_dtype`: its rows at
+ *                     pruned positions are set to +0 (the unpack's fill, done
+ *                     here so a scattering rra_attend completes the output).
+ * Packed order is images in batch order, tokens in original order. */
+RRA_API rra_status rra_pack(const uint8_t* keep, int B, int N, int H, int d, rra_dtype in_dtype,
+                            const void* q, const void* k, const void* v,
+                            int32_t* cu_seqlens, int32_t* dst_idx, int32_t* src_idx,
+                            void* qp, void* kp, void* vp,
+                            void* out_zero_fill, rra_dtype out_dtype, void* stream);
+
+/* Bidirectional ragged attention on packed buffers (method overview,
+ * bullet 2; abstract).  For image b with rows s = cu[b] .. e = cu[b+1]-1 and
+ * head h, for every row i in [s, e]:
+ *   O[i, h, :] = sum_j softmax_j(scale * <Q[i,h,:], K[j,h,:]>) V[j, h, :],
+ *   j over [s, e] only (no causal mask).  One kernel launch; the grid is sized
+ * from max_seqlen (an upper bound on every image's length) and lengths are
+ * read on the device.
+ *   src_idx == NULL: `o` is packed [cap, H, d] and row i is written at row i.
+ *   src_idx != NULL: `o` is padded [B, N, H, d] and row i is written at flat
+ *   position src_idx[i] (the unpack fused into the epilogue, bullet 3); rows
+ *   at pruned positions are not touched (rra_pack's out_zero_fill sets them).
+ * An image with zero rows writes nothing. */
+RRA_API rra_status rra_attend(const void* qp, const void* kp, const void* vp,
+                              const int32_t* cu_seqlens, int B, int max_seqlen, int H, int d,
+                              float scale, rra_dtype in_dtype, void* o, rra_dtype out_dtype,
+                              const int32_t* src_idx, int N, void* stream);
+
+/* Unpack (method overview, bullet 3): out[b, j] = op[dst_idx[b*N+j]] when
+ * dst_idx >= 0, else +0.  `op` is packed [cap, H, d] and `out` padded
+ * [B, N, H, d], both of `dtype` (F16, BF16 or F32). */
+RRA_API rra_status rra_unpack(const void* op, const int32_t* dst_idx, int B, int N, int H, int d,
+                              rra_dtype dtype, void* out, void* stream);
+
+/* The whole path: rra_pack (with out_zero_fill = out) then rra_attend
+ * scattering into `out` [B, N, H, d] of out_dtype.  Two kernel launches, no
+ * host synchronisation.  `workspace` holds rra_workspace_bytes() bytes laid
+ * out as rra_workspace_offsets() states; after the call it holds
+ * cu_seqlens, the pack indices and the packed Q/K/V. */
+RRA_API rra_status rra_pipeline(const uint8_t* keep, const void* q, const void* k, const void* v,
+                                int B, int N, int H, int d, float scale, rra_dtype in_dtype,
+                                void* out, rra_dtype out_dtype,
+                                void* workspace, size_t workspace_bytes, void* stream);
+
+/* The same as rra_pipeline for inputs and output in pinned HOST memory:
+ * enqueues host->device copies of keep/q/k/v into the caller's device
+ * buffers (keep_d, q_d, k_d, v_d), the pipeline into out_d, and a
+ * device->host copy of out_d into out_h, all on `stream`.  The caller syncs
+ * the stream before reading out_h. */
+RRA_API rra_status rra_pipeline_host(const uint8_t* keep_h, const void* q_h, const void* k_h,
+                                     const void* v_h, int B, int N, int H, int d, float scale,
+                                     rra_dtype in_dtype, void* out_h, rra_dtype out_dtype,
+                                     uint8_t* keep_d, void* q_d, void* k_d, void* v_d, void* out_d,
+                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* A captured CUDA graph of one rra_pipeline call on fixed buffers: the
+ * host-dispatch fix (problem section of the article).  rra_plan_create
+ * validates the arguments exactly like rra_pipeline, runs the pipeline once
+ * eagerly and captures it on a private stream; rra_plan_launch replays it on
+ * `stream` with one graph launch.  The plan keeps the pointers, not the
+ * data: later launches read whatever the buffers hold then. */
+typedef struct rra_plan rra_plan;
+RRA_API rra_status rra_plan_create(const uint8_t* keep, const void* q, const void* k, const void* v,
+                                   int B, int N, int H, int d, float scale, rra_dtype in_dtype,
+                                   void* out, rra_dtype out_dtype,
+                                   void* workspace, size_t workspace_bytes, rra_plan** plan);
+RRA_API rra_status rra_plan_launch(rra_plan* plan, void* stream);
+RRA_API void rra_plan_destroy(rra_plan* plan);
+
+/* Reads (and with clear != 0 resets) the device-side error code of the
+ * current device.  Synchronous: call it after the stream has been synced. */
+RRA_API rra_status rra_get_device_error(int32_t* code, int clear);
+
+/* Host-timed latency of rra_attend: `warmup` then `reps` repetitions of
+ * {t0 = steady_clock; rra_attend(...); cudaStreamSynchronize; t1}; the
+ * per-call microseconds go to samples_us[reps].  A measurement helper for
+ * the dispatch-floor numbers of the abstract; it launches rra_attend only. */
+RRA_API rra_status rra_time_attend_host(const void* qp, const void* kp, const void* vp,
+                                        const int32_t* cu_seqlens, int B, int max_seqlen, int H,
+                                        int d, float scale, rra_dtype in_dtype, void* o,
+                                        rra_dtype out_dtype, const int32_t* src_idx, int N,
+                                        void* stream, int warmup, int reps, double* samples_us);
+
+/* Same helper for a graph plan: {t0; rra_plan_launch; sync; t1}. */
+RRA_API rra_status rra_time_plan_host(rra_plan* plan, void* stream, int warmup, int reps,
+                                      double* samples_us);
+
+/* Reference floor for the two helpers above: {t0; launch an empty kernel;
+ * sync; t1}.  It measures this host + driver + GPU's own dispatch floor, the
+ * quantity the abstract compares across attention implementations. */
+RRA_API rra_status rra_time_null_host(void* stream, int warmup, int reps, double* samples_us);
+
+RRA_API const char* rra_status_string(rra_status status);
+RRA_API const char* rra_last_error_message(void);
+
+/* Number of this library's kernel launches enqueued by this process so far
+ * (every entry point adds the launches it makes; graph replays through
+ * rra_plan_launch add the launches the graph holds). */
+RRA_API uint64_t rra_launch_count(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* RRA_H */

@@ -1,0 +1,494 @@
+// C-ABI entry points of librra (declared in include/rra.h): host-side
+// argument checks, workspace layout, the two-launch pipeline, CUDA-graph
+// plans, the device error word and host-timing helpers.
+#include <atomic>
+#include <chrono>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <mutex>
+
+#include "common.cuh"
+
+namespace rra {
+namespace {
+
+// Device-side error word (one per device that loads the library).
+__device__ int32_t g_device_error = 0;
+
+__global__ void null_kernel() {}
+
+thread_local char g_last_message[256] = "";
+std::atomic<uint64_t> g_launches{0};
+
+rra_status fail(rra_status s, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_last_message, sizeof(g_last_message), fmt, ap);
+  va_end(ap);
+  return s;
+}
+
+rra_status cuda_fail(cudaError_t e, const char* what) {
+  return fail(RRA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+struct DeviceState {
+  bool ready = false;
+  int num_sms = 0;
+  int32_t* err = nullptr;
+};
+
+constexpr int kMaxDevices = 64;
+DeviceState g_devices[kMaxDevices];
+std::mutex g_device_mutex;
+
+// Per-device set-up, done once per device with that device current.
+rra_status device_state(DeviceState** out) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+  if (dev < 0 || dev >= kMaxDevices) return fail(RRA_ERR_UNSUPPORTED, "device ordinal %d too large", dev);
+  DeviceState& st = g_devices[dev];
+  std::lock_guard<std::mutex> lock(g_device_mutex);
+  if (!st.ready) {
+    e = cudaDeviceGetAttribute(&st.num_sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaDeviceGetAttribute");
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_device_error);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(error word)");
+    st.err = static_cast<int32_t*>(p);
+    st.ready = true;
+  }
+  *out = &st;
+  return RRA_OK;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool valid_in(rra_dtype t) { return t == RRA_F16 || t == RRA_BF16; }
+bool valid_out(rra_dtype t) { return t == RRA_F16 || t == RRA_BF16 || t == RRA_F32; }
+bool finite(float x) { return x == x && x != INFINITY && x != -INFINITY; }
+
+rra_status check_shape(int B, int N, int H, int d) {
+  if (d != 64) return fail(RRA_ERR_UNSUPPORTED, "head dim %d unsupported (only 64)", d);
+  if (B < 1 || B > 65535) return fail(RRA_ERR_INVALID_ARG, "B=%d outside [1, 65535]", B);
+  if (N < 1) return fail(RRA_ERR_INVALID_ARG, "N=%d < 1", N);
+  if (N > 1024) return fail(RRA_ERR_UNSUPPORTED, "N=%d > 1024", N);
+  if (H < 1 || H > 65535) return fail(RRA_ERR_INVALID_ARG, "H=%d outside [1, 65535]", H);
+  const long long elems = static_cast<long long>(B) * N * H * d;
+  if (elems >= (1LL << 31)) return fail(RRA_ERR_UNSUPPORTED, "B*N*H*d=%lld >= 2^31", elems);
+  return RRA_OK;
+}
+
+#define RRA_CHECK_PTR(p)                                                               \
+  do {                                                                                 \
+    if ((p) == nullptr) return fail(RRA_ERR_INVALID_ARG, "%s is null", #p);           \
+    if (!aligned16(p)) return fail(RRA_ERR_MISALIGNED, "%s not 16-byte aligned", #p); \
+  } while (0)
+
+#define RRA_TRY(expr)            \
+  do {                           \
+    rra_status _s = (expr);      \
+    if (_s != RRA_OK) return _s; \
+  } while (0)
+
+size_t align256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+void workspace_layout(int B, int N, int H, int d, rra_dtype in, size_t off[6], size_t* total) {
+  const size_t tokens = static_cast<size_t>(B) * N;
+  const size_t packed = tokens * H * d * dtype_bytes(in);
+  size_t o = 0;
+  off[0] = o; o = align256(o + (static_cast<size_t>(B) + 1) * 4);
+  off[1] = o; o = align256(o + tokens * 4);
+  off[2] = o; o = align256(o + tokens * 4);
+  off[3] = o; o = align256(o + packed);
+  off[4] = o; o = align256(o + packed);
+  off[5] = o; o = align256(o + packed);
+  *total = o;
+}
+
+// ---------------------------------------------------------------- enqueue
+
+rra_status enqueue_pack(const DeviceState& st, const uint8_t* keep, int B, int N, int H, int d,
+                        rra_dtype in, const void* q, const void* k, const void* v, int32_t* cu,
+                        int32_t* dst, int32_t* src, void* qp, void* kp, void* vp, void* outz,
+                        rra_dtype out_dt, cudaStream_t s) {
+  PackArgs a{};
+  a.keep = keep;
+  a.B = B;
+  a.N = N;
+  a.row_vecs = H * d * dtype_bytes(in) / 16;
+  a.out_row_vecs = outz ? H * d * dtype_bytes(out_dt) / 16 : 0;
+  a.q = static_cast<const uint4*>(q);
+  a.k = static_cast<const uint4*>(k);
+  a.v = static_cast<const uint4*>(v);
+  a.qp = static_cast<uint4*>(qp);
+  a.kp = static_cast<uint4*>(kp);
+  a.vp = static_cast<uint4*>(vp);
+  a.out_zero = static_cast<uint4*>(outz);
+  a.cu_seqlens = cu;
+  a.dst_idx = dst;
+  a.src_idx = src;
+  cudaError_t e = launch_pack(a, st.num_sms, s);
+  if (e != cudaSuccess) return cuda_fail(e, "pack launch");
+  return RRA_OK;
+}
+
+rra_status enqueue_attend(const DeviceState& st, const void* qp, const void* kp, const void* vp,
+                          const int32_t* cu, int B, int max_seqlen, int H, float scale,
+                          rra_dtype in, void* o, rra_dtype out_dt, const int32_t* src_idx, int N,
+                          cudaStream_t s) {
+  AttendArgs a{};
+  a.qp = qp;
+  a.kp = kp;
+  a.vp = vp;
+  a.cu_seqlens = cu;
+  a.src_idx = src_idx;
+  a.o = o;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.max_seqlen = max_seqlen;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = st.err;
+  cudaError_t e = launch_attend(a, in, out_dt, s);
+  if (e != cudaSuccess) return cuda_fail(e, "attend launch");
+  return RRA_OK;
+}
+
+struct PipelineArgs {
+  const uint8_t* keep;
+  const void *q, *k, *v;
+  int B, N, H, d;
+  float scale;
+  rra_dtype in, out_dt;
+  void* out;
+  void* ws;
+  size_t ws_bytes;
+};
+
+rra_status check_pipeline(const PipelineArgs& p) {
+  RRA_TRY(check_shape(p.B, p.N, p.H, p.d));
+  if (!valid_in(p.in)) return fail(RRA_ERR_INVALID_ARG, "input dtype %d invalid", static_cast<int>(p.in));
+  if (!valid_out(p.out_dt))
+    return fail(RRA_ERR_INVALID_ARG, "output dtype %d invalid", static_cast<int>(p.out_dt));
+  if (!finite(p.scale)) return fail(RRA_ERR_INVALID_ARG, "scale is not finite");
+  if (p.keep == nullptr) return fail(RRA_ERR_INVALID_ARG, "keep is null");
+  RRA_CHECK_PTR(p.q);
+  RRA_CHECK_PTR(p.k);
+  RRA_CHECK_PTR(p.v);
+  RRA_CHECK_PTR(p.out);
+  RRA_CHECK_PTR(p.ws);
+  size_t off[6], total = 0;
+  workspace_layout(p.B, p.N, p.H, p.d, p.in, off, &total);
+  if (p.ws_bytes < total)
+    return fail(RRA_ERR_INVALID_ARG, "workspace %zu bytes < %zu needed", p.ws_bytes, total);
+  return RRA_OK;
+}
+
+rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaStream_t s) {
+  size_t off[6], total = 0;
+  workspace_layout(p.B, p.N, p.H, p.d, p.in, off, &total);
+  uint8_t* ws = static_cast<uint8_t*>(p.ws);
+  int32_t* cu = reinterpret_cast<int32_t*>(ws + off[0]);
+  int32_t* dst = reinterpret_cast<int32_t*>(ws + off[1]);
+  int32_t* src = reinterpret_cast<int32_t*>(ws + off[2]);
+  void* qp = ws + off[3];
+  void* kp = ws + off[4];
+  void* vp = ws + off[5];
+  RRA_TRY(enqueue_pack(st, p.keep, p.B, p.N, p.H, p.d, p.in, p.q, p.k, p.v, cu, dst, src, qp, kp, vp,
+                       p.out, p.out_dt, s));
+  return enqueue_attend(st, qp, kp, vp, cu, p.B, p.N, p.H, p.scale, p.in, p.out, p.out_dt, src, p.N, s);
+}
+
+}  // namespace
+}  // namespace rra
+
+using namespace rra;
+
+struct rra_plan {
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+  int launches = 0;
+};
+
+extern "C" {
+
+const char* rra_status_string(rra_status s) {
+  switch (s) {
+    case RRA_OK: return "RRA_OK";
+    case RRA_ERR_INVALID_ARG: return "RRA_ERR_INVALID_ARG";
+    case RRA_ERR_UNSUPPORTED: return "RRA_ERR_UNSUPPORTED";
+    case RRA_ERR_MISALIGNED: return "RRA_ERR_MISALIGNED";
+    case RRA_ERR_CUDA: return "RRA_ERR_CUDA";
+    case RRA_ERR_DEVICE: return "RRA_ERR_DEVICE";
+  }
+  return "RRA_UNKNOWN_STATUS";
+}
+
+const char* rra_last_error_message(void) { return g_last_message; }
+
+uint64_t rra_launch_count(void) { return g_launches.load(); }
+
+size_t rra_workspace_bytes(int B, int N, int H, int d, rra_dtype in_dtype) {
+  if (check_shape(B, N, H, d) != RRA_OK || !valid_in(in_dtype)) return 0;
+  size_t off[6], total = 0;
+  workspace_layout(B, N, H, d, in_dtype, off, &total);
+  return total;
+}
+
+rra_status rra_workspace_offsets(int B, int N, int H, int d, rra_dtype in_dtype, size_t offsets[6]) {
+  RRA_TRY(check_shape(B, N, H, d));
+  if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
+  if (offsets == nullptr) return fail(RRA_ERR_INVALID_ARG, "offsets is null");
+  size_t total = 0;
+  workspace_layout(B, N, H, d, in_dtype, offsets, &total);
+  return RRA_OK;
+}
+
+rra_status rra_pack(const uint8_t* keep, int B, int N, int H, int d, rra_dtype in_dtype,
+                    const void* q, const void* k, const void* v, int32_t* cu_seqlens,
+                    int32_t* dst_idx, int32_t* src_idx, void* qp, void* kp, void* vp,
+                    void* out_zero_fill, rra_dtype out_dtype, void* stream) {
+  RRA_TRY(check_shape(B, N, H, d));
+  if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
+  if (out_zero_fill && !valid_out(out_dtype)) return fail(RRA_ERR_INVALID_ARG, "output dtype invalid");
+  if (keep == nullptr) return fail(RRA_ERR_INVALID_ARG, "keep is null");
+  RRA_CHECK_PTR(q);
+  RRA_CHECK_PTR(k);
+  RRA_CHECK_PTR(v);
+  RRA_CHECK_PTR(qp);
+  RRA_CHECK_PTR(kp);
+  RRA_CHECK_PTR(vp);
+  if (cu_seqlens == nullptr || dst_idx == nullptr || src_idx == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "index buffer is null");
+  if (out_zero_fill && !aligned16(out_zero_fill))
+    return fail(RRA_ERR_MISALIGNED, "out_zero_fill not 16-byte aligned");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  RRA_TRY(enqueue_pack(*st, keep, B, N, H, d, in_dtype, q, k, v, cu_seqlens, dst_idx, src_idx, qp, kp, vp,
+                       out_zero_fill, out_dtype, static_cast<cudaStream_t>(stream)));
+  g_launches += 1;
+  return RRA_OK;
+}
+
+rra_status rra_attend(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens,
+                      int B, int max_seqlen, int H, int d, float scale, rra_dtype in_dtype, void* o,
+                      rra_dtype out_dtype, const int32_t* src_idx, int N, void* stream) {
+  RRA_TRY(check_shape(B, max_seqlen, H, d));
+  if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
+  if (!valid_out(out_dtype)) return fail(RRA_ERR_INVALID_ARG, "output dtype invalid");
+  if (!finite(scale)) return fail(RRA_ERR_INVALID_ARG, "scale is not finite");
+  RRA_CHECK_PTR(qp);
+  RRA_CHECK_PTR(kp);
+  RRA_CHECK_PTR(vp);
+  RRA_CHECK_PTR(o);
+  if (cu_seqlens == nullptr) return fail(RRA_ERR_INVALID_ARG, "cu_seqlens is null");
+  if (src_idx != nullptr) RRA_TRY(check_shape(B, N, H, d));
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  RRA_TRY(enqueue_attend(*st, qp, kp, vp, cu_seqlens, B, max_seqlen, H, scale, in_dtype, o, out_dtype,
+                         src_idx, src_idx ? N : 0, static_cast<cudaStream_t>(stream)));
+  g_launches += 1;
+  return RRA_OK;
+}
+
+rra_status rra_unpack(const void* op, const int32_t* dst_idx, int B, int N, int H, int d, rra_dtype dtype,
+                      void* out, void* stream) {
+  RRA_TRY(check_shape(B, N, H, d));
+  if (!valid_out(dtype)) return fail(RRA_ERR_INVALID_ARG, "dtype invalid");
+  RRA_CHECK_PTR(op);
+  RRA_CHECK_PTR(out);
+  if (dst_idx == nullptr) return fail(RRA_ERR_INVALID_ARG, "dst_idx is null");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  UnpackArgs a{};
+  a.op = static_cast<const uint4*>(op);
+  a.dst_idx = dst_idx;
+  a.out = static_cast<uint4*>(out);
+  a.B = B;
+  a.N = N;
+  a.row_vecs = H * d * dtype_bytes(dtype) / 16;
+  a.err = st->err;
+  cudaError_t e = launch_unpack(a, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "unpack launch");
+  g_launches += 1;
+  return RRA_OK;
+}
+
+rra_status rra_pipeline(const uint8_t* keep, const void* q, const void* k, const void* v, int B, int N,
+                        int H, int d, float scale, rra_dtype in_dtype, void* out, rra_dtype out_dtype,
+                        void* workspace, size_t workspace_bytes, void* stream) {
+  PipelineArgs p{keep, q, k, v, B, N, H, d, scale, in_dtype, out_dtype, out, workspace, workspace_bytes};
+  RRA_TRY(check_pipeline(p));
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  RRA_TRY(enqueue_pipeline(*st, p, static_cast<cudaStream_t>(stream)));
+  g_launches += 2;
+  return RRA_OK;
+}
+
+rra_status rra_pipeline_host(const uint8_t* keep_h, const void* q_h, const void* k_h, const void* v_h,
+                             int B, int N, int H, int d, float scale, rra_dtype in_dtype, void* out_h,
+                             rra_dtype out_dtype, uint8_t* keep_d, void* q_d, void* k_d, void* v_d,
+                             void* out_d, void* workspace, size_t workspace_bytes, void* stream) {
+  PipelineArgs p{keep_d, q_d, k_d, v_d, B, N, H, d, scale, in_dtype, out_dtype, out_d, workspace,
+                 workspace_bytes};
+  RRA_TRY(check_pipeline(p));
+  if (keep_h == nullptr || q_h == nullptr || k_h == nullptr || v_h == nullptr || out_h == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "host buffer is null");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const size_t tokens = static_cast<size_t>(B) * N;
+  const size_t in_bytes = tokens * H * d * dtype_bytes(in_dtype);
+  const size_t out_bytes = tokens * H * d * dtype_bytes(out_dtype);
+  cudaError_t e;
+  if ((e = cudaMemcpyAsync(keep_d, keep_h, tokens, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "keep H2D");
+  if ((e = cudaMemcpyAsync(q_d, q_h, in_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "q H2D");
+  if ((e = cudaMemcpyAsync(k_d, k_h, in_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "k H2D");
+  if ((e = cudaMemcpyAsync(v_d, v_h, in_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
+    return cuda_fail(e, "v H2D");
+  RRA_TRY(enqueue_pipeline(*st, p, s));
+  g_launches += 2;
+  if ((e = cudaMemcpyAsync(out_h, out_d, out_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
+    return cuda_fail(e, "out D2H");
+  return RRA_OK;
+}
+
+rra_status rra_plan_create(const uint8_t* keep, const void* q, const void* k, const void* v, int B, int N,
+                           int H, int d, float scale, rra_dtype in_dtype, void* out, rra_dtype out_dtype,
+                           void* workspace, size_t workspace_bytes, rra_plan** plan) {
+  if (plan == nullptr) return fail(RRA_ERR_INVALID_ARG, "plan is null");
+  *plan = nullptr;
+  PipelineArgs p{keep, q, k, v, B, N, H, d, scale, in_dtype, out_dtype, out, workspace, workspace_bytes};
+  RRA_TRY(check_pipeline(p));
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  // Run once eagerly on a private stream: loads the kernels' modules before
+  // capture and surfaces launch errors with a plain status.
+  cudaStream_t s = nullptr;
+  cudaError_t e = cudaStreamCreateWithFlags(&s, cudaStreamNonBlocking);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreate");
+  rra_status rs = enqueue_pipeline(*st, p, s);
+  if (rs == RRA_OK) {
+    g_launches += 2;
+    e = cudaStreamSynchronize(s);
+    if (e != cudaSuccess) rs = cuda_fail(e, "plan warm-up");
+  }
+  cudaGraph_t graph = nullptr;
+  if (rs == RRA_OK) {
+    e = cudaStreamBeginCapture(s, cudaStreamCaptureModeThreadLocal);
+    if (e != cudaSuccess) {
+      rs = cuda_fail(e, "cudaStreamBeginCapture");
+    } else {
+      rra_status cap = enqueue_pipeline(*st, p, s);
+      e = cudaStreamEndCapture(s, &graph);
+      if (cap != RRA_OK) rs = cap;
+      else if (e != cudaSuccess) rs = cuda_fail(e, "cudaStreamEndCapture");
+    }
+  }
+  cudaGraphExec_t exec = nullptr;
+  if (rs == RRA_OK) {
+    e = cudaGraphInstantiate(&exec, graph, 0);
+    if (e != cudaSuccess) rs = cuda_fail(e, "cudaGraphInstantiate");
+  }
+  cudaStreamDestroy(s);
+  if (rs != RRA_OK) {
+    if (graph) cudaGraphDestroy(graph);
+    return rs;
+  }
+  rra_plan* pl = new rra_plan;
+  pl->graph = graph;
+  pl->exec = exec;
+  pl->launches = 2;
+  *plan = pl;
+  return RRA_OK;
+}
+
+rra_status rra_plan_launch(rra_plan* plan, void* stream) {
+  if (plan == nullptr || plan->exec == nullptr) return fail(RRA_ERR_INVALID_ARG, "plan is null");
+  cudaError_t e = cudaGraphLaunch(plan->exec, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cudaGraphLaunch");
+  g_launches += static_cast<uint64_t>(plan->launches);
+  return RRA_OK;
+}
+
+void rra_plan_destroy(rra_plan* plan) {
+  if (plan == nullptr) return;
+  if (plan->exec) cudaGraphExecDestroy(plan->exec);
+  if (plan->graph) cudaGraphDestroy(plan->graph);
+  delete plan;
+}
+
+rra_status rra_get_device_error(int32_t* code, int clear) {
+  if (code == nullptr) return fail(RRA_ERR_INVALID_ARG, "code is null");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  cudaError_t e = cudaMemcpy(code, st->err, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read device error");
+  if (clear) {
+    e = cudaMemset(st->err, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "clear device error");
+  }
+  return *code == 0 ? RRA_OK : RRA_ERR_DEVICE;
+}
+
+rra_status rra_time_attend_host(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens,
+                                int B, int max_seqlen, int H, int d, float scale, rra_dtype in_dtype,
+                                void* o, rra_dtype out_dtype, const int32_t* src_idx, int N, void* stream,
+                                int warmup, int reps, double* samples_us) {
+  if (reps < 1 || warmup < 0 || samples_us == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "bad timing arguments");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < warmup + reps; ++i) {
+    const auto t0 = std::chrono::steady_clock::now();
+    rra_status rs = rra_attend(qp, kp, vp, cu_seqlens, B, max_seqlen, H, d, scale, in_dtype, o, out_dtype,
+                               src_idx, N, stream);
+    if (rs != RRA_OK) return rs;
+    cudaError_t e = cudaStreamSynchronize(s);
+    const auto t1 = std::chrono::steady_clock::now();
+    if (e != cudaSuccess) return cuda_fail(e, "sync");
+    if (i >= warmup) samples_us[i - warmup] = std::chrono::duration<double, std::micro>(t1 - t0).count();
+  }
+  return RRA_OK;
+}
+
+rra_status rra_time_plan_host(rra_plan* plan, void* stream, int warmup, int reps, double* samples_us) {
+  if (reps < 1 || warmup < 0 || samples_us == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "bad timing arguments");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < warmup + reps; ++i) {
+    const auto t0 = std::chrono::steady_clock::now();
+    rra_status rs = rra_plan_launch(plan, stream);
+    if (rs != RRA_OK) return rs;
+    cudaError_t e = cudaStreamSynchronize(s);
+    const auto t1 = std::chrono::steady_clock::now();
+    if (e != cudaSuccess) return cuda_fail(e, "sync");
+    if (i >= warmup) samples_us[i - warmup] = std::chrono::duration<double, std::micro>(t1 - t0).count();
+  }
+  return RRA_OK;
+}
+
+rra_status rra_time_null_host(void* stream, int warmup, int reps, double* samples_us) {
+  if (reps < 1 || warmup < 0 || samples_us == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "bad timing arguments");
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int i = 0; i < warmup + reps; ++i) {
+    const auto t0 = std::chrono::steady_clock::now();
+    null_kernel<<<1, 32, 0, s>>>();
+    cudaError_t e = cudaGetLastError();
+    if (e == cudaSuccess) e = cudaStreamSynchronize(s);
+    const auto t1 = std::chrono::steady_clock::now();
+    if (e != cudaSuccess) return cuda_fail(e, "null kernel");
+    if (i >= warmup) samples_us[i - warmup] = std::chrono::duration<double, std::micro>(t1 - t0).count();
+  }
+  return RRA_OK;
+}
+
+}  // extern "C"

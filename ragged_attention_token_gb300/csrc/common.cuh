@@ -1,0 +1,65 @@
+// Internal declarations shared by the kernels and the C-ABI layer.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <stdint.h>
+
+#include "../../include/rra.h"
+
+namespace rra {
+
+inline int dtype_bytes(rra_dtype t) { return t == RRA_F32 ? 4 : 2; }
+
+// Records a device-side error code: the first code wins, later ones are kept
+// out so the reported code names the earliest anomaly seen.
+__device__ __forceinline__ void record_error(int32_t* err, int32_t code) {
+  if (err != nullptr) atomicCAS(err, 0, code);
+}
+
+struct PackArgs {
+  const uint8_t* keep;
+  int B, N;
+  int tok_per_cta;    // tokens handled by one CTA (multiple of 32)
+  int row_vecs;       // 16-byte vectors per token row of q/k/v (H*d*in_bytes/16)
+  int out_row_vecs;   // 16-byte vectors per token row of the zero-filled output, 0 = none
+  const uint4* q;
+  const uint4* k;
+  const uint4* v;
+  uint4* qp;
+  uint4* kp;
+  uint4* vp;
+  uint4* out_zero;
+  int32_t* cu_seqlens;
+  int32_t* dst_idx;
+  int32_t* src_idx;
+};
+
+struct AttendArgs {
+  const void* qp;
+  const void* kp;
+  const void* vp;
+  const int32_t* cu_seqlens;
+  const int32_t* src_idx;   // nullptr: packed output
+  void* o;
+  int B, H, N, max_seqlen;
+  float scale_log2;         // softmax scale times log2(e)
+  int32_t* err;
+};
+
+struct UnpackArgs {
+  const uint4* op;
+  const int32_t* dst_idx;
+  uint4* out;
+  int B, N;
+  int row_vecs;
+  int32_t* err;
+};
+
+// Launchers (each enqueues exactly one kernel on `stream`).
+cudaError_t launch_pack(const PackArgs& a, int num_sms, cudaStream_t stream);
+cudaError_t launch_attend(const AttendArgs& a, rra_dtype in, rra_dtype out, cudaStream_t stream);
+cudaError_t launch_unpack(const UnpackArgs& a, cudaStream_t stream);
+
+}  // namespace rra

@@ -1,0 +1,257 @@
+"""ctypes binding of librra (include/rra.h), with the same names.
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (torch provides device memory and
+streams); sizes and dtypes are read from them and passed as plain integers.
+Loading fails loudly when librra.so is missing -- there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+import torch
+
+_PKG_DIR = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG_DIR, "librra.so")
+HEADER_PATH = os.path.join(os.path.dirname(_PKG_DIR), "include", "rra.h")
+
+RRA_OK, RRA_ERR_INVALID_ARG, RRA_ERR_UNSUPPORTED, RRA_ERR_MISALIGNED, RRA_ERR_CUDA, RRA_ERR_DEVICE = range(6)
+RRA_F16, RRA_BF16, RRA_F32 = 0, 1, 2
+DEVERR_NONE, DEVERR_SEQ_TOO_LONG, DEVERR_SEQ_NEGATIVE, DEVERR_INDEX_RANGE, DEVERR_WAIT_TIMEOUT = range(5)
+
+_DTYPE = {torch.float16: RRA_F16, torch.bfloat16: RRA_BF16, torch.float32: RRA_F32}
+
+_vp = ctypes.c_void_p
+_i = ctypes.c_int
+_f = ctypes.c_float
+_sz = ctypes.c_size_t
+_dp = ctypes.POINTER(ctypes.c_double)
+
+_SIGNATURES = {
+    "rra_workspace_bytes": (_sz, [_i, _i, _i, _i, _i]),
+    "rra_workspace_offsets": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
+    "rra_pack": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp]),
+    "rra_attend": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp]),
+    "rra_unpack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
+    "rra_pipeline": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
+    "rra_pipeline_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i,
+                               _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "rra_plan_create": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz,
+                             ctypes.POINTER(_vp)]),
+    "rra_plan_launch": (_i, [_vp, _vp]),
+    "rra_plan_destroy": (None, [_vp]),
+    "rra_get_device_error": (_i, [ctypes.POINTER(ctypes.c_int32), _i]),
+    "rra_time_attend_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp,
+                                  _i, _i, _dp]),
+    "rra_time_plan_host": (_i, [_vp, _vp, _i, _i, _dp]),
+    "rra_time_null_host": (_i, [_vp, _i, _i, _dp]),
+    "rra_status_string": (ctypes.c_char_p, [_i]),
+    "rra_last_error_message": (ctypes.c_char_p, []),
+    "rra_launch_count": (ctypes.c_uint64, []),
+}
+
+_LIB = None
+
+
+class RRAError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(message)
+        self.status = status
+
+
+def header_symbols(path: str = HEADER_PATH) -> list[str]:
+    """Every function the C header declares."""
+    text = open(path).read()
+    return sorted(set(re.findall(r"RRA_API\s+[\w\s\*]*?\b(rra_\w+)\s*\(", text)))
+
+
+def lib() -> ctypes.CDLL:
+    """Load librra.so once (raises if it has not been built)."""
+    global _LIB
+    if _LIB is None:
+        if not os.path.exists(LIB_PATH):
+            raise RuntimeError(f"{LIB_PATH} is missing: build it with "
+                               "`python -m ragged_attention_token_gb300.build`")
+        L = ctypes.CDLL(LIB_PATH)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(L, name)
+            fn.restype = res
+            fn.argtypes = args
+        _LIB = L
+    return _LIB
+
+
+def _check(status: int) -> None:
+    if status != RRA_OK:
+        L = lib()
+        raise RRAError(status, f"{L.rra_status_string(status).decode()}: "
+                               f"{L.rra_last_error_message().decode()}")
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError("expected a contiguous tensor")
+    return t.data_ptr()
+
+
+def _stream(stream):
+    if stream is None:
+        return torch.cuda.current_stream().cuda_stream
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _nbytes(t) -> int:
+    return t.numel() * t.element_size()
+
+
+def dtype_code(dt: torch.dtype) -> int:
+    return _DTYPE[dt]
+
+
+def workspace_bytes(B: int, N: int, H: int, d: int, dtype: torch.dtype) -> int:
+    return int(lib().rra_workspace_bytes(B, N, H, d, _DTYPE[dtype]))
+
+
+def workspace_offsets(B: int, N: int, H: int, d: int, dtype: torch.dtype) -> list[int]:
+    arr = (_sz * 6)()
+    _check(lib().rra_workspace_offsets(B, N, H, d, _DTYPE[dtype], arr))
+    return list(arr)
+
+
+def workspace_views(ws: torch.Tensor, B: int, N: int, H: int, d: int, dtype: torch.dtype):
+    """(cu_seqlens, dst_idx, src_idx, qp, kp, vp) views into a pipeline workspace."""
+    off = workspace_offsets(B, N, H, d, dtype)
+    es = torch.empty((), dtype=dtype).element_size()
+    cap = B * N
+    cu = ws[off[0]:off[0] + 4 * (B + 1)].view(torch.int32)
+    dst = ws[off[1]:off[1] + 4 * cap].view(torch.int32)
+    src = ws[off[2]:off[2] + 4 * cap].view(torch.int32)
+    packed = [ws[o:o + cap * H * d * es].view(dtype).view(cap, H, d) for o in off[3:6]]
+    return (cu, dst, src, *packed)
+
+
+def pack(keep, q, k, v, cu_seqlens, dst_idx, src_idx, qp, kp, vp, out_zero_fill=None, stream=None):
+    B, N, H, d = q.shape
+    out_dt = _DTYPE[out_zero_fill.dtype] if out_zero_fill is not None else RRA_F32
+    _check(lib().rra_pack(_ptr(keep), B, N, H, d, _DTYPE[q.dtype], _ptr(q), _ptr(k), _ptr(v),
+                          _ptr(cu_seqlens), _ptr(dst_idx), _ptr(src_idx), _ptr(qp), _ptr(kp), _ptr(vp),
+                          _ptr(out_zero_fill), out_dt, _stream(stream)))
+
+
+def attend(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, scale: float = 0.125,
+           src_idx=None, N: int = 0, stream=None):
+    H, d = qp.shape[-2], qp.shape[-1]
+    _check(lib().rra_attend(_ptr(qp), _ptr(kp), _ptr(vp), _ptr(cu_seqlens), B, max_seqlen, H, d,
+                            float(scale), _DTYPE[qp.dtype], _ptr(o), _DTYPE[o.dtype], _ptr(src_idx), N,
+                            _stream(stream)))
+
+
+def unpack(op, dst_idx, B: int, N: int, out, stream=None):
+    H, d = op.shape[-2], op.shape[-1]
+    _check(lib().rra_unpack(_ptr(op), _ptr(dst_idx), B, N, H, d, _DTYPE[op.dtype], _ptr(out),
+                            _stream(stream)))
+
+
+def pipeline(keep, q, k, v, out, workspace, scale: float = 0.125, stream=None):
+    B, N, H, d = q.shape
+    _check(lib().rra_pipeline(_ptr(keep), _ptr(q), _ptr(k), _ptr(v), B, N, H, d, float(scale),
+                              _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], _ptr(workspace),
+                              _nbytes(workspace), _stream(stream)))
+
+
+def pipeline_host(keep_h, q_h, k_h, v_h, out_h, keep_d, q_d, k_d, v_d, out_d, workspace,
+                  scale: float = 0.125, stream=None):
+    """Host-buffer pipeline: H2D copies, pipeline, D2H copy, all enqueued on `stream`."""
+    for t in (keep_h, q_h, k_h, v_h, out_h):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host buffers must be contiguous CPU tensors (pinned for async copies)")
+    B, N, H, d = q_h.shape
+    _check(lib().rra_pipeline_host(keep_h.data_ptr(), q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
+                                   B, N, H, d, float(scale), _DTYPE[q_h.dtype], out_h.data_ptr(),
+                                   _DTYPE[out_h.dtype], _ptr(keep_d), _ptr(q_d), _ptr(k_d), _ptr(v_d),
+                                   _ptr(out_d), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+class Plan:
+    """A CUDA graph of one pipeline call on fixed buffers (rra_plan_*)."""
+
+    def __init__(self, keep, q, k, v, out, workspace, scale: float = 0.125):
+        B, N, H, d = q.shape
+        self._h = _vp()
+        self._keepalive = (keep, q, k, v, out, workspace)
+        _check(lib().rra_plan_create(_ptr(keep), _ptr(q), _ptr(k), _ptr(v), B, N, H, d, float(scale),
+                                     _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], _ptr(workspace),
+                                     _nbytes(workspace), ctypes.byref(self._h)))
+
+    def launch(self, stream=None):
+        _check(lib().rra_plan_launch(self._h, _stream(stream)))
+
+    def time_host(self, warmup: int, reps: int, stream=None) -> list[float]:
+        buf = (ctypes.c_double * reps)()
+        _check(lib().rra_time_plan_host(self._h, _stream(stream), warmup, reps, buf))
+        return list(buf)
+
+    def close(self):
+        if self._h:
+            lib().rra_plan_destroy(self._h)
+            self._h = _vp()
+            self._keepalive = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def get_device_error(clear: bool = True) -> int:
+    code = ctypes.c_int32(0)
+    st = lib().rra_get_device_error(ctypes.byref(code), 1 if clear else 0)
+    if st not in (RRA_OK, RRA_ERR_DEVICE):
+        _check(st)
+    return int(code.value)
+
+
+def time_attend_host(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, warmup: int, reps: int,
+                     scale: float = 0.125, src_idx=None, N: int = 0, stream=None) -> list[float]:
+    H, d = qp.shape[-2], qp.shape[-1]
+    buf = (ctypes.c_double * reps)()
+    _check(lib().rra_time_attend_host(_ptr(qp), _ptr(kp), _ptr(vp), _ptr(cu_seqlens), B, max_seqlen, H, d,
+                                      float(scale), _DTYPE[qp.dtype], _ptr(o), _DTYPE[o.dtype],
+                                      _ptr(src_idx), N, _stream(stream), warmup, reps, buf))
+    return list(buf)
+
+
+def time_null_host(warmup: int, reps: int, stream=None) -> list[float]:
+    """Host-timed {empty kernel launch + sync}: the platform's dispatch floor."""
+    buf = (ctypes.c_double * reps)()
+    _check(lib().rra_time_null_host(_stream(stream), warmup, reps, buf))
+    return list(buf)
+
+
+def launch_count() -> int:
+    return int(lib().rra_launch_count())
+
+
+# ------------------------------------------------------------- conveniences
+
+def alloc_workspace(B: int, N: int, H: int, d: int, dtype: torch.dtype, device="cuda") -> torch.Tensor:
+    n = workspace_bytes(B, N, H, d, dtype)
+    if n == 0:
+        raise RRAError(RRA_ERR_INVALID_ARG, "unsupported sizes for a workspace")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def run_pipeline(keep, q, k, v, scale: float = 0.125, out_dtype=None, stream=None):
+    """Allocate output + workspace with torch and run rra_pipeline once."""
+    B, N, H, d = q.shape
+    out = torch.empty((B, N, H, d), dtype=out_dtype or q.dtype, device=q.device)
+    ws = alloc_workspace(B, N, H, d, q.dtype, q.device)
+    pipeline(keep, q, k, v, out, ws, scale=scale, stream=stream)
+    return out, ws

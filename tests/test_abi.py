@@ -1,0 +1,94 @@
+"""The C-ABI library loads and exports every symbol include/rra.h declares.
+
+CPU only: the calls below fail host-side argument checks before any CUDA
+call is made, so no GPU is needed.
+"""
+import ctypes
+import subprocess
+
+import pytest
+
+from ragged_attention_token_gb300 import build, rra
+
+
+@pytest.fixture(scope="module")
+def L():
+    if not build.up_to_date():
+        build.build()
+    return rra.lib()
+
+
+def test_header_declares_the_boundary():
+    syms = rra.header_symbols()
+    for name in ("rra_pack", "rra_attend", "rra_unpack", "rra_pipeline", "rra_plan_create",
+                 "rra_plan_launch", "rra_plan_destroy", "rra_workspace_bytes", "rra_get_device_error"):
+        assert name in syms
+    assert set(syms) == set(rra._SIGNATURES), "binding and header disagree"
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in rra.header_symbols():
+        assert hasattr(L, name), name
+    out = subprocess.run(["nm", "-D", "--defined-only", rra.LIB_PATH], capture_output=True, text=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert exported == set(rra.header_symbols()), exported ^ set(rra.header_symbols())
+
+
+def test_workspace_layout(L):
+    B, N, H, d = 3, 197, 6, 64
+    n = L.rra_workspace_bytes(B, N, H, d, rra.RRA_BF16)
+    off = (ctypes.c_size_t * 6)()
+    assert L.rra_workspace_offsets(B, N, H, d, rra.RRA_BF16, off) == rra.RRA_OK
+    off = list(off)
+    assert off[0] == 0 and all(o % 256 == 0 for o in off)
+    assert off[1] >= (B + 1) * 4 and off[2] - off[1] >= B * N * 4 and off[3] - off[2] >= B * N * 4
+    packed = B * N * H * d * 2
+    assert off[4] - off[3] >= packed and off[5] - off[4] >= packed and n - off[5] >= packed
+    assert L.rra_workspace_bytes(B, N, H, 32, rra.RRA_BF16) == 0
+    assert L.rra_workspace_bytes(B, 2000, H, d, rra.RRA_BF16) == 0
+    assert L.rra_workspace_bytes(B, N, H, d, rra.RRA_F32) == 0     # fp32 inputs unsupported
+
+
+def _attend(L, **kw):
+    a = dict(qp=0x1000, kp=0x2000, vp=0x3000, cu=0x4000, B=2, S=197, H=6, d=64, scale=0.125,
+             ind=rra.RRA_BF16, o=0x5000, outd=rra.RRA_BF16, src=None, N=197, stream=None)
+    a.update(kw)
+    return L.rra_attend(a["qp"], a["kp"], a["vp"], a["cu"], a["B"], a["S"], a["H"], a["d"], a["scale"],
+                        a["ind"], a["o"], a["outd"], a["src"], a["N"], a["stream"])
+
+
+def test_host_side_errors(L):
+    assert _attend(L, d=32) == rra.RRA_ERR_UNSUPPORTED
+    assert _attend(L, S=1025) == rra.RRA_ERR_UNSUPPORTED
+    assert _attend(L, B=0) == rra.RRA_ERR_INVALID_ARG
+    assert _attend(L, H=0) == rra.RRA_ERR_INVALID_ARG
+    assert _attend(L, qp=None) == rra.RRA_ERR_INVALID_ARG
+    assert _attend(L, cu=None) == rra.RRA_ERR_INVALID_ARG
+    assert _attend(L, kp=0x2008) == rra.RRA_ERR_MISALIGNED
+    assert _attend(L, o=0x5004) == rra.RRA_ERR_MISALIGNED
+    assert b"not 16-byte aligned" in L.rra_last_error_message()
+    assert _attend(L, ind=rra.RRA_F32) == rra.RRA_ERR_INVALID_ARG
+    assert _attend(L, outd=7) == rra.RRA_ERR_INVALID_ARG
+    assert _attend(L, scale=float("nan")) == rra.RRA_ERR_INVALID_ARG
+    st = L.rra_pipeline(0x100, 0x1000, 0x2000, 0x3000, 2, 197, 6, 64, 0.125, rra.RRA_BF16, 0x5000,
+                        rra.RRA_BF16, 0x6000, 16, None)
+    assert st == rra.RRA_ERR_INVALID_ARG and b"workspace" in L.rra_last_error_message()
+    st = L.rra_pack(None, 2, 197, 6, 64, rra.RRA_BF16, 0x1000, 0x2000, 0x3000, 0x100, 0x200, 0x300,
+                    0x1000, 0x2000, 0x3000, None, rra.RRA_BF16, None)
+    assert st == rra.RRA_ERR_INVALID_ARG
+    st = L.rra_unpack(0x1000, 0x100, 2, 197, 6, 64, rra.RRA_BF16, 0x1001, None)
+    assert st == rra.RRA_ERR_MISALIGNED
+    plan = ctypes.c_void_p()
+    st = L.rra_plan_create(0x100, 0x1000, 0x2000, 0x3000, 2, 197, 6, 48, 0.125, rra.RRA_BF16, 0x5000,
+                           rra.RRA_BF16, 0x6000, 1 << 30, ctypes.byref(plan))
+    assert st == rra.RRA_ERR_UNSUPPORTED and not plan.value
+    assert L.rra_plan_launch(None, None) == rra.RRA_ERR_INVALID_ARG
+    L.rra_plan_destroy(None)
+    buf = (ctypes.c_double * 1)()
+    assert L.rra_time_null_host(None, 0, 0, buf) == rra.RRA_ERR_INVALID_ARG
+
+
+def test_status_strings(L):
+    for s, name in enumerate(["RRA_OK", "RRA_ERR_INVALID_ARG", "RRA_ERR_UNSUPPORTED", "RRA_ERR_MISALIGNED",
+                              "RRA_ERR_CUDA", "RRA_ERR_DEVICE"]):
+        assert L.rra_status_string(s).decode() == name

@@ -1,0 +1,268 @@
+"""CUDA path vs the CPU oracle on the same seeded inputs (needs a GPU).
+
+Bit-exact: cu_seqlens, dst_idx, src_idx, packed Q/K/V, pruned output rows
+(+0), a one-token image's output (= its V), unpack, NaN-poisoned pruned rows,
+repeat runs and batch permutations.  Attention outputs: max-abs <= 2e-3 in
+fp32-output mode, plus half an output ulp when stored as bf16/fp16.
+Every workload runs at its full size in the pipeline's own launch
+configuration; the oracle is cheap enough to compute every output.
+"""
+from __future__ import annotations
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import ATOL, SCALE, bits, check_indices_and_packing, check_output, oracle_result, run_pipeline
+from ragged_attention_token_gb300 import rra
+from ragged_attention_token_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+_PROGRESSIVE_MASKS = None
+
+
+def _progressive(layer):
+    global _PROGRESSIVE_MASKS
+    if _PROGRESSIVE_MASKS is None:
+        _PROGRESSIVE_MASKS = W.progressive_masks()
+    return W.make_progressive_layer(layer, _PROGRESSIVE_MASKS)
+
+
+CASES = (
+    [("tiny", lambda: W.make_tiny())]
+    + [(f"serving_B{B}", (lambda B=B: W.make_serving(B))) for B in W.SERVING_BATCHES]
+    + [(f"batched_p{int(p * 100)}", (lambda p=p: W.make_batched(p))) for p in W.BATCHED_RATES]
+    + [(f"hires_p{int(p * 100)}", (lambda p=p: W.make_hires(p))) for p in W.HIRES_RATES]
+    + [(f"progressive_L{L}", (lambda L=L: _progressive(L))) for L in range(1, 13)]
+)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _lib():
+    assert torch.cuda.is_available()
+    rra.lib()
+    rra.get_device_error(clear=True)
+
+
+@pytest.mark.parametrize("name,make", CASES, ids=[c[0] for c in CASES])
+def test_pipeline_full_size(name, make):
+    case = make()
+    ref = oracle_result(case)
+    keep = case.keep.numpy()
+    for out_dtype in (case.dtype, torch.float32):
+        got = run_pipeline(case, out_dtype)
+        assert got["err"] == 0
+        check_indices_and_packing(got, ref)
+        err = check_output(got["out"], keep, ref["out"])
+        if out_dtype == torch.float32:
+            assert err <= ATOL
+        print(f"{name} out={out_dtype} max_abs_err={err:.3e}")
+
+
+def _edge_cases():
+    C = W.make_custom
+    return [
+        ("B1_one_token", lambda: C(1, 197, 6, [1])),
+        ("empty_images", lambda: C(3, 197, 6, [0, 5, 0])),
+        ("all_empty", lambda: C(2, 50, 3, [0, 0])),
+        ("N1", lambda: C(3, 1, 4, [1, 0, 1])),
+        ("N63_all", lambda: C(2, 63, 3, [63, 63])),
+        ("N64_all", lambda: C(2, 64, 3, [64, 64])),
+        ("N65_all", lambda: C(2, 65, 3, [65, 65])),
+        ("N127_mixed", lambda: C(3, 127, 2, [127, 64, 1])),
+        ("N128_all", lambda: C(1, 128, 2, [128])),
+        ("N129_mixed", lambda: C(2, 129, 2, [129, 65])),
+        ("N1024_max", lambda: C(2, 1024, 2, [1024, 777])),
+        ("no_cls_random", lambda: C(5, 197, 3, [20, 197, 0, 100, 1], cls=False)),
+        ("bernoulli_half", lambda: C(7, 300, 3, None, random_mask=True)),
+        ("large_logits_x8", lambda: C(4, 197, 6, [197, 100, 39, 2], value_scale=8.0)),
+        ("fp16_ragged", lambda: C(4, 197, 3, [197, 60, 7, 1], dtype=torch.float16)),
+        ("fp16_large_logits", lambda: C(2, 577, 2, [577, 300], dtype=torch.float16, value_scale=4.0)),
+        ("H1", lambda: C(9, 97, 1, [97, 1, 2, 3, 50, 0, 64, 65, 96])),
+    ]
+
+
+EDGE = _edge_cases()
+
+
+@pytest.mark.parametrize("name,make", EDGE, ids=[e[0] for e in EDGE])
+def test_pipeline_edge_cases(name, make):
+    case = make()
+    ref = oracle_result(case)
+    keep = case.keep.numpy()
+    for out_dtype in (case.dtype, torch.float32):
+        got = run_pipeline(case, out_dtype)
+        assert got["err"] == 0
+        check_indices_and_packing(got, ref)
+        check_output(got["out"], keep, ref["out"])
+
+
+def test_single_token_returns_v_bit_exact():
+    case = W.make_custom(4, 197, 6, [1, 1, 1, 1])
+    got = run_pipeline(case)
+    m = case.keep.numpy() != 0
+    assert np.array_equal(bits(got["out"])[m], bits(case.v)[m])
+    got32 = run_pipeline(case, torch.float32)
+    assert np.array_equal(got32["out"].numpy()[m], case.v.float().numpy()[m])
+
+
+def test_nan_in_pruned_rows_changes_nothing():
+    case = W.make_batched(0.8)
+    clean = run_pipeline(case)
+    pruned = (case.keep == 0)[:, :, None, None]
+    for x in (case.q, case.k, case.v):
+        x.masked_fill_(pruned, float("nan"))
+    dirty = run_pipeline(case)
+    assert np.array_equal(bits(clean["out"]), bits(dirty["out"]))
+
+
+def test_repeat_runs_and_batch_permutation_bit_exact():
+    case = W.make_batched(0.5)
+    a = run_pipeline(case)
+    b = run_pipeline(case)
+    assert np.array_equal(bits(a["out"]), bits(b["out"]))
+    perm = torch.randperm(case.B, generator=torch.Generator().manual_seed(5))
+    case2 = W.Case(case.name + "_perm", case.B, case.N, case.H, case.d, case.dtype, case.keep[perm].clone(),
+                   case.q[perm].clone(), case.k[perm].clone(), case.v[perm].clone(), case.seed)
+    c = run_pipeline(case2)
+    assert np.array_equal(bits(a["out"])[perm.numpy()], bits(c["out"]))
+
+
+def _packed_inputs(case):
+    ref = oracle_result(case)
+    B, N, H, d = case.B, case.N, case.H, case.d
+    cap = B * N
+    qp, kp, vp = (torch.empty((cap, H, d), dtype=case.dtype, device="cuda") for _ in range(3))
+    for t, r in zip((qp, kp, vp), ref["packed_bits"]):
+        t.view(torch.uint8).fill_(0xFF)
+        t[: len(ref["src"])].view(torch.int16).copy_(torch.from_numpy(r))
+    cu = torch.from_numpy(ref["cu"]).to("cuda")
+    return ref, qp, kp, vp, cu
+
+
+@pytest.mark.parametrize("make", [lambda: W.make_tiny(), lambda: W.make_hires(0.5)], ids=["tiny", "hires_p50"])
+def test_attend_packed_output_and_unpack(make):
+    case = make()
+    ref, qp, kp, vp, cu = _packed_inputs(case)
+    B, N, H, d = case.B, case.N, case.H, case.d
+    T = len(ref["src"])
+    o = torch.full((B * N, H, d), float("nan"), dtype=torch.float32, device="cuda")
+    rra.attend(qp, kp, vp, cu, B, N, o, scale=SCALE)
+    torch.cuda.synchronize()
+    assert rra.get_device_error() == 0
+    err = np.abs(o[:T].cpu().double().numpy() - ref["o"]).max()
+    assert err <= ATOL
+    assert torch.isnan(o[T:]).all()                       # rows >= T untouched
+    # unpack is a bit copy of the packed rows plus +0 at pruned positions
+    ob = o.to(case.dtype)
+    dst = torch.from_numpy(ref["dst"]).to("cuda")
+    out = torch.full((B, N, H, d), float("nan"), dtype=case.dtype, device="cuda")
+    rra.unpack(ob, dst, B, N, out)
+    torch.cuda.synchronize()
+    assert rra.get_device_error() == 0
+    want = oracle.unpack(bits(ob), ref["dst"], B, N)
+    assert np.array_equal(bits(out), want)
+
+
+def test_pack_standalone_leaves_rows_beyond_T():
+    case = W.make_serving(2)
+    ref = oracle_result(case)
+    keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
+    B, N, H, d = case.B, case.N, case.H, case.d
+    cu = torch.empty(B + 1, dtype=torch.int32, device="cuda")
+    dst = torch.empty(B * N, dtype=torch.int32, device="cuda")
+    src = torch.full((B * N,), -7, dtype=torch.int32, device="cuda")
+    qp, kp, vp = (torch.empty((B * N, H, d), dtype=case.dtype, device="cuda") for _ in range(3))
+    rra.pack(keep, q, k, v, cu, dst, src, qp, kp, vp)
+    torch.cuda.synchronize()
+    T = len(ref["src"])
+    assert np.array_equal(cu.cpu().numpy(), ref["cu"])
+    assert np.array_equal(dst.cpu().numpy(), ref["dst"])
+    assert np.array_equal(src.cpu().numpy()[:T], ref["src"])
+    assert (src[T:] == -7).all()                          # beyond T untouched
+
+
+def test_mask_values_any_nonzero_keeps():
+    case = W.make_serving(4)
+    ref = oracle_result(case)
+    mult = torch.randint(1, 256, case.keep.shape, generator=torch.Generator().manual_seed(3), dtype=torch.int32)
+    case.keep = (case.keep.to(torch.int32) * mult).to(torch.uint8)
+    assert ((case.keep != 0).numpy() == (ref["dst"].reshape(case.B, case.N) >= 0)).all()
+    got = run_pipeline(case)
+    check_indices_and_packing(got, ref)
+
+
+def test_device_error_codes():
+    case = W.make_serving(2)
+    ref, qp, kp, vp, cu = _packed_inputs(case)
+    B, N, H, d = case.B, case.N, case.H, case.d
+    o = torch.zeros((B * N, H, d), dtype=torch.float32, device="cuda")
+    rra.get_device_error(clear=True)
+    n0 = int(ref["cu"][1])
+    rra.attend(qp, kp, vp, cu, B, n0 - 1, o, scale=SCALE)      # max_seqlen below a real length
+    torch.cuda.synchronize()
+    assert rra.get_device_error(clear=True) == rra.DEVERR_SEQ_TOO_LONG
+    assert rra.get_device_error() == 0
+    bad = torch.tensor([0, 10, 5], dtype=torch.int32, device="cuda")
+    rra.attend(qp, kp, vp, bad, B, N, o, scale=SCALE)
+    torch.cuda.synchronize()
+    assert rra.get_device_error(clear=True) == rra.DEVERR_SEQ_NEGATIVE
+    src = torch.full((B * N,), B * N + 5, dtype=torch.int32, device="cuda")
+    out = torch.zeros((B, N, H, d), dtype=torch.float32, device="cuda")
+    rra.attend(qp, kp, vp, cu, B, N, out, scale=SCALE, src_idx=src, N=N)
+    torch.cuda.synchronize()
+    assert rra.get_device_error(clear=True) == rra.DEVERR_INDEX_RANGE
+    assert (out == 0).all()
+    got = run_pipeline(case)                                    # a later good call reports nothing
+    assert got["err"] == 0
+
+
+def test_graph_plan_and_host_pipeline_match_direct():
+    case = W.make_serving(4)
+    keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
+    B, N, H, d = case.B, case.N, case.H, case.d
+    direct, _ = rra.run_pipeline(keep, q, k, v, scale=SCALE)
+    out = torch.empty_like(q)
+    ws = rra.alloc_workspace(B, N, H, d, case.dtype)
+    plan = rra.Plan(keep, q, k, v, out, ws, scale=SCALE)
+    out.zero_()
+    n0 = rra.launch_count()
+    plan.launch()
+    plan.launch()
+    torch.cuda.synchronize()
+    assert rra.launch_count() - n0 == 4
+    assert torch.equal(out.view(torch.int16), direct.view(torch.int16))
+    samples = plan.time_host(2, 5)
+    assert all(s > 0 for s in samples)
+    plan.close()
+    keep_h, q_h, k_h, v_h = (x.pin_memory() for x in (case.keep, case.q, case.k, case.v))
+    out_h = torch.empty(q.shape, dtype=q.dtype).pin_memory()
+    bufs = [torch.empty_like(x) for x in (keep, q, k, v)]
+    out_d = torch.empty_like(q)
+    rra.pipeline_host(keep_h, q_h, k_h, v_h, out_h, *bufs, out_d, ws, scale=SCALE)
+    torch.cuda.synchronize()
+    assert torch.equal(out_h.view(torch.int16), direct.cpu().view(torch.int16))
+
+
+def test_host_timed_helpers():
+    case = W.make_serving(1)
+    ref, qp, kp, vp, cu = _packed_inputs(case)
+    o = torch.empty_like(qp)
+    s = rra.time_attend_host(qp, kp, vp, cu, case.B, case.N, o, warmup=5, reps=20)
+    assert len(s) == 20 and all(x > 0 for x in s)
+    torch.cuda.synchronize()
+    T = len(ref["src"])
+    err = np.abs(o[:T].cpu().double().numpy() - ref["o"]).max()
+    assert err <= ATOL + 2 ** -8
+    z = rra.time_null_host(5, 20)
+    assert len(z) == 20 and all(x > 0 for x in z)
+
+
+def test_launch_count_counts_kernels():
+    case = W.make_tiny()
+    keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
+    n0 = rra.launch_count()
+    rra.run_pipeline(keep, q, k, v)
+    assert rra.launch_count() - n0 == 2
