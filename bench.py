@@ -1,0 +1,563 @@
+"""Benchmark of the pack -> ragged attention -> unpack path on one or more GPUs.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl rra|reference]
+                    [--workload serving|tiny|batched|hires] [--sweep]
+
+One step = one pass of the whole path (pack, then attention with the unpack
+fused into its epilogue) over one batch of the workload.  Default workload:
+the serving case, DeiT-S-shaped B=4, N=197, H=6, d=64, bf16, 80% of patches
+pruned (39 +- 4 tokens per image).  Inputs are seeded synthetic data resident
+in HBM; R copies of the input set rotate so that their total size exceeds L2
+and every step reads cold inputs.
+
+Printed (rank 0, one JSON line): kept tokens/s of the path (value), the
+host-timed latency of one rra_attend call at BS=1/2/4, end-to-end tokens/s
+from pinned host buffers through rra_pipeline_host, the dominant kernel's
+roofline fraction, the CPU oracle's throughput on a bounded sample, SM clocks
+sampled during the run and the number of kernel launches.
+
+--impl reference times the CPU oracle (the only reference implementation:
+the pages ship no code) on the same workload and prints the same line shape.
+Under torchrun every rank runs its own replica (images are independent, so
+the work partitions with no collective); rank 0 prints the aggregate.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+os.environ.setdefault("OPENBLAS_NUM_THREADS", "1")
+os.environ.setdefault("OMP_NUM_THREADS", "1")
+os.environ.setdefault("MKL_NUM_THREADS", "1")
+
+import torch  # noqa: E402
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from ragged_attention_token_gb300 import workloads as W  # noqa: E402
+
+METRIC = "ragged attend µs @BS1-4 (host-timed); pack-attend-unpack tokens/s; % roofline"
+UNIT = "tokens/s"
+SCALE = 0.125
+L2_BYTES = 129 * 1024 * 1024
+
+
+# ----------------------------------------------------------------- workloads
+
+def make_case(name: str):
+    if name == "serving":
+        return W.make_serving(4), "serving DeiT-S: B=4, N=197, H=6, d=64, bf16, 80% pruned (39+-4 tokens/image)"
+    if name == "tiny":
+        return W.make_tiny(), "tiny DeiT-T: B=2, N=197, H=3, d=64, fp16, keep rate ~U[0.2,1]"
+    if name == "batched":
+        return W.make_batched(0.8), "batched DeiT-B: B=64, N=197, H=12, d=64, bf16, 80% pruned +-10%"
+    if name == "hires":
+        return W.make_hires(0.5), "high-res DeiT-B 384px: B=32, N=577, H=12, d=64, bf16, 50% pruned +-10%"
+    raise ValueError(name)
+
+
+def case_bytes(case, out_bytes_per_el=None):
+    """Algorithmic bytes per launch (attend, pack, fused minimum) and attention FLOPs."""
+    B, N, H, d = case.B, case.N, case.H, case.d
+    s = case.q.element_size()
+    so = out_bytes_per_el or s
+    T = case.kept_tokens
+    return dict(
+        attend=3 * T * H * d * s + T * H * d * so,
+        pack=B * N + 2 * 3 * T * H * d * s + (B * N - T) * H * d * so + 4 * (B + 1) + 4 * B * N + 4 * T,
+        fused_min=B * N + 3 * T * H * d * s + B * N * H * d * so + 12 * B * N,
+        flops=4 * H * d * sum(n * n for n in case.lengths),
+    )
+
+
+# ------------------------------------------------------------------ peaks
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return dict(hbm_gbs=float(p["hbm_gbs"]), bf16_tflops=float(p["bf16_tflops"]),
+                    bf16_tflops_sustained=float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    source="measured")
+    except Exception:
+        return dict(hbm_gbs=6800.0, bf16_tflops=1900.0, bf16_tflops_sustained=1700.0, source="fallback")
+
+
+# ------------------------------------------------------------------ clocks
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        self.gpu = gpu_index
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+        self.t_start = time.time()
+
+    def stop(self):
+        self.t_stop = time.time()
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out, _ = self.proc.communicate()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for line in out.strip().splitlines():
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for nm, val in zip(names, parts[5:9]):
+                if val.lower() == "active":
+                    reasons.add(nm)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "window_s": round(self.t_stop - self.t_start, 2)}
+
+
+# -------------------------------------------------------------- GPU helpers
+
+class InputSets:
+    """R device copies of one seeded input set (rotated to defeat L2 reuse)."""
+
+    def __init__(self, case, device, rra, out_dtype, R=None):
+        B, N, H, d = case.B, case.N, case.H, case.d
+        base = [x.to(device) for x in (case.keep, case.q, case.k, case.v)]
+        ws_bytes = rra.workspace_bytes(B, N, H, d, case.dtype)
+        per_set = sum(x.numel() * x.element_size() for x in base) + ws_bytes + \
+            B * N * H * d * torch.empty((), dtype=out_dtype).element_size()
+        if R is None:
+            R = max(2, min(512, math.ceil(2 * L2_BYTES / per_set)))
+        self.R = R
+        self.per_set = per_set
+        self.sets = []
+        for _ in range(R):
+            keep, q, k, v = (x.clone() for x in base)
+            out = torch.empty((B, N, H, d), dtype=out_dtype, device=device)
+            ws = torch.empty(ws_bytes, dtype=torch.uint8, device=device)
+            self.sets.append((keep, q, k, v, out, ws))
+
+
+def capture(fn_list, stream):
+    """A CUDA graph of the launches in fn_list, captured on `stream` (after one eager pass)."""
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.stream(stream):
+        for fn in fn_list:
+            fn()
+        stream.synchronize()
+        with torch.cuda.graph(g, stream=stream):
+            for fn in fn_list:
+                fn()
+    stream.synchronize()
+    return g
+
+
+def graph_time_per_launch(fn_list, stream, reps=5):
+    """Median device µs per launch of a CUDA graph of back-to-back launches.
+
+    The graph is replayed on the same stream the events are recorded on."""
+    g = capture(fn_list, stream)
+    times = []
+    with torch.cuda.stream(stream):
+        g.replay()
+        for _ in range(reps):
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            times.append(e0.elapsed_time(e1) * 1e3 / len(fn_list))
+    del g
+    return statistics.median(times)
+
+
+def kernel_times(case, sets, rra, stream, n_launch=None):
+    """Per-launch device µs of the pack kernel and the attention kernel (cold inputs)."""
+    B, N, H, d = case.B, case.N, case.H, case.d
+    R = sets.R
+    n_launch = n_launch or max(R, 64)
+    views = [rra.workspace_views(s[5], B, N, H, d, case.dtype) for s in sets.sets]
+
+    def pack_fn(i):
+        keep, q, k, v, out, ws = sets.sets[i % R]
+        cu, dst, src, qp, kp, vp = views[i % R]
+        return lambda: rra.pack(keep, q, k, v, cu, dst, src, qp, kp, vp, out, stream=stream)
+
+    def attend_fn(i):
+        keep, q, k, v, out, ws = sets.sets[i % R]
+        cu, dst, src, qp, kp, vp = views[i % R]
+        return lambda: rra.attend(qp, kp, vp, cu, B, N, out, scale=SCALE, src_idx=src, N=N, stream=stream)
+
+    t_pack = graph_time_per_launch([pack_fn(i) for i in range(n_launch)], stream)
+    t_attend = graph_time_per_launch([attend_fn(i) for i in range(n_launch)], stream)
+    return t_pack, t_attend
+
+
+def roofline_obj(bytes_alg, flops, us, peaks):
+    t = us * 1e-6
+    bw = bytes_alg / t / 1e9
+    tf = flops / t / 1e12
+    hbm_frac = bw / peaks["hbm_gbs"]
+    ten_frac = tf / peaks["bf16_tflops"]
+    if ten_frac > hbm_frac:
+        return {"bound": "tensor", "achieved": round(tf, 2), "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                "frac": round(ten_frac, 4), "traffic": None}
+    return {"bound": "hbm", "achieved": round(bw, 1), "peak": peaks["hbm_gbs"], "unit": "GB/s",
+            "frac": round(hbm_frac, 4), "traffic": None}
+
+
+def host_latency(rra, B, stream, reps=1000, warmup=100):
+    """Median host-timed µs of one rra_attend (+ stream sync) at serving batch B."""
+    case = W.make_serving(B)
+    keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
+    out, ws = rra.run_pipeline(keep, q, k, v, scale=SCALE)
+    cu, dst, src, qp, kp, vp = rra.workspace_views(ws, B, case.N, case.H, case.d, case.dtype)
+    torch.cuda.synchronize()
+    c_samples = rra.time_attend_host(qp, kp, vp, cu, B, case.N, out, warmup=warmup, reps=reps, src_idx=src,
+                                     N=case.N, stream=stream)
+    py = []
+    for i in range(warmup + reps):
+        t0 = time.perf_counter()
+        rra.attend(qp, kp, vp, cu, B, case.N, out, scale=SCALE, src_idx=src, N=case.N, stream=stream)
+        stream.synchronize()
+        t1 = time.perf_counter()
+        if i >= warmup:
+            py.append((t1 - t0) * 1e6)
+    plan = rra.Plan(keep, q, k, v, out, ws, scale=SCALE)
+    g_samples = plan.time_host(warmup, reps, stream=stream)
+    plan.close()
+    null = rra.time_null_host(warmup, reps, stream=stream)
+    return {"attend_c": round(statistics.median(c_samples), 2),
+            "attend_python": round(statistics.median(py), 2),
+            "pipeline_graph_c": round(statistics.median(g_samples), 2),
+            "null_kernel_c": round(statistics.median(null), 2)}
+
+
+# ----------------------------------------------------------------- CPU side
+
+def oracle_tokens_per_s(case, budget_s=10.0):
+    """The CPU oracle (as it stands) on the workload: kept tokens/s on this host."""
+    import oracle
+    keep = case.keep.numpy()
+    q, k, v = (x.double().numpy() for x in (case.q, case.k, case.v))
+    T = case.kept_tokens
+    steps = 0
+    t0 = time.perf_counter()
+    while True:
+        oracle.pipeline(keep, q, k, v, SCALE)
+        steps += 1
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            break
+    return T * steps / el, steps, el
+
+
+CPU_THREADS = 1   # single-threaded Python loops; BLAS pinned to one thread above
+
+
+# -------------------------------------------------------------------- main
+
+def dist_setup(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        backend = "nccl" if (args.impl == "rra" and torch.cuda.is_available()) else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend=backend)
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x, world, device):
+    if world == 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return 0
+    case, desc = make_case(args.workload)
+    import oracle
+    keep = case.keep.numpy()
+    q, k, v = (x.double().numpy() for x in (case.q, case.k, case.v))
+    T = case.kept_tokens
+    t0 = time.perf_counter()
+    oracle.pipeline(keep, q, k, v, SCALE)
+    t_one = time.perf_counter() - t0
+    steps = max(1, min(args.steps, int(120.0 / max(t_one, 1e-6))))   # about two minutes at most
+    warm = max(0, min(args.warmup, steps))
+    for _ in range(warm):
+        oracle.pipeline(keep, q, k, v, SCALE)
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        oracle.pipeline(keep, q, k, v, SCALE)
+    el = time.perf_counter() - t0
+    value = T * steps / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": args.gpus,
+        "steps": steps, "warmup": warm, "ms_per_step": round(el / steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": desc, "B": case.B, "N": case.N, "H": case.H, "d": case.d,
+                   "kept_tokens_per_step": T},
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": CPU_THREADS, "kind": "oracle",
+                         "sample": f"{steps} full steps of the workload (steps capped at ~2 min of CPU)"},
+        "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+        "gpu_launches": 0,
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+def run_rra(args, world, rank, local):
+    from ragged_attention_token_gb300 import build as _build
+    if not _build.up_to_date():
+        if rank == 0:
+            _build.build()
+        barrier(world)
+    from ragged_attention_token_gb300 import rra
+
+    device = torch.device("cuda", local)
+    torch.cuda.set_device(device)
+    rra.lib()
+    stream = torch.cuda.Stream(device=device)
+    peaks = measured_peaks()
+    case, desc = make_case(args.workload)
+    B, N, H, d = case.B, case.N, case.H, case.d
+    T = case.kept_tokens
+    sets = InputSets(case, device, rra, case.dtype)
+    plans = [rra.Plan(*s, scale=SCALE) for s in sets.sets]
+    launches_per_step = 2
+
+    # The timed steps replay CUDA graphs that each hold R consecutive steps
+    # (one per rotating input set): the host dispatches once per R steps.
+    def step_fn(s):
+        return lambda: rra.pipeline(*s[:5], s[5], scale=SCALE, stream=stream)
+    q_full, rem = divmod(args.steps, sets.R)
+    n_cap0 = rra.launch_count()
+    g_full = capture([step_fn(s) for s in sets.sets], stream)
+    per_full = (rra.launch_count() - n_cap0) // 2            # eager pass + capture each count once
+    g_rem, per_rem = None, 0
+    if rem:
+        n_cap0 = rra.launch_count()
+        g_rem = capture([step_fn(s) for s in sets.sets[:rem]], stream)
+        per_rem = (rra.launch_count() - n_cap0) // 2
+
+    sampler = ClockSampler(device.index if device.index is not None else 0)
+    sampler.start()
+    with torch.cuda.stream(stream):
+        for i in range(max(3, args.warmup)):
+            plans[i % sets.R].launch(stream)
+        stream.synchronize()
+        # identical load for a while so the clock samples describe the timed region
+        t_end = time.time() + args.clock_window
+        while time.time() < t_end:
+            for _ in range(8):
+                g_full.replay()
+            stream.synchronize()
+
+        barrier(world)
+        torch.cuda.synchronize(device)
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        for _ in range(q_full):
+            g_full.replay()
+        if g_rem is not None:
+            g_rem.replay()
+        e1.record(stream)
+        e1.synchronize()
+        torch.cuda.synchronize(device)
+        barrier(world)
+        launches = q_full * per_full + per_rem
+
+        # the same steps dispatched one call at a time (one graph launch per step)
+        e4 = torch.cuda.Event(enable_timing=True)
+        e5 = torch.cuda.Event(enable_timing=True)
+        e4.record(stream)
+        for i in range(args.steps):
+            plans[i % sets.R].launch(stream)
+        e5.record(stream)
+        e5.synchronize()
+    clocks = sampler.stop()
+    el_ms = max_over_ranks(e0.elapsed_time(e1), world, device)
+    value = T * args.steps * world / (el_ms * 1e-3)
+    per_call_ms = max_over_ranks(e4.elapsed_time(e5), world, device)
+    per_call_value = T * args.steps * world / (per_call_ms * 1e-3)
+
+    # e2e: pinned host inputs -> device -> path -> host output, every step
+    keep_h, q_h, k_h, v_h = (x.pin_memory() for x in (case.keep, case.q, case.k, case.v))
+    out_h = torch.empty((B, N, H, d), dtype=case.dtype).pin_memory()
+    keep_d, q_d, k_d, v_d, out_d, ws_d = sets.sets[0]
+    h2d = sum(x.numel() * x.element_size() for x in (keep_h, q_h, k_h, v_h))
+    d2h = out_h.numel() * out_h.element_size()
+    with torch.cuda.stream(stream):
+        for _ in range(max(3, args.warmup)):
+            rra.pipeline_host(keep_h, q_h, k_h, v_h, out_h, keep_d, q_d, k_d, v_d, out_d, ws_d, SCALE, stream)
+        stream.synchronize()
+        barrier(world)
+        e2 = torch.cuda.Event(enable_timing=True)
+        e3 = torch.cuda.Event(enable_timing=True)
+        e2.record(stream)
+        for _ in range(args.steps):
+            rra.pipeline_host(keep_h, q_h, k_h, v_h, out_h, keep_d, q_d, k_d, v_d, out_d, ws_d, SCALE, stream)
+        e3.record(stream)
+        e3.synchronize()
+    e2e_ms = max_over_ranks(e2.elapsed_time(e3), world, device)
+    e2e_value = T * args.steps * world / (e2e_ms * 1e-3)
+
+    # per-kernel device time (graph of back-to-back launches on cold inputs)
+    t_pack, t_attend = kernel_times(case, sets, rra, stream)
+    by = case_bytes(case)
+    kern = {"pack_us": round(t_pack, 3), "attend_us": round(t_attend, 3)}
+    if t_attend >= t_pack:
+        dom, roof = "attend", roofline_obj(by["attend"], by["flops"], t_attend, peaks)
+    else:
+        dom, roof = "pack", roofline_obj(by["pack"], 0, t_pack, peaks)
+    roof["kernel"] = dom
+    roof["peak_source"] = peaks["source"]
+
+    extra = {}
+    if rank == 0 and not args.quick:
+        extra["host_us"] = {f"bs{b}": host_latency(rra, b, stream) for b in W.SERVING_BATCHES}
+        big, big_desc = make_case("batched")
+        big_sets = InputSets(big, device, rra, big.dtype)
+        bp, ba = kernel_times(big, big_sets, rra, stream)
+        bb = case_bytes(big)
+        extra["batched_b64_p80"] = {"workload": big_desc, "pack_us": round(bp, 3), "attend_us": round(ba, 3),
+                                    "attend_roofline": roofline_obj(bb["attend"], bb["flops"], ba, peaks),
+                                    "pipeline_tokens_per_s": round(big.kept_tokens / ((bp + ba) * 1e-6), 1)}
+        del big_sets
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        tps, st, el = oracle_tokens_per_s(case, budget_s=args.cpu_budget)
+        cpu = {"value": round(tps, 1), "unit": UNIT, "cores": CPU_THREADS, "kind": "oracle",
+               "sample": f"{st} full steps of the same workload in {el:.1f} s (fp64 numpy, 1 thread)"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": world, "steps": args.steps,
+            "warmup": max(3, args.warmup), "ms_per_step": round(el_ms / args.steps, 5), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if case.dtype == torch.bfloat16 else "f16",
+            "data": "synthetic (seeded N(0,1) Q/K/V, seeded keep masks)",
+            "config": {"workload": desc, "B": B, "N": N, "H": H, "d": d, "kept_tokens_per_step": T,
+                       "path": f"CUDA graphs of {sets.R} pipeline steps (pack + attention with fused unpack), "
+                               "replayed back to back",
+                       "l2": f"{sets.R} rotating input sets of {sets.per_set / 2**20:.1f} MiB "
+                             f"({sets.R * sets.per_set / 2**20:.0f} MiB > L2)",
+                       "parallelism": f"replicas x{world}"},
+            "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                    "path": "rra_pipeline_host (pinned H2D, pack, attend, D2H)"},
+            "roofline": roof,
+            "kernels": kern,
+            "cpu_baseline": cpu,
+            "clocks": clocks,
+            "gpu_launches": int(launches) * world,
+            "launches_per_step": launches_per_step,
+            "per_call_dispatch": {"value": round(per_call_value, 1), "unit": UNIT,
+                                  "ms_per_step": round(per_call_ms / args.steps, 5),
+                                  "path": "one rra_plan_launch (graph of 2 kernels) per step from Python"},
+        }
+        line.update(extra)
+        print(json.dumps(line), flush=True)
+    for p in plans:
+        p.close()
+    return 0
+
+
+def run_sweep(args):
+    """Every workload: device µs per kernel, path tokens/s, roofline (one JSON line each)."""
+    from ragged_attention_token_gb300 import build as _build
+    _build.build()
+    from ragged_attention_token_gb300 import rra
+    device = torch.device("cuda", 0)
+    stream = torch.cuda.Stream(device=device)
+    peaks = measured_peaks()
+    cases = [W.make_tiny()] + [W.make_serving(b) for b in W.SERVING_BATCHES] + \
+            [W.make_batched(p) for p in W.BATCHED_RATES] + [W.make_hires(p) for p in W.HIRES_RATES]
+    masks = W.progressive_masks()
+    cases += [W.make_progressive_layer(L, masks) for L in (1, 4, 7, 10)]
+    for case in cases:
+        sets = InputSets(case, device, rra, case.dtype)
+        tp, ta = kernel_times(case, sets, rra, stream)
+        by = case_bytes(case)
+        roof_t = max(by["attend"] / (peaks["hbm_gbs"] * 1e9), by["flops"] / (peaks["bf16_tflops"] * 1e12)) * 1e6
+        fused_t = by["fused_min"] / (peaks["hbm_gbs"] * 1e9) * 1e6
+        print(json.dumps({"case": case.name, "B": case.B, "N": case.N, "H": case.H, "T": case.kept_tokens,
+                          "pack_us": round(tp, 3), "attend_us": round(ta, 3),
+                          "attend_roofline_us": round(roof_t, 3), "attend_frac": round(roof_t / ta, 4),
+                          "attend": roofline_obj(by["attend"], by["flops"], ta, peaks),
+                          "pipeline_us": round(tp + ta, 3), "pipeline_fused_min_us": round(fused_t, 3),
+                          "pipeline_frac_of_fused_min": round(fused_t / (tp + ta), 4),
+                          "tokens_per_s": round(case.kept_tokens / ((tp + ta) * 1e-6), 1)}), flush=True)
+        del sets
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=50)
+    ap.add_argument("--impl", choices=("rra", "reference"), default="rra")
+    ap.add_argument("--workload", default="serving", choices=("serving", "tiny", "batched", "hires"))
+    ap.add_argument("--sweep", action="store_true", help="per-workload kernel timings, one line each")
+    ap.add_argument("--quick", action="store_true", help="skip host-latency and B=64 extras")
+    ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
+    ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work")
+    ap.add_argument("--clock-window", type=float, default=1.5, help="seconds of load before the timed region")
+    args = ap.parse_args(argv)
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        rc = run_reference(args, world, rank)
+    elif args.sweep:
+        rc = run_sweep(args) if rank == 0 else 0
+    else:
+        rc = run_rra(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+    return rc
+
+
+if __name__ == "__main__":
+    sys.exit(main())
