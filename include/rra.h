@@ -27,10 +27,13 @@
  *   - Input dtype is RRA_F16 or RRA_BF16; attention outputs may also be
  *     RRA_F32.  Softmax and both products accumulate in fp32.
  *   - Ownership: the caller allocates and frees every buffer.  The library
- *     allocates no device memory, except the CUDA graph owned by an rra_plan.
+ *     allocates no device memory, except the CUDA graph owned by an rra_plan
+ *     (and the fixed scratch array of rra_pipeline_static, which is part of
+ *     the loaded module).
  *   - Asynchrony: every call only enqueues work on `stream` (a cudaStream_t;
  *     NULL is the legacy default stream).  Nothing synchronises and nothing
- *     is copied device->host, so every call can be captured in a CUDA graph.
+ *     is copied device->host, so the pack / attend / unpack / pipeline calls
+ *     can be captured in a CUDA graph.
  *   - Errors: argument checks run on the host before anything is launched
  *     and return a status with nothing enqueued.  A failed launch returns
  *     RRA_ERR_CUDA.  Inconsistent device-side data (e.g. a cu_seqlens entry
@@ -143,6 +146,32 @@ RRA_API rra_status rra_pipeline_host(const uint8_t* keep_h, const void* q_h, con
                                      rra_dtype in_dtype, void* out_h, rra_dtype out_dtype,
                                      uint8_t* keep_d, void* q_d, void* k_d, void* v_d, void* out_d,
                                      void* workspace, size_t workspace_bytes, void* stream);
+
+/* Size of the scratch array rra_pipeline_static uses on each GPU (64 MiB). */
+#define RRA_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
+
+/* rra_pipeline for callers that cannot allocate device memory.  The paper
+ * has no counterpart to this entry point: it exists for code that may not
+ * call cudaMalloc -- a plugin inside a host that owns all device memory, a
+ * capture region it does not control, or a real-time loop that cannot
+ * afford an allocation's implicit synchronisation -- and so cannot hand
+ * rra_pipeline a workspace.  Same arguments and result as rra_pipeline
+ * without the workspace: the scratch (cu_seqlens, pack indices, packed
+ * Q/K/V) lives in one static device array of RRA_STATIC_SCRATCH_BYTES that
+ * every GPU loading this library holds until the process exits.
+ *   - Allocates nothing and calls no allocating routine.
+ *   - Sizes whose workspace (rra_workspace_bytes) exceeds the array return
+ *     RRA_ERR_UNSUPPORTED with nothing enqueued.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture.
+ *   - All calls share the one array and it keeps the last call's contents
+ *     (nothing in it has to start at zero).  Calls whose work overlaps on
+ *     the GPU -- different streams without ordering between them -- race on
+ *     it; order them on one stream or with events. */
+RRA_API rra_status rra_pipeline_static(const uint8_t* keep, const void* q, const void* k, const void* v,
+                                       int B, int N, int H, int d, float scale, rra_dtype in_dtype,
+                                       void* out, rra_dtype out_dtype, void* stream);
 
 /* A captured CUDA graph of one rra_pipeline call on fixed buffers: the
  * host-dispatch fix (problem section of the article).  rra_plan_create

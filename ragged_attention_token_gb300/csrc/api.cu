@@ -203,6 +203,11 @@ rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaSt
 }
 
 }  // namespace
+
+void set_last_error_message(const char* msg) {
+  snprintf(g_last_message, sizeof(g_last_message), "%s", msg);
+}
+
 }  // namespace rra
 
 using namespace rra;

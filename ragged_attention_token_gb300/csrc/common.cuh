@@ -57,6 +57,9 @@ struct UnpackArgs {
   int32_t* err;
 };
 
+// Sets the message rra_last_error_message() returns on the calling thread.
+void set_last_error_message(const char* msg);
+
 // Launchers (each enqueues exactly one kernel on `stream`).
 cudaError_t launch_pack(const PackArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_attend(const AttendArgs& a, rra_dtype in, rra_dtype out, cudaStream_t stream);

@@ -36,6 +36,7 @@ _SIGNATURES = {
     "rra_attend": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp]),
     "rra_unpack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "rra_pipeline": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
+    "rra_pipeline_static": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "rra_pipeline_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i,
                                _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
     "rra_plan_create": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz,
@@ -163,6 +164,13 @@ def pipeline(keep, q, k, v, out, workspace, scale: float = 0.125, stream=None):
     _check(lib().rra_pipeline(_ptr(keep), _ptr(q), _ptr(k), _ptr(v), B, N, H, d, float(scale),
                               _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], _ptr(workspace),
                               _nbytes(workspace), _stream(stream)))
+
+
+def pipeline_static(keep, q, k, v, out, scale: float = 0.125, stream=None):
+    """rra_pipeline_static: the pipeline with the library's static scratch (no workspace)."""
+    B, N, H, d = q.shape
+    _check(lib().rra_pipeline_static(_ptr(keep), _ptr(q), _ptr(k), _ptr(v), B, N, H, d, float(scale),
+                                     _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], _stream(stream)))
 
 
 def pipeline_host(keep_h, q_h, k_h, v_h, out_h, keep_d, q_d, k_d, v_d, out_d, workspace,
