@@ -110,6 +110,8 @@ RRA_API rra_status rra_pack(const uint8_t* keep, int B, int N, int H, int d, rra
  *   j over [s, e] only (no causal mask).  One kernel launch; the grid is sized
  * from max_seqlen (an upper bound on every image's length) and lengths are
  * read on the device.
+ * qp, kp and vp must span B*max_seqlen rows (the tile loads may read rows
+ * up to that bound past the last image; what they hold is never used).
  *   src_idx == NULL: `o` is packed [cap, H, d] and row i is written at row i.
  *   src_idx != NULL: `o` is padded [B, N, H, d] and row i is written at flat
  *   position src_idx[i] (the unpack fused into the epilogue, bullet 3); rows
@@ -186,6 +188,14 @@ RRA_API rra_status rra_plan_create(const uint8_t* keep, const void* q, const voi
                                    void* workspace, size_t workspace_bytes, rra_plan** plan);
 RRA_API rra_status rra_plan_launch(rra_plan* plan, void* stream);
 RRA_API void rra_plan_destroy(rra_plan* plan);
+
+/* Which kernel rra_attend (and everything built on it) launches; process-
+ * wide, returns the previous choice (or -1 for an unknown value).
+ *   RRA_ATTEND_TCGEN05  (default) TMA tile loads + tcgen05.mma with TMEM
+ *                       accumulators, persistent CTAs;
+ *   RRA_ATTEND_MMA_SYNC warp-level mma.sync kernel, kept for comparison. */
+typedef enum { RRA_ATTEND_TCGEN05 = 0, RRA_ATTEND_MMA_SYNC = 1 } rra_attend_kernel;
+RRA_API int rra_set_attend_kernel(int kernel);
 
 /* Reads (and with clear != 0 resets) the device-side error code of the
  * current device.  Synchronous: call it after the stream has been synced. */

@@ -20,6 +20,7 @@ __global__ void null_kernel() {}
 
 thread_local char g_last_message[256] = "";
 std::atomic<uint64_t> g_launches{0};
+std::atomic<int> g_attend_kernel{RRA_ATTEND_TCGEN05};
 
 rra_status fail(rra_status s, const char* fmt, ...) {
   va_list ap;
@@ -152,7 +153,14 @@ rra_status enqueue_attend(const DeviceState& st, const void* qp, const void* kp,
   a.max_seqlen = max_seqlen;
   a.scale_log2 = scale * 1.4426950408889634f;
   a.err = st.err;
-  cudaError_t e = launch_attend(a, in, out_dt, s);
+  cudaError_t e;
+  if (g_attend_kernel.load() == RRA_ATTEND_TCGEN05) {
+    if (!attend_tc_available())
+      return fail(RRA_ERR_CUDA, "attend: the driver's tensor-map encoder is unavailable");
+    e = launch_attend_tc(a, in, out_dt, st.num_sms, s);
+  } else {
+    e = launch_attend(a, in, out_dt, s);
+  }
   if (e != cudaSuccess) return cuda_fail(e, "attend launch");
   return RRA_OK;
 }
@@ -235,6 +243,11 @@ const char* rra_status_string(rra_status s) {
 const char* rra_last_error_message(void) { return g_last_message; }
 
 uint64_t rra_launch_count(void) { return g_launches.load(); }
+
+int rra_set_attend_kernel(int kernel) {
+  if (kernel != RRA_ATTEND_TCGEN05 && kernel != RRA_ATTEND_MMA_SYNC) return -1;
+  return g_attend_kernel.exchange(kernel);
+}
 
 size_t rra_workspace_bytes(int B, int N, int H, int d, rra_dtype in_dtype) {
   if (check_shape(B, N, H, d) != RRA_OK || !valid_in(in_dtype)) return 0;

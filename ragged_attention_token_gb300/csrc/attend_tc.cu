@@ -1,0 +1,535 @@
+// Bidirectional ragged attention on the packed buffers, sm_103a tensor-core
+// version: TMA tile loads, tcgen05.mma with TMEM accumulators.
+//
+// Follows "Dispatch-Aware Ragged Attention for Pruned Vision Transformers",
+// abstract (non-causal attention over pruned ViT sequences of at most 197 /
+// 577 tokens) and the agents-report.net article, method overview bullet 2
+// (attention computed directly on the compact buffer).
+//
+// Work unit = (image b, head h, tile of 128 query rows).  Persistent CTAs of
+// 128 threads (three per SM) walk the units with a grid stride; a unit whose
+// tile starts past the image's length (read from cu_seqlens on the device)
+// costs two loads and is skipped.  Per unit, keys stream in chunks of 64:
+//
+//   TMA   Q tile (once) and the chunk's K and V rows -> shared memory, in
+//         32-row boxes of the packed [T, H, 64] tensor with the 128-byte
+//         swizzle, so at most 31 rows past the image are fetched;
+//   MMA   S = Q K^T (M=128, N=chunk rounded up to 16, K=64) -> TMEM cols 0..63;
+//   SIMT  thread r owns query row r (TMEM lane r): it reads its S row, takes
+//         the online-softmax max / rescale in base 2, and writes P as two
+//         bf16/fp16 parts (hi = round(p), lo = round(p - hi)) into shared
+//         memory in the swizzled K-major layout the MMA reads;
+//   MMA   O_chunk = P_hi V + P_lo V (M=128, N=64, K=chunk) -> TMEM cols 64..127;
+//   SIMT  O (registers) = O * correction + O_chunk.
+//
+// P is split because one bf16 rounding of the weights alone leaves up to
+// ~2e-3 of output error at these lengths; hi + lo carries ~16 bits.  Keys
+// past the image's end are masked (p = 0) and the V rows the MMA reads past
+// the end are zeroed in shared memory, so whatever the buffer holds there
+// (even NaN) never reaches a kept output.  Every mbarrier wait is bounded
+// by a clock-cycle limit: on expiry the CTA records RRA_DEVERR_WAIT_TIMEOUT,
+// waits (bounded) for its own copies, frees its TMEM and returns.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "common.cuh"
+
+namespace rra {
+namespace {
+
+constexpr int BM = 128;        // query rows per unit (= TMEM lanes)
+constexpr int BN = 64;         // keys per chunk
+constexpr int HD = 64;         // head dim
+constexpr int THREADS = 128;
+constexpr int BOX = 32;        // rows per TMA box
+constexpr int CTAS_PER_SM = 3;
+
+constexpr uint32_t OFF_Q = 0;                        // 128 rows x 128 B
+constexpr uint32_t OFF_K = OFF_Q + BM * 128;         //  64 rows x 128 B
+constexpr uint32_t OFF_V = OFF_K + BN * 128;
+constexpr uint32_t OFF_PH = OFF_V + BN * 128;        // 128 rows x 64 keys x 2 B
+constexpr uint32_t OFF_PL = OFF_PH + BM * 128;
+constexpr uint32_t OFF_BAR = OFF_PL + BM * 128;      // two mbarriers + TMEM address slot
+constexpr uint32_t SMEM_USED = OFF_BAR + 64;
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // slack to align the base to 1024 B
+constexpr uint32_t TMEM_COLS = 128;                  // S: cols [0,64), O: cols [64,128)
+constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
+
+template <typename T> struct IsBf16;
+template <> struct IsBf16<__nv_bfloat16> { static constexpr uint32_t value = 1; };
+template <> struct IsBf16<__half> { static constexpr uint32_t value = 0; };
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+// ------------------------------------------------------------ mbarrier / TMA
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+// Bounded wait for the phase with the given parity; false when the limit passed.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], "
+      "[%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+// ------------------------------------------------------------------ tcgen05
+
+__device__ __forceinline__ void tmem_alloc(uint32_t slot, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(slot), "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+// 16 consecutive fp32 columns of this thread's TMEM lane; the wait is tied to
+// the destination registers so no use is scheduled before it completes.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]),
+                 "+r"(r[7]), "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]),
+                 "+r"(r[14]), "+r"(r[15])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle (layout code 2), sm_100
+// descriptor version 1.  lbo/sbo in bytes.
+__device__ __forceinline__ uint64_t sdesc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= static_cast<uint64_t>((saddr & 0x3FFFFu) >> 4);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= static_cast<uint64_t>(1) << 46;
+  d |= static_cast<uint64_t>(2) << 61;
+  return d;
+}
+
+// Instruction descriptor, kind::f16 with fp32 accumulation.
+__device__ __forceinline__ uint32_t idesc_f16(uint32_t bf16, uint32_t b_mn_major, int M, int N) {
+  return (1u << 4) | (bf16 << 7) | (bf16 << 10) | (b_mn_major << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+template <bool BF16>
+__device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t& lo) {
+  if constexpr (BF16) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(x, y);
+    __nv_bfloat162 l = __floats2bfloat162_rn(x - __low2float(h), y - __high2float(h));
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
+  } else {
+    __half2 h = __floats2half2_rn(x, y);
+    __half2 l = __floats2half2_rn(x - __low2float(h), y - __high2float(h));
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    lo = *reinterpret_cast<uint32_t*>(&l);
+  }
+}
+
+__device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
+  asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
+               : "memory");
+}
+
+template <typename Tout>
+__device__ __forceinline__ void store_row(Tout* dst, const float* o, float inv);
+template <>
+__device__ __forceinline__ void store_row<float>(float* dst, const float* o, float inv) {
+  float4* p = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 16; ++i) p[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
+                                                  o[4 * i + 3] * inv);
+}
+template <>
+__device__ __forceinline__ void store_row<__nv_bfloat16>(__nv_bfloat16* dst, const float* o, float inv) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __nv_bfloat162 t = __floats2bfloat162_rn(o[8 * i + 2 * j] * inv, o[8 * i + 2 * j + 1] * inv);
+      w[j] = *reinterpret_cast<uint32_t*>(&t);
+    }
+    p[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+template <>
+__device__ __forceinline__ void store_row<__half>(__half* dst, const float* o, float inv) {
+  uint4* p = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      __half2 t = __floats2half2_rn(o[8 * i + 2 * j] * inv, o[8 * i + 2 * j + 1] * inv);
+      w[j] = *reinterpret_cast<uint32_t*>(&t);
+    }
+    p[i] = make_uint4(w[0], w[1], w[2], w[3]);
+  }
+}
+
+template <typename Tin, typename Tout, bool SCATTER>
+__global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
+    attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
+                     const __grid_constant__ CUtensorMap tmap_v, const AttendArgs a, int qtiles, int units) {
+  constexpr uint32_t BF = IsBf16<Tin>::value;
+  extern __shared__ uint8_t smem_raw[];
+  const uint32_t raw = smem_u32(smem_raw);
+  const uint32_t base = (raw + 1023u) & ~1023u;
+  uint8_t* gbase = smem_raw + (base - raw);
+  const uint32_t sQ = base + OFF_Q, sK = base + OFF_K, sV = base + OFF_V;
+  const uint32_t sPH = base + OFF_PH, sPL = base + OFF_PL;
+  const uint32_t bar_load = base + OFF_BAR, bar_mma = base + OFF_BAR + 8, slot = base + OFF_BAR + 16;
+  const volatile uint32_t* slot_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + 16);
+
+  const int tid = threadIdx.x, warp = tid >> 5;
+  if (warp == 0) {
+    tmem_alloc(slot, TMEM_COLS);
+    tmem_relinquish();
+  }
+  if (tid == 32) {
+    mbar_init(bar_load, 1);
+    mbar_init(bar_mma, 1);
+    fence_barrier_init();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *slot_ptr;
+  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+  const uint32_t tS = tmem, tO = tmem + 64;
+  const uint32_t idesc_pv = idesc_f16(BF, 1, BM, HD);
+  const int H = a.H;
+
+  uint32_t ph_load = 0, ph_mma = 0;
+  bool load_pending = false, mma_pending = false;
+  bool bad = false;      // this thread saw a wait time out
+  bool abort = false;    // some thread did: the whole CTA stops
+
+  for (int u = blockIdx.x; u < units; u += gridDim.x) {
+    const int qt = u % qtiles;
+    const int bh = u / qtiles;
+    const int h = bh % H;
+    const int b = bh / H;
+    const int s0 = __ldg(a.cu_seqlens + b);
+    const int n = __ldg(a.cu_seqlens + b + 1) - s0;
+    if (n < 0 || n > a.max_seqlen) {
+      if (qt == 0 && h == 0 && tid == 0)
+        record_error(a.err, n < 0 ? RRA_DEVERR_SEQ_NEGATIVE : RRA_DEVERR_SEQ_TOO_LONG);
+      continue;
+    }
+    const int q0 = qt * BM;
+    if (q0 >= n) continue;
+    const int rows_q = min(BM, n - q0);
+    const int nchunks = (n + BN - 1) / BN;
+
+    float o_acc[HD];
+    float m_run = -INFINITY, l_run = 0.f;
+#pragma unroll
+    for (int i = 0; i < HD; ++i) o_acc[i] = 0.f;
+
+    for (int c = 0; c < nchunks; ++c) {
+      const int k0 = c * BN;
+      const int n_c = min(BN, n - k0);
+      const int nk16 = (n_c + 15) & ~15;
+      const int kboxes = (n_c + BOX - 1) / BOX;
+      const int qboxes = (c == 0) ? (rows_q + BOX - 1) / BOX : 0;
+
+      // Everyone is done with shared K/V/P and TMEM S/O from the last chunk.
+      tc_fence_before();
+      if (__syncthreads_or(bad)) { abort = true; break; }
+      if (tid == 0) {
+        tc_fence_after();
+        mbar_expect_tx(bar_load, static_cast<uint32_t>((qboxes + 2 * kboxes) * BOX * 128));
+        for (int j = 0; j < qboxes; ++j) tma_load_3d(sQ + j * BOX * 128, &tmap_q, 0, h, s0 + q0 + j * BOX, bar_load);
+        for (int j = 0; j < kboxes; ++j) {
+          tma_load_3d(sK + j * BOX * 128, &tmap_k, 0, h, s0 + k0 + j * BOX, bar_load);
+          tma_load_3d(sV + j * BOX * 128, &tmap_v, 0, h, s0 + k0 + j * BOX, bar_load);
+        }
+      }
+      load_pending = true;
+      bad |= !mbar_wait(bar_load, ph_load, WAIT_LIMIT_CYCLES);
+      if (!bad) { ph_load ^= 1; load_pending = false; }
+      // V rows [n_c, nk16) enter the MMA with p = 0: make them exact zeros.
+      if (tid < (nk16 - n_c) * 8)
+        st_shared_v4(sV + (n_c + (tid >> 3)) * 128 + (tid & 7) * 16, 0u, 0u, 0u, 0u);
+      fence_proxy_async();
+      if (__syncthreads_or(bad)) { abort = true; break; }
+
+      // S = Q K^T -> TMEM columns [0, nk16)
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idesc_s = idesc_f16(BF, 0, BM, nk16);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK + kk * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
+        umma_commit(bar_mma);
+      }
+      mma_pending = true;
+      bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
+      if (!bad) { ph_mma ^= 1; mma_pending = false; }
+      tc_fence_after();
+
+      // Softmax on this thread's row, reading S from TMEM in 16-column
+      // pieces twice (max, then exponentials) to keep registers low.
+      const float c2 = a.scale_log2;
+      float mx = -INFINITY;
+#pragma unroll
+      for (int g = 0; g < BN / 16; ++g) {
+        if (g * 16 < nk16) {
+          float t[16];
+          tmem_ld16(tS + lane_off + g * 16, t);
+#pragma unroll
+          for (int i = 0; i < 16; ++i)
+            if (g * 16 + i < n_c) mx = fmaxf(mx, t[i] * c2);
+        }
+      }
+      const float m_new = fmaxf(m_run, mx);
+      const float corr = fast_exp2(m_run - m_new);   // 0 on the first chunk
+      l_run *= corr;
+      const int r = tid;
+#pragma unroll
+      for (int g = 0; g < BN / 16; ++g) {
+        if (g * 16 < nk16) {
+          float t[16];
+          tmem_ld16(tS + lane_off + g * 16, t);
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            float p[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int j = g * 16 + half * 8 + i;
+              p[i] = (j < n_c) ? fast_exp2(fmaf(t[half * 8 + i], c2, -m_new)) : 0.f;
+              l_run += p[i];
+            }
+            uint32_t hi[4], lo[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i) split2<BF == 1>(p[2 * i], p[2 * i + 1], hi[i], lo[i]);
+            const int chunk = g * 2 + half;
+            const uint32_t off = r * 128 + ((chunk ^ (r & 7)) << 4);
+            st_shared_v4(sPH + off, hi[0], hi[1], hi[2], hi[3]);
+            st_shared_v4(sPL + off, lo[0], lo[1], lo[2], lo[3]);
+          }
+        }
+      }
+      m_run = m_new;
+      fence_proxy_async();
+      tc_fence_before();
+      if (__syncthreads_or(bad)) { abort = true; break; }
+
+      // O_chunk = P_hi V + P_lo V -> TMEM columns [64, 128)
+      if (tid == 0) {
+        tc_fence_after();
+        const int ksteps = nk16 / 16;
+        for (int kk = 0; kk < ksteps; ++kk)
+          umma_f16(tO, sdesc(sPH + kk * 32, 16, 1024), sdesc(sV + kk * 2048, BN * 128, 1024), idesc_pv,
+                   kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < ksteps; ++kk)
+          umma_f16(tO, sdesc(sPL + kk * 32, 16, 1024), sdesc(sV + kk * 2048, BN * 128, 1024), idesc_pv, 1u);
+        umma_commit(bar_mma);
+      }
+      mma_pending = true;
+      bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
+      if (!bad) { ph_mma ^= 1; mma_pending = false; }
+      tc_fence_after();
+#pragma unroll
+      for (int g = 0; g < HD / 16; ++g) {
+        float oc[16];
+        tmem_ld16(tO + lane_off + g * 16, oc);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) o_acc[g * 16 + i] = o_acc[g * 16 + i] * corr + oc[i];
+      }
+    }
+    if (abort) break;
+    if (__syncthreads_or(bad)) { abort = true; break; }
+
+    // Epilogue: this thread's row, normalised, to the packed or padded output.
+    const int i = q0 + tid;
+    if (i < n) {
+      long long dst_row = static_cast<long long>(s0) + i;
+      bool ok = true;
+      if constexpr (SCATTER) {
+        dst_row = __ldg(a.src_idx + dst_row);
+        if (dst_row < 0 || dst_row >= static_cast<long long>(a.B) * a.N) {
+          record_error(a.err, RRA_DEVERR_INDEX_RANGE);
+          ok = false;
+        }
+      }
+      if (ok) {
+        Tout* out = static_cast<Tout*>(a.o) + (static_cast<size_t>(dst_row) * H + h) * HD;
+        store_row<Tout>(out, o_acc, 1.f / l_run);
+      }
+    }
+  }
+
+  if (abort) {
+    if (tid == 0) record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
+    // Give our own copies and MMAs in flight a bounded chance to land.
+    if (load_pending) mbar_wait(bar_load, ph_load, WAIT_LIMIT_CYCLES / 8);
+    if (mma_pending) mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES / 8);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, TMEM_COLS);
+  }
+}
+
+// ---------------------------------------------------------------- host side
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool encode_fn() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+// 3-D map over a packed [rows, H, 64] tensor: box = 32 rows of one head.
+cudaError_t make_map(CUtensorMap* map, const void* ptr, int H, long long rows, bool bf16) {
+  cuuint64_t dims[3] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[2] = {static_cast<cuuint64_t>(HD * 2), static_cast<cuuint64_t>(H) * HD * 2};
+  cuuint32_t box[3] = {HD, 1, BOX};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 3,
+                        const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+constexpr int kMaxDev = 64;
+
+template <typename Tin, typename Tout, bool SCATTER>
+cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t stream) {
+  static bool attr_set[kMaxDev] = {};
+  static std::mutex m;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  {
+    std::lock_guard<std::mutex> lock(m);
+    if (!attr_set[dev]) {
+      e = cudaFuncSetAttribute(attend_tc_kernel<Tin, Tout, SCATTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                               static_cast<int>(SMEM_ALLOC));
+      if (e != cudaSuccess) return e;
+      attr_set[dev] = true;
+    }
+  }
+  const bool bf16 = IsBf16<Tin>::value == 1;
+  const long long rows = static_cast<long long>(a.B) * a.max_seqlen;
+  CUtensorMap mq, mk, mv;
+  if ((e = make_map(&mq, a.qp, a.H, rows, bf16)) != cudaSuccess) return e;
+  if ((e = make_map(&mk, a.kp, a.H, rows, bf16)) != cudaSuccess) return e;
+  if ((e = make_map(&mv, a.vp, a.H, rows, bf16)) != cudaSuccess) return e;
+  const int qtiles = (a.max_seqlen + BM - 1) / BM;
+  const long long units = static_cast<long long>(a.B) * a.H * qtiles;
+  const long long cap = static_cast<long long>(CTAS_PER_SM) * (num_sms > 0 ? num_sms : 152);
+  const int grid = static_cast<int>(units < cap ? units : cap);
+  attend_tc_kernel<Tin, Tout, SCATTER><<<grid, THREADS, SMEM_ALLOC, stream>>>(mq, mk, mv, a, qtiles,
+                                                                              static_cast<int>(units));
+  return cudaGetLastError();
+}
+
+template <typename Tin, typename Tout>
+cudaError_t launch_tc_out(const AttendArgs& a, int num_sms, cudaStream_t stream) {
+  if (a.src_idx != nullptr) return launch_tc_typed<Tin, Tout, true>(a, num_sms, stream);
+  return launch_tc_typed<Tin, Tout, false>(a, num_sms, stream);
+}
+
+}  // namespace
+
+bool attend_tc_available() { return encode_fn(); }
+
+cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  if (static_cast<long long>(a.B) * a.max_seqlen >= (1LL << 31)) return cudaErrorInvalidValue;
+  if (in == RRA_BF16) {
+    if (out == RRA_BF16) return launch_tc_out<__nv_bfloat16, __nv_bfloat16>(a, num_sms, stream);
+    if (out == RRA_F16) return launch_tc_out<__nv_bfloat16, __half>(a, num_sms, stream);
+    return launch_tc_out<__nv_bfloat16, float>(a, num_sms, stream);
+  }
+  if (out == RRA_BF16) return launch_tc_out<__half, __nv_bfloat16>(a, num_sms, stream);
+  if (out == RRA_F16) return launch_tc_out<__half, __half>(a, num_sms, stream);
+  return launch_tc_out<__half, float>(a, num_sms, stream);
+}
+
+}  // namespace rra

@@ -64,5 +64,8 @@ void set_last_error_message(const char* msg);
 cudaError_t launch_pack(const PackArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_attend(const AttendArgs& a, rra_dtype in, rra_dtype out, cudaStream_t stream);
 cudaError_t launch_unpack(const UnpackArgs& a, cudaStream_t stream);
+// tcgen05 + TMA attention; needs the driver's tensor-map encoder.
+bool attend_tc_available();
+cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream);
 
 }  // namespace rra

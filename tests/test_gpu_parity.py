@@ -39,15 +39,27 @@ CASES = (
 )
 
 
+KERNELS = [("tcgen05", rra.ATTEND_TCGEN05), ("mma_sync", rra.ATTEND_MMA_SYNC)]
+
+
 @pytest.fixture(scope="module", autouse=True)
 def _lib():
     assert torch.cuda.is_available()
     rra.lib()
     rra.get_device_error(clear=True)
+    yield
+    rra.set_attend_kernel(rra.ATTEND_TCGEN05)
+
+
+@pytest.fixture(params=KERNELS, ids=[k[0] for k in KERNELS])
+def kernel(request):
+    prev = rra.set_attend_kernel(request.param[1])
+    yield request.param[0]
+    rra.set_attend_kernel(prev)
 
 
 @pytest.mark.parametrize("name,make", CASES, ids=[c[0] for c in CASES])
-def test_pipeline_full_size(name, make):
+def test_pipeline_full_size(name, make, kernel):
     case = make()
     ref = oracle_result(case)
     keep = case.keep.numpy()
@@ -58,7 +70,7 @@ def test_pipeline_full_size(name, make):
         err = check_output(got["out"], keep, ref["out"])
         if out_dtype == torch.float32:
             assert err <= ATOL
-        print(f"{name} out={out_dtype} max_abs_err={err:.3e}")
+        print(f"{kernel} {name} out={out_dtype} max_abs_err={err:.3e}")
 
 
 def _edge_cases():
@@ -88,7 +100,7 @@ EDGE = _edge_cases()
 
 
 @pytest.mark.parametrize("name,make", EDGE, ids=[e[0] for e in EDGE])
-def test_pipeline_edge_cases(name, make):
+def test_pipeline_edge_cases(name, make, kernel):
     case = make()
     ref = oracle_result(case)
     keep = case.keep.numpy()
@@ -99,7 +111,7 @@ def test_pipeline_edge_cases(name, make):
         check_output(got["out"], keep, ref["out"])
 
 
-def test_single_token_returns_v_bit_exact():
+def test_single_token_returns_v_bit_exact(kernel):
     case = W.make_custom(4, 197, 6, [1, 1, 1, 1])
     got = run_pipeline(case)
     m = case.keep.numpy() != 0
@@ -108,7 +120,7 @@ def test_single_token_returns_v_bit_exact():
     assert np.array_equal(got32["out"].numpy()[m], case.v.float().numpy()[m])
 
 
-def test_nan_in_pruned_rows_changes_nothing():
+def test_nan_in_pruned_rows_changes_nothing(kernel):
     case = W.make_batched(0.8)
     clean = run_pipeline(case)
     pruned = (case.keep == 0)[:, :, None, None]
@@ -118,7 +130,7 @@ def test_nan_in_pruned_rows_changes_nothing():
     assert np.array_equal(bits(clean["out"]), bits(dirty["out"]))
 
 
-def test_repeat_runs_and_batch_permutation_bit_exact():
+def test_repeat_runs_and_batch_permutation_bit_exact(kernel):
     case = W.make_batched(0.5)
     a = run_pipeline(case)
     b = run_pipeline(case)
@@ -143,7 +155,7 @@ def _packed_inputs(case):
 
 
 @pytest.mark.parametrize("make", [lambda: W.make_tiny(), lambda: W.make_hires(0.5)], ids=["tiny", "hires_p50"])
-def test_attend_packed_output_and_unpack(make):
+def test_attend_packed_output_and_unpack(make, kernel):
     case = make()
     ref, qp, kp, vp, cu = _packed_inputs(case)
     B, N, H, d = case.B, case.N, case.H, case.d
@@ -194,7 +206,7 @@ def test_mask_values_any_nonzero_keeps():
     check_indices_and_packing(got, ref)
 
 
-def test_device_error_codes():
+def test_device_error_codes(kernel):
     case = W.make_serving(2)
     ref, qp, kp, vp, cu = _packed_inputs(case)
     B, N, H, d = case.B, case.N, case.H, case.d
@@ -266,3 +278,10 @@ def test_launch_count_counts_kernels():
     n0 = rra.launch_count()
     rra.run_pipeline(keep, q, k, v)
     assert rra.launch_count() - n0 == 2
+
+
+def test_attend_kernel_selector():
+    prev = rra.set_attend_kernel(rra.ATTEND_MMA_SYNC)
+    assert rra.set_attend_kernel(prev) == rra.ATTEND_MMA_SYNC
+    with pytest.raises(ValueError):
+        rra.set_attend_kernel(7)
