@@ -51,7 +51,11 @@ L2_BYTES = 129 * 1024 * 1024
 
 # ----------------------------------------------------------------- workloads
 
-def make_case(name: str):
+def make_case(name: str, pruning: float | None = None):
+    if name == "batched" and pruning is not None:
+        return W.make_batched(pruning), f"batched DeiT-B: B=64, N=197, H=12, d=64, bf16, {int(pruning * 100)}% pruned +-10%"
+    if name == "hires" and pruning is not None:
+        return W.make_hires(pruning), f"high-res DeiT-B 384px: B=32, N=577, H=12, d=64, bf16, {int(pruning * 100)}% pruned +-10%"
     if name == "serving":
         return W.make_serving(4), "serving DeiT-S: B=4, N=197, H=6, d=64, bf16, 80% pruned (39+-4 tokens/image)"
     if name == "tiny":
@@ -354,13 +358,14 @@ def run_rra(args, world, rank, local):
             _build.build()
         barrier(world)
     from ragged_attention_token_gb300 import rra
+    rra.set_attend_kernel(rra.ATTEND_TCGEN05 if args.attend_kernel == "tcgen05" else rra.ATTEND_MMA_SYNC)
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
     rra.lib()
     stream = torch.cuda.Stream(device=device)
     peaks = measured_peaks()
-    case, desc = make_case(args.workload)
+    case, desc = make_case(args.workload, args.pruning)
     B, N, H, d = case.B, case.N, case.H, case.d
     T = case.kept_tokens
     sets = InputSets(case, device, rra, case.dtype)
@@ -489,6 +494,7 @@ def run_rra(args, world, rank, local):
                     "path": "rra_pipeline_host (pinned H2D, pack, attend, D2H)"},
             "roofline": roof,
             "kernels": kern,
+            "attend_kernel": args.attend_kernel,
             "cpu_baseline": cpu,
             "clocks": clocks,
             "gpu_launches": int(launches) * world,
@@ -509,6 +515,7 @@ def run_sweep(args):
     from ragged_attention_token_gb300 import build as _build
     _build.build()
     from ragged_attention_token_gb300 import rra
+    rra.set_attend_kernel(rra.ATTEND_TCGEN05 if args.attend_kernel == "tcgen05" else rra.ATTEND_MMA_SYNC)
     device = torch.device("cuda", 0)
     stream = torch.cuda.Stream(device=device)
     peaks = measured_peaks()
@@ -522,7 +529,7 @@ def run_sweep(args):
         by = case_bytes(case)
         roof_t = max(by["attend"] / (peaks["hbm_gbs"] * 1e9), by["flops"] / (peaks["bf16_tflops"] * 1e12)) * 1e6
         fused_t = by["fused_min"] / (peaks["hbm_gbs"] * 1e9) * 1e6
-        print(json.dumps({"case": case.name, "B": case.B, "N": case.N, "H": case.H, "T": case.kept_tokens,
+        print(json.dumps({"kernel": args.attend_kernel, "case": case.name, "B": case.B, "N": case.N, "H": case.H, "T": case.kept_tokens,
                           "pack_us": round(tp, 3), "attend_us": round(ta, 3),
                           "attend_roofline_us": round(roof_t, 3), "attend_frac": round(roof_t / ta, 4),
                           "attend": roofline_obj(by["attend"], by["flops"], ta, peaks),
@@ -545,6 +552,10 @@ def main(argv=None):
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work")
     ap.add_argument("--clock-window", type=float, default=1.5, help="seconds of load before the timed region")
+    ap.add_argument("--pruning", type=float, default=None,
+                    help="pruning rate for the batched / hires workloads (their sweep values)")
+    ap.add_argument("--attend-kernel", choices=("tcgen05", "mma_sync"), default="tcgen05",
+                    help="attention kernel behind rra_attend")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

@@ -16,11 +16,15 @@
 //         swizzle, so at most 31 rows past the image are fetched;
 //   MMA   S = Q K^T (M=128, N=chunk rounded up to 16, K=64) -> TMEM cols 0..63;
 //   SIMT  thread r owns query row r (TMEM lane r): it reads its S row, takes
-//         the online-softmax max / rescale in base 2, and writes P as two
-//         bf16/fp16 parts (hi = round(p), lo = round(p - hi)) into shared
-//         memory in the swizzled K-major layout the MMA reads;
-//   MMA   O_chunk = P_hi V + P_lo V (M=128, N=64, K=chunk) -> TMEM cols 64..127;
-//   SIMT  O (registers) = O * correction + O_chunk.
+//         the softmax max in base 2, and writes P as two bf16/fp16 parts
+//         (hi = round(p), lo = round(p - hi)) back over S in TMEM;
+//   MMA   O += P_hi V + P_lo V (M=128, N=64, K=chunk), A read from TMEM,
+//         O accumulating in TMEM cols 64..127 across the unit's chunks.
+//
+// The softmax is lazily rescaled: exponentials use a per-row reference max
+// that only moves (rescaling O in TMEM) when a chunk's max exceeds it by
+// more than 8 in the log2 domain.  The next item's TMA loads are issued
+// before the current item computes (two K/V stages, two Q slots).
 //
 // P is split because one bf16 rounding of the weights alone leaves up to
 // ~2e-3 of output error at these lengths; hi + lo carries ~16 bits.  Keys
@@ -46,15 +50,17 @@ constexpr int THREADS = 128;
 constexpr int BOX = 32;        // rows per TMA box
 constexpr int CTAS_PER_SM = 3;
 
-constexpr uint32_t OFF_Q = 0;                        // 128 rows x 128 B
-constexpr uint32_t OFF_K = OFF_Q + BM * 128;         //  64 rows x 128 B
-constexpr uint32_t OFF_V = OFF_K + BN * 128;
-constexpr uint32_t OFF_PH = OFF_V + BN * 128;        // 128 rows x 64 keys x 2 B
-constexpr uint32_t OFF_PL = OFF_PH + BM * 128;
-constexpr uint32_t OFF_BAR = OFF_PL + BM * 128;      // two mbarriers + TMEM address slot
+constexpr int STAGES = 2;      // K/V chunk ring and Q tile slots
+
+constexpr uint32_t Q_BYTES = BM * 128;               // 128 rows x 128 B
+constexpr uint32_t KV_BYTES = BN * 128;              //  64 rows x 128 B
+constexpr uint32_t OFF_Q = 0;                        // Q[STAGES]
+constexpr uint32_t OFF_K = OFF_Q + STAGES * Q_BYTES; // K[STAGES]
+constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
+constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;  // load[STAGES], mma, TMEM slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // slack to align the base to 1024 B
-constexpr uint32_t TMEM_COLS = 128;                  // S: cols [0,64), O: cols [64,128)
+constexpr uint32_t TMEM_COLS = 128;                  // S/P: cols [0,64), O: cols [64,128)
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
 
 template <typename T> struct IsBf16;
@@ -131,6 +137,22 @@ __device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
+// Same with the A operand read from TMEM (M rows = lanes, K packed 2 per column).
+__device__ __forceinline__ void umma_f16_tmem_a(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                                uint32_t accumulate) {
+  asm volatile(
+      "{\n .reg .pred p;\n setp.ne.b32 p, %4, 0;\n"
+      " tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n}\n" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+// 8 consecutive 32-bit columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_st8(uint32_t taddr, const uint32_t* v) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr), "r"(v[0]),
+               "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7])
+               : "memory");
+}
+__device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 __device__ __forceinline__ void umma_commit(uint32_t bar) {
   asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
                : "memory");
@@ -237,6 +259,43 @@ __device__ __forceinline__ void store_row<__half>(__half* dst, const float* o, f
   }
 }
 
+// One unit of work as every thread of the CTA sees it (all fields uniform).
+struct Unit {
+  int u, b, h, s0, n, q0, rows_q, nchunks;
+};
+
+// First unit at index >= u (stride `step`) whose query tile holds rows; a
+// unit with an inconsistent length records an error and is skipped.
+__device__ __forceinline__ Unit next_unit(int u, int step, int units, int BH, const AttendArgs& a, int tid) {
+  Unit x;
+  for (; u < units; u += step) {
+    const int qt = u / BH;
+    const int bh = u - qt * BH;
+    const int h = bh % a.H;
+    const int b = bh / a.H;
+    const int s0 = __ldg(a.cu_seqlens + b);
+    const int n = __ldg(a.cu_seqlens + b + 1) - s0;
+    if (n < 0 || n > a.max_seqlen) {
+      if (qt == 0 && h == 0 && tid == 0)
+        record_error(a.err, n < 0 ? RRA_DEVERR_SEQ_NEGATIVE : RRA_DEVERR_SEQ_TOO_LONG);
+      continue;
+    }
+    const int q0 = qt * BM;
+    if (q0 >= n) continue;
+    x.u = u;
+    x.b = b;
+    x.h = h;
+    x.s0 = s0;
+    x.n = n;
+    x.q0 = q0;
+    x.rows_q = min(BM, n - q0);
+    x.nchunks = (n + BN - 1) / BN;
+    return x;
+  }
+  x.u = units;
+  return x;
+}
+
 template <typename Tin, typename Tout, bool SCATTER>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -246,10 +305,12 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t sQ = base + OFF_Q, sK = base + OFF_K, sV = base + OFF_V;
-  const uint32_t sPH = base + OFF_PH, sPL = base + OFF_PL;
-  const uint32_t bar_load = base + OFF_BAR, bar_mma = base + OFF_BAR + 8, slot = base + OFF_BAR + 16;
-  const volatile uint32_t* slot_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + 16);
+  const uint32_t bar_mma = base + OFF_BAR + 16, slot = base + OFF_BAR + 24;
+  const volatile uint32_t* slot_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + 24);
+  auto sQ = [&](int i) { return base + OFF_Q + i * Q_BYTES; };
+  auto sK = [&](int i) { return base + OFF_K + i * KV_BYTES; };
+  auto sV = [&](int i) { return base + OFF_V + i * KV_BYTES; };
+  auto bar_load = [&](int i) { return base + OFF_BAR + i * 8; };
 
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
@@ -257,7 +318,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     tmem_relinquish();
   }
   if (tid == 32) {
-    mbar_init(bar_load, 1);
+    mbar_init(bar_load(0), 1);
+    mbar_init(bar_load(1), 1);
     mbar_init(bar_mma, 1);
     fence_barrier_init();
   }
@@ -268,173 +330,218 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
   const uint32_t tS = tmem, tO = tmem + 64;
   const uint32_t idesc_pv = idesc_f16(BF, 1, BM, HD);
-  const int H = a.H;
+  const int BH = a.B * a.H;
+  const int step = gridDim.x;
+  (void)qtiles;
 
-  uint32_t ph_load = 0, ph_mma = 0;
-  bool load_pending = false, mma_pending = false;
+  // Issues the TMA loads of (unit x, chunk c) into K/V stage `st` and, for
+  // the first chunk, the unit's Q tile into Q slot `qs` (thread 0 only).
+  auto issue = [&](const Unit& x, int c, int st, int qs) {
+    const int k0 = c * BN;
+    const int n_c = min(BN, x.n - k0);
+    const int kboxes = (n_c + BOX - 1) / BOX;
+    const int qboxes = (c == 0) ? (x.rows_q + BOX - 1) / BOX : 0;
+    mbar_expect_tx(bar_load(st), static_cast<uint32_t>((qboxes + 2 * kboxes) * BOX * 128));
+    for (int j = 0; j < qboxes; ++j)
+      tma_load_3d(sQ(qs) + j * BOX * 128, &tmap_q, 0, x.h, x.s0 + x.q0 + j * BOX, bar_load(st));
+    for (int j = 0; j < kboxes; ++j) {
+      tma_load_3d(sK(st) + j * BOX * 128, &tmap_k, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
+      tma_load_3d(sV(st) + j * BOX * 128, &tmap_v, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
+    }
+  };
+
+  uint32_t ph_load[STAGES] = {0u, 0u};
+  uint32_t ph_mma = 0;
+  bool load_pending[STAGES] = {false, false};
+  bool mma_pending = false;
   bool bad = false;      // this thread saw a wait time out
   bool abort = false;    // some thread did: the whole CTA stops
 
-  for (int u = blockIdx.x; u < units; u += gridDim.x) {
-    const int qt = u % qtiles;
-    const int bh = u / qtiles;
-    const int h = bh % H;
-    const int b = bh / H;
-    const int s0 = __ldg(a.cu_seqlens + b);
-    const int n = __ldg(a.cu_seqlens + b + 1) - s0;
-    if (n < 0 || n > a.max_seqlen) {
-      if (qt == 0 && h == 0 && tid == 0)
-        record_error(a.err, n < 0 ? RRA_DEVERR_SEQ_NEGATIVE : RRA_DEVERR_SEQ_TOO_LONG);
-      continue;
+  Unit cur = next_unit(blockIdx.x, step, units, BH, a, tid);
+  int c = 0, stage = 0, qslot = 0;
+  if (cur.u < units) {
+    if (tid == 0) issue(cur, 0, 0, 0);
+    load_pending[0] = true;
+  }
+
+  float m_run = -INFINITY, l_run = 0.f;   // this row's reference max and sum
+
+  while (cur.u < units) {
+    // Prefetch the next item into the other stage while this one computes.
+    Unit nxt = cur;
+    int nc = c + 1, nqslot = qslot;
+    if (nc >= cur.nchunks) {
+      nxt = next_unit(cur.u + step, step, units, BH, a, tid);
+      nc = 0;
+      nqslot = qslot ^ 1;
     }
-    const int q0 = qt * BM;
-    if (q0 >= n) continue;
-    const int rows_q = min(BM, n - q0);
-    const int nchunks = (n + BN - 1) / BN;
-
-    float o_acc[HD];
-    float m_run = -INFINITY, l_run = 0.f;
-#pragma unroll
-    for (int i = 0; i < HD; ++i) o_acc[i] = 0.f;
-
-    for (int c = 0; c < nchunks; ++c) {
-      const int k0 = c * BN;
-      const int n_c = min(BN, n - k0);
-      const int nk16 = (n_c + 15) & ~15;
-      const int kboxes = (n_c + BOX - 1) / BOX;
-      const int qboxes = (c == 0) ? (rows_q + BOX - 1) / BOX : 0;
-
-      // Everyone is done with shared K/V/P and TMEM S/O from the last chunk.
-      tc_fence_before();
-      if (__syncthreads_or(bad)) { abort = true; break; }
+    if (nxt.u < units) {
       if (tid == 0) {
         tc_fence_after();
-        mbar_expect_tx(bar_load, static_cast<uint32_t>((qboxes + 2 * kboxes) * BOX * 128));
-        for (int j = 0; j < qboxes; ++j) tma_load_3d(sQ + j * BOX * 128, &tmap_q, 0, h, s0 + q0 + j * BOX, bar_load);
-        for (int j = 0; j < kboxes; ++j) {
-          tma_load_3d(sK + j * BOX * 128, &tmap_k, 0, h, s0 + k0 + j * BOX, bar_load);
-          tma_load_3d(sV + j * BOX * 128, &tmap_v, 0, h, s0 + k0 + j * BOX, bar_load);
-        }
+        issue(nxt, nc, stage ^ 1, nqslot);
       }
-      load_pending = true;
-      bad |= !mbar_wait(bar_load, ph_load, WAIT_LIMIT_CYCLES);
-      if (!bad) { ph_load ^= 1; load_pending = false; }
-      // V rows [n_c, nk16) enter the MMA with p = 0: make them exact zeros.
-      if (tid < (nk16 - n_c) * 8)
-        st_shared_v4(sV + (n_c + (tid >> 3)) * 128 + (tid & 7) * 16, 0u, 0u, 0u, 0u);
-      fence_proxy_async();
-      if (__syncthreads_or(bad)) { abort = true; break; }
+      load_pending[stage ^ 1] = true;
+    }
 
-      // S = Q K^T -> TMEM columns [0, nk16)
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t idesc_s = idesc_f16(BF, 0, BM, nk16);
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK + kk * 32, 16, 1024), idesc_s, kk > 0 ? 1u : 0u);
-        umma_commit(bar_mma);
-      }
-      mma_pending = true;
-      bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
-      if (!bad) { ph_mma ^= 1; mma_pending = false; }
+    const int k0 = c * BN;
+    const int n_c = min(BN, cur.n - k0);
+    const int nk16 = (n_c + 15) & ~15;
+    const bool rows_here = warp * 32 < cur.rows_q;   // warp-uniform
+
+    bad |= !mbar_wait(bar_load(stage), ph_load[stage], WAIT_LIMIT_CYCLES);
+    if (!bad) { ph_load[stage] ^= 1; load_pending[stage] = false; }
+    // V rows [n_c, nk16) enter the MMA with p = 0: make them exact zeros.
+    if (tid < (nk16 - n_c) * 8)
+      st_shared_v4(sV(stage) + (n_c + (tid >> 3)) * 128 + (tid & 7) * 16, 0u, 0u, 0u, 0u);
+    fence_proxy_async();
+    if (__syncthreads_or(bad)) { abort = true; break; }
+
+    // S = Q K^T -> TMEM columns [0, nk16)
+    if (tid == 0) {
       tc_fence_after();
+      const uint32_t idesc_s = idesc_f16(BF, 0, BM, nk16);
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk)
+        umma_f16(tS, sdesc(sQ(qslot) + kk * 32, 16, 1024), sdesc(sK(stage) + kk * 32, 16, 1024), idesc_s,
+                 kk > 0 ? 1u : 0u);
+      umma_commit(bar_mma);
+    }
+    mma_pending = true;
+    bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
+    if (!bad) { ph_mma ^= 1; mma_pending = false; }
+    tc_fence_after();
 
-      // Softmax on this thread's row, reading S from TMEM in 16-column
-      // pieces twice (max, then exponentials) to keep registers low.
-      const float c2 = a.scale_log2;
-      float mx = -INFINITY;
+    // Softmax on this thread's row (lane), lazily rescaled: O stays in TMEM
+    // across chunks and exponentials use the running reference max m_ref;
+    // only when a row's max grows past m_ref + 8 (p could exceed 2^8) is
+    // the warp's O rescaled in TMEM.  S is read in 16-column pieces twice
+    // (max, then exponentials); each piece's P_hi / P_lo (8 columns of packed
+    // pairs each) overwrites exactly the S columns just read.
+    const float c2 = a.scale_log2;
+    if (rows_here) {
+      const bool full = (n_c == BN);
+      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
       for (int g = 0; g < BN / 16; ++g) {
         if (g * 16 < nk16) {
           float t[16];
           tmem_ld16(tS + lane_off + g * 16, t);
+          if (full) {
 #pragma unroll
-          for (int i = 0; i < 16; ++i)
-            if (g * 16 + i < n_c) mx = fmaxf(mx, t[i] * c2);
-        }
-      }
-      const float m_new = fmaxf(m_run, mx);
-      const float corr = fast_exp2(m_run - m_new);   // 0 on the first chunk
-      l_run *= corr;
-      const int r = tid;
+            for (int i = 0; i < 16; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], t[i] * c2);
+          } else {
 #pragma unroll
-      for (int g = 0; g < BN / 16; ++g) {
-        if (g * 16 < nk16) {
-          float t[16];
-          tmem_ld16(tS + lane_off + g * 16, t);
-#pragma unroll
-          for (int half = 0; half < 2; ++half) {
-            float p[8];
-#pragma unroll
-            for (int i = 0; i < 8; ++i) {
-              const int j = g * 16 + half * 8 + i;
-              p[i] = (j < n_c) ? fast_exp2(fmaf(t[half * 8 + i], c2, -m_new)) : 0.f;
-              l_run += p[i];
-            }
-            uint32_t hi[4], lo[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) split2<BF == 1>(p[2 * i], p[2 * i + 1], hi[i], lo[i]);
-            const int chunk = g * 2 + half;
-            const uint32_t off = r * 128 + ((chunk ^ (r & 7)) << 4);
-            st_shared_v4(sPH + off, hi[0], hi[1], hi[2], hi[3]);
-            st_shared_v4(sPL + off, lo[0], lo[1], lo[2], lo[3]);
+            for (int i = 0; i < 16; ++i)
+              if (g * 16 + i < n_c) mx4[i & 3] = fmaxf(mx4[i & 3], t[i] * c2);
           }
         }
       }
-      m_run = m_new;
-      fence_proxy_async();
-      tc_fence_before();
-      if (__syncthreads_or(bad)) { abort = true; break; }
-
-      // O_chunk = P_hi V + P_lo V -> TMEM columns [64, 128)
-      if (tid == 0) {
-        tc_fence_after();
-        const int ksteps = nk16 / 16;
-        for (int kk = 0; kk < ksteps; ++kk)
-          umma_f16(tO, sdesc(sPH + kk * 32, 16, 1024), sdesc(sV + kk * 2048, BN * 128, 1024), idesc_pv,
-                   kk > 0 ? 1u : 0u);
-        for (int kk = 0; kk < ksteps; ++kk)
-          umma_f16(tO, sdesc(sPL + kk * 32, 16, 1024), sdesc(sV + kk * 2048, BN * 128, 1024), idesc_pv, 1u);
-        umma_commit(bar_mma);
-      }
-      mma_pending = true;
-      bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
-      if (!bad) { ph_mma ^= 1; mma_pending = false; }
-      tc_fence_after();
+      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+      if (c == 0) {
+        m_run = mx;
+      } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
+        const float m_new = fmaxf(m_run, mx);
+        const float alpha = fast_exp2(m_run - m_new);
+        l_run *= alpha;
 #pragma unroll
-      for (int g = 0; g < HD / 16; ++g) {
-        float oc[16];
-        tmem_ld16(tO + lane_off + g * 16, oc);
+        for (int g = 0; g < HD / 16; ++g) {
+          float oc[16];
+          tmem_ld16(tO + lane_off + g * 16, oc);
+          uint32_t w[16];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) o_acc[g * 16 + i] = o_acc[g * 16 + i] * corr + oc[i];
+          for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(oc[i] * alpha);
+          tmem_st8(tO + lane_off + g * 16, w);
+          tmem_st8(tO + lane_off + g * 16 + 8, w + 8);
+        }
+        m_run = m_new;
       }
-    }
-    if (abort) break;
-    if (__syncthreads_or(bad)) { abort = true; break; }
-
-    // Epilogue: this thread's row, normalised, to the packed or padded output.
-    const int i = q0 + tid;
-    if (i < n) {
-      long long dst_row = static_cast<long long>(s0) + i;
-      bool ok = true;
-      if constexpr (SCATTER) {
-        dst_row = __ldg(a.src_idx + dst_row);
-        if (dst_row < 0 || dst_row >= static_cast<long long>(a.B) * a.N) {
-          record_error(a.err, RRA_DEVERR_INDEX_RANGE);
-          ok = false;
+      float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+      for (int g = 0; g < BN / 16; ++g) {
+        if (g * 16 < nk16) {
+          float t[16];
+          tmem_ld16(tS + lane_off + g * 16, t);
+          uint32_t hi[8], lo[8];
+#pragma unroll
+          for (int i = 0; i < 8; ++i) {
+            const int j = g * 16 + 2 * i;
+            float p0 = fast_exp2(fmaf(t[2 * i], c2, -m_run));
+            float p1 = fast_exp2(fmaf(t[2 * i + 1], c2, -m_run));
+            if (!full) {
+              p0 = (j < n_c) ? p0 : 0.f;
+              p1 = (j + 1 < n_c) ? p1 : 0.f;
+            }
+            l4[(2 * i) & 3] += p0;
+            l4[(2 * i + 1) & 3] += p1;
+            split2<BF == 1>(p0, p1, hi[i], lo[i]);
+          }
+          tmem_st8(tS + lane_off + g * 16, hi);
+          tmem_st8(tS + lane_off + g * 16 + 8, lo);
         }
       }
-      if (ok) {
-        Tout* out = static_cast<Tout*>(a.o) + (static_cast<size_t>(dst_row) * H + h) * HD;
-        store_row<Tout>(out, o_acc, 1.f / l_run);
+      l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
+      tmem_st_wait();
+    }
+    tc_fence_before();
+    if (__syncthreads_or(bad)) { abort = true; break; }
+
+    // O += P_hi V + P_lo V in TMEM columns [64, 128) (fresh on a unit's first chunk)
+    if (tid == 0) {
+      tc_fence_after();
+      const int ksteps = nk16 / 16;
+      for (int kk = 0; kk < ksteps; ++kk)
+        umma_f16_tmem_a(tO, tS + kk * 16, sdesc(sV(stage) + kk * 2048, KV_BYTES, 1024), idesc_pv,
+                        (kk > 0 || c > 0) ? 1u : 0u);
+      for (int kk = 0; kk < ksteps; ++kk)
+        umma_f16_tmem_a(tO, tS + kk * 16 + 8, sdesc(sV(stage) + kk * 2048, KV_BYTES, 1024), idesc_pv, 1u);
+      umma_commit(bar_mma);
+    }
+    mma_pending = true;
+    bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
+    if (!bad) { ph_mma ^= 1; mma_pending = false; }
+    tc_fence_after();
+
+    if (c == cur.nchunks - 1 && rows_here) {
+      // Epilogue: this thread's row, normalised, to the packed or padded output.
+      float o_acc[HD];
+#pragma unroll
+      for (int g = 0; g < HD / 16; ++g) tmem_ld16(tO + lane_off + g * 16, o_acc + g * 16);
+      const int i = cur.q0 + tid;
+      if (i < cur.n) {
+        long long dst_row = static_cast<long long>(cur.s0) + i;
+        bool ok = true;
+        if constexpr (SCATTER) {
+          dst_row = __ldg(a.src_idx + dst_row);
+          if (dst_row < 0 || dst_row >= static_cast<long long>(a.B) * a.N) {
+            record_error(a.err, RRA_DEVERR_INDEX_RANGE);
+            ok = false;
+          }
+        }
+        if (ok) {
+          Tout* out = static_cast<Tout*>(a.o) + (static_cast<size_t>(dst_row) * a.H + cur.h) * HD;
+          store_row<Tout>(out, o_acc, 1.f / l_run);
+        }
       }
     }
+    if (c == cur.nchunks - 1) {
+      m_run = -INFINITY;
+      l_run = 0.f;
+    }
+    // All TMEM reads of S/P and O are done before the next S MMA.
+    tc_fence_before();
+    if (__syncthreads_or(bad)) { abort = true; break; }
+
+    cur = nxt;
+    c = nc;
+    qslot = nqslot;
+    stage ^= 1;
   }
 
   if (abort) {
     if (tid == 0) record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
     // Give our own copies and MMAs in flight a bounded chance to land.
-    if (load_pending) mbar_wait(bar_load, ph_load, WAIT_LIMIT_CYCLES / 8);
+    for (int st = 0; st < STAGES; ++st)
+      if (load_pending[st]) mbar_wait(bar_load(st), ph_load[st], WAIT_LIMIT_CYCLES / 8);
     if (mma_pending) mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES / 8);
   }
   tc_fence_before();
