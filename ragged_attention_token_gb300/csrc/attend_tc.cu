@@ -23,8 +23,10 @@
 //
 // The softmax is lazily rescaled: exponentials use a per-row reference max
 // that only moves (rescaling O in TMEM) when a chunk's max exceeds it by
-// more than 8 in the log2 domain.  The next item's TMA loads are issued
-// before the current item computes (two K/V stages, two Q slots).
+// more than 8 in the log2 domain (bf16: a single pass against the running
+// reference, redone exactly only when a row's chunk sum exceeds 2^32).
+// The next item's K/V loads are issued before the current item computes (two
+// stages) and the next unit's Q right after the current unit's last S product.
 //
 // P is split because one bf16 rounding of the weights alone leaves up to
 // ~2e-3 of output error at these lengths; hi + lo carries ~16 bits.  Keys
@@ -49,18 +51,18 @@ constexpr int HD = 64;         // head dim
 constexpr int THREADS = 128;
 constexpr int BOX = 32;        // rows per TMA box
 constexpr int CTAS_PER_SM = 3;
+constexpr int STAGES = 2;      // K/V chunk ring
 
-constexpr int STAGES = 2;      // K/V chunk ring and Q tile slots
-
-constexpr uint32_t Q_BYTES = BM * 128;               // 128 rows x 128 B
-constexpr uint32_t KV_BYTES = BN * 128;              //  64 rows x 128 B
-constexpr uint32_t OFF_Q = 0;                        // Q[STAGES]
-constexpr uint32_t OFF_K = OFF_Q + STAGES * Q_BYTES; // K[STAGES]
-constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;
-constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;  // load[STAGES], mma, TMEM slot
+constexpr uint32_t Q_BYTES = BM * 128;                 // 128 rows x 128 B
+constexpr uint32_t KV_BYTES = BN * 128;                //  64 rows x 128 B
+constexpr uint32_t OFF_Q = 0;                          // one Q tile
+constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;            // K[STAGES]
+constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;  // V[STAGES]
+constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;  // load[STAGES], q, mma, TMEM slot
 constexpr uint32_t SMEM_USED = OFF_BAR + 64;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;    // slack to align the base to 1024 B
-constexpr uint32_t TMEM_COLS = 128;                  // S/P: cols [0,64), O: cols [64,128)
+constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;      // slack to align the base to 1024 B
+constexpr uint32_t TMEM_COLS = 128;                    // S/P: cols [0,64), O: cols [64,128)
+constexpr uint32_t WAIT_SUSPEND_NS = 20000;            // try_wait suspend hint
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
 
 template <typename T> struct IsBf16;
@@ -85,9 +87,9 @@ __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity)
+      : "r"(bar), "r"(parity), "r"(WAIT_SUSPEND_NS)
       : "memory");
   return ok != 0;
 }
@@ -261,7 +263,7 @@ __device__ __forceinline__ void store_row<__half>(__half* dst, const float* o, f
 
 // One unit of work as every thread of the CTA sees it (all fields uniform).
 struct Unit {
-  int u, b, h, s0, n, q0, rows_q, nchunks;
+  int u, h, s0, n, q0, rows_q, nchunks;
 };
 
 // First unit at index >= u (stride `step`) whose query tile holds rows; a
@@ -283,7 +285,6 @@ __device__ __forceinline__ Unit next_unit(int u, int step, int units, int BH, co
     const int q0 = qt * BM;
     if (q0 >= n) continue;
     x.u = u;
-    x.b = b;
     x.h = h;
     x.s0 = s0;
     x.n = n;
@@ -296,21 +297,101 @@ __device__ __forceinline__ Unit next_unit(int u, int step, int units, int BH, co
   return x;
 }
 
+// bf16 hi/lo split of two weights: hi = p truncated to bf16 (upper 16 bits,
+// exact), lo = p - hi (exact in fp32) rounded to bf16; hi + lo carries p to
+// 2^-16 relative.  Packed low half = first element (K order).
+__device__ __forceinline__ void split2_bf16_trunc(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+  const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+  hi = __byte_perm(b0, b1, 0x7632);
+  const float r0 = p0 - __uint_as_float(b0 & 0xFFFF0000u);
+  const float r1 = p1 - __uint_as_float(b1 & 0xFFFF0000u);
+  __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+  lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+// Exponentials of one S row chunk against reference mref, packed as P hi/lo
+// pairs in registers; returns the chunk's row sum.  With ref_first the
+// reference is replaced by this row's first score (so that weight is exactly
+// 1: a one-token image returns V bit for bit) and written back to mref.
+template <bool BF16>
+__device__ __forceinline__ float chunk_weights(uint32_t tS_row, int nk16, int n_c, bool full, float c2, float& mref,
+                                               bool ref_first, uint32_t (&hi)[32], uint32_t (&lo)[32]) {
+  float l4[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+  for (int g = 0; g < BN / 16; ++g) {
+    if (g * 16 < nk16) {
+      float t[16];
+      tmem_ld16(tS_row + g * 16, t);
+      if (g == 0 && ref_first) mref = t[0] * c2;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int j = g * 16 + 2 * i;
+        float p0 = fast_exp2(fmaf(t[2 * i], c2, -mref));
+        float p1 = fast_exp2(fmaf(t[2 * i + 1], c2, -mref));
+        if (!full) {
+          p0 = (j < n_c) ? p0 : 0.f;
+          p1 = (j + 1 < n_c) ? p1 : 0.f;
+        }
+        l4[(2 * i) & 3] += p0;
+        l4[(2 * i + 1) & 3] += p1;
+        if constexpr (BF16) split2_bf16_trunc(p0, p1, hi[g * 8 + i], lo[g * 8 + i]);
+        else split2<false>(p0, p1, hi[g * 8 + i], lo[g * 8 + i]);
+      }
+    }
+  }
+  return (l4[0] + l4[1]) + (l4[2] + l4[3]);
+}
+
+// Max of scale*S over the chunk's valid columns.
+__device__ __forceinline__ float chunk_max(uint32_t tS_row, int nk16, int n_c, bool full, float c2) {
+  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+  for (int g = 0; g < BN / 16; ++g) {
+    if (g * 16 < nk16) {
+      float t[16];
+      tmem_ld16(tS_row + g * 16, t);
+      if (full) {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], t[i] * c2);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i)
+          if (g * 16 + i < n_c) mx4[i & 3] = fmaxf(mx4[i & 3], t[i] * c2);
+      }
+    }
+  }
+  return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+}
+
+// O row (TMEM) *= alpha.
+__device__ __forceinline__ void rescale_o(uint32_t tO_row, float alpha) {
+#pragma unroll
+  for (int g = 0; g < HD / 16; ++g) {
+    float oc[16];
+    tmem_ld16(tO_row + g * 16, oc);
+    uint32_t w[16];
+#pragma unroll
+    for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(oc[i] * alpha);
+    tmem_st8(tO_row + g * 16, w);
+    tmem_st8(tO_row + g * 16 + 8, w + 8);
+  }
+}
+
 template <typename Tin, typename Tout, bool SCATTER>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const AttendArgs a, int qtiles, int units) {
-  constexpr uint32_t BF = IsBf16<Tin>::value;
+  constexpr bool BF = IsBf16<Tin>::value == 1;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
   uint8_t* gbase = smem_raw + (base - raw);
-  const uint32_t bar_mma = base + OFF_BAR + 16, slot = base + OFF_BAR + 24;
-  const volatile uint32_t* slot_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + 24);
-  auto sQ = [&](int i) { return base + OFF_Q + i * Q_BYTES; };
+  const uint32_t sQ = base + OFF_Q;
   auto sK = [&](int i) { return base + OFF_K + i * KV_BYTES; };
   auto sV = [&](int i) { return base + OFF_V + i * KV_BYTES; };
   auto bar_load = [&](int i) { return base + OFF_BAR + i * 8; };
+  const uint32_t bar_q = base + OFF_BAR + 16, bar_mma = base + OFF_BAR + 24, slot = base + OFF_BAR + 32;
+  const volatile uint32_t* slot_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + 32);
 
   const int tid = threadIdx.x, warp = tid >> 5;
   if (warp == 0) {
@@ -320,6 +401,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   if (tid == 32) {
     mbar_init(bar_load(0), 1);
     mbar_init(bar_load(1), 1);
+    mbar_init(bar_q, 1);
     mbar_init(bar_mma, 1);
     fence_barrier_init();
   }
@@ -329,65 +411,73 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   const uint32_t tmem = *slot_ptr;
   const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
   const uint32_t tS = tmem, tO = tmem + 64;
-  const uint32_t idesc_pv = idesc_f16(BF, 1, BM, HD);
+  const uint32_t idesc_pv = idesc_f16(BF ? 1u : 0u, 1, BM, HD);
   const int BH = a.B * a.H;
   const int step = gridDim.x;
+  const float c2 = a.scale_log2;
   (void)qtiles;
 
-  // Issues the TMA loads of (unit x, chunk c) into K/V stage `st` and, for
-  // the first chunk, the unit's Q tile into Q slot `qs` (thread 0 only).
-  auto issue = [&](const Unit& x, int c, int st, int qs) {
+  // TMA issue (thread 0 only): K/V rows of (unit x, chunk c) into stage st;
+  // the unit's Q tile into the single Q buffer.
+  auto issue_kv = [&](const Unit& x, int c, int st) {
     const int k0 = c * BN;
     const int n_c = min(BN, x.n - k0);
     const int kboxes = (n_c + BOX - 1) / BOX;
-    const int qboxes = (c == 0) ? (x.rows_q + BOX - 1) / BOX : 0;
-    mbar_expect_tx(bar_load(st), static_cast<uint32_t>((qboxes + 2 * kboxes) * BOX * 128));
-    for (int j = 0; j < qboxes; ++j)
-      tma_load_3d(sQ(qs) + j * BOX * 128, &tmap_q, 0, x.h, x.s0 + x.q0 + j * BOX, bar_load(st));
+    mbar_expect_tx(bar_load(st), static_cast<uint32_t>(2 * kboxes * BOX * 128));
     for (int j = 0; j < kboxes; ++j) {
       tma_load_3d(sK(st) + j * BOX * 128, &tmap_k, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
       tma_load_3d(sV(st) + j * BOX * 128, &tmap_v, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
     }
   };
+  auto issue_q = [&](const Unit& x) {
+    const int qboxes = (x.rows_q + BOX - 1) / BOX;
+    mbar_expect_tx(bar_q, static_cast<uint32_t>(qboxes * BOX * 128));
+    for (int j = 0; j < qboxes; ++j) tma_load_3d(sQ + j * BOX * 128, &tmap_q, 0, x.h, x.s0 + x.q0 + j * BOX, bar_q);
+  };
 
   uint32_t ph_load[STAGES] = {0u, 0u};
-  uint32_t ph_mma = 0;
+  uint32_t ph_q = 0, ph_mma = 0;
   bool load_pending[STAGES] = {false, false};
-  bool mma_pending = false;
+  bool q_pending = false, mma_pending = false;
   bool bad = false;      // this thread saw a wait time out
   bool abort = false;    // some thread did: the whole CTA stops
 
   Unit cur = next_unit(blockIdx.x, step, units, BH, a, tid);
-  int c = 0, stage = 0, qslot = 0;
+  int c = 0, stage = 0;
   if (cur.u < units) {
-    if (tid == 0) issue(cur, 0, 0, 0);
+    if (tid == 0) {
+      issue_q(cur);
+      issue_kv(cur, 0, 0);
+    }
+    q_pending = true;
     load_pending[0] = true;
   }
-
-  float m_run = -INFINITY, l_run = 0.f;   // this row's reference max and sum
+  float m_run = 0.f, l_run = 0.f;   // this row's reference max (log2 units) and sum
 
   while (cur.u < units) {
-    // Prefetch the next item into the other stage while this one computes.
+    // Prefetch the next item's K/V into the other stage while this one computes.
     Unit nxt = cur;
-    int nc = c + 1, nqslot = qslot;
+    int nc = c + 1;
     if (nc >= cur.nchunks) {
       nxt = next_unit(cur.u + step, step, units, BH, a, tid);
       nc = 0;
-      nqslot = qslot ^ 1;
     }
-    if (nxt.u < units) {
-      if (tid == 0) {
-        tc_fence_after();
-        issue(nxt, nc, stage ^ 1, nqslot);
-      }
+    const bool have_next = nxt.u < units;
+    if (have_next) {
+      if (tid == 0) issue_kv(nxt, nc, stage ^ 1);
       load_pending[stage ^ 1] = true;
     }
 
     const int k0 = c * BN;
     const int n_c = min(BN, cur.n - k0);
     const int nk16 = (n_c + 15) & ~15;
+    const bool full = (n_c == BN);
     const bool rows_here = warp * 32 < cur.rows_q;   // warp-uniform
 
+    if (c == 0) {
+      bad |= !mbar_wait(bar_q, ph_q, WAIT_LIMIT_CYCLES);
+      if (!bad) { ph_q ^= 1; q_pending = false; }
+    }
     bad |= !mbar_wait(bar_load(stage), ph_load[stage], WAIT_LIMIT_CYCLES);
     if (!bad) { ph_load[stage] ^= 1; load_pending[stage] = false; }
     // V rows [n_c, nk16) enter the MMA with p = 0: make them exact zeros.
@@ -399,10 +489,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     // S = Q K^T -> TMEM columns [0, nk16)
     if (tid == 0) {
       tc_fence_after();
-      const uint32_t idesc_s = idesc_f16(BF, 0, BM, nk16);
+      const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
 #pragma unroll
       for (int kk = 0; kk < HD / 16; ++kk)
-        umma_f16(tS, sdesc(sQ(qslot) + kk * 32, 16, 1024), sdesc(sK(stage) + kk * 32, 16, 1024), idesc_s,
+        umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(stage) + kk * 32, 16, 1024), idesc_s,
                  kk > 0 ? 1u : 0u);
       umma_commit(bar_mma);
     }
@@ -410,76 +500,59 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
     if (!bad) { ph_mma ^= 1; mma_pending = false; }
     tc_fence_after();
+    // The unit's last S product is done: its Q buffer can take the next unit's tile.
+    if (nc == 0 && have_next) {
+      if (tid == 0 && !bad) issue_q(nxt);
+      q_pending = true;
+    }
 
-    // Softmax on this thread's row (lane), lazily rescaled: O stays in TMEM
-    // across chunks and exponentials use the running reference max m_ref;
-    // only when a row's max grows past m_ref + 8 (p could exceed 2^8) is
-    // the warp's O rescaled in TMEM.  S is read in 16-column pieces twice
-    // (max, then exponentials); each piece's P_hi / P_lo (8 columns of packed
-    // pairs each) overwrites exactly the S columns just read.
-    const float c2 = a.scale_log2;
+    // Softmax on this thread's row (TMEM lane).  Exponentials are taken
+    // against a per-row reference m_run (log2 units) and O accumulates in
+    // TMEM across chunks.  bf16: one pass, the reference being the row's first
+    // score on the first chunk and the running reference after; only when a
+    // row's chunk sum exceeds 2^32 is the chunk redone exactly (true max, O
+    // rescaled).  fp16 (narrower
+    // range for P): max pass first, rescale when the max grows by > 8.
     if (rows_here) {
-      const bool full = (n_c == BN);
-      float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+      const uint32_t tS_row = tS + lane_off, tO_row = tO + lane_off;
+      uint32_t hi[32], lo[32];
+      float lc;
+      if constexpr (BF) {
+        lc = chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0, hi, lo);
+        const bool valid_row = tid < cur.rows_q;
+        const bool redo = valid_row && !(lc <= 0x1p32f);
+        if (__any_sync(0xffffffffu, redo)) {
+          const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
+          const float m_new = (c == 0) ? mx : fmaxf(m_run, mx);
+          if (c > 0) {
+            const float alpha = fast_exp2(m_run - m_new);
+            l_run *= alpha;
+            rescale_o(tO_row, alpha);
+          }
+          m_run = m_new;
+          lc = chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, false, hi, lo);
+        }
+      } else {
+        const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
+        if (c == 0) {
+          m_run = mx;
+        } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
+          const float m_new = fmaxf(m_run, mx);
+          const float alpha = fast_exp2(m_run - m_new);
+          l_run *= alpha;
+          rescale_o(tO_row, alpha);
+          m_run = m_new;
+        }
+        lc = chunk_weights<false>(tS_row, nk16, n_c, full, c2, m_run, false, hi, lo);
+      }
+      l_run += lc;
 #pragma unroll
       for (int g = 0; g < BN / 16; ++g) {
         if (g * 16 < nk16) {
-          float t[16];
-          tmem_ld16(tS + lane_off + g * 16, t);
-          if (full) {
-#pragma unroll
-            for (int i = 0; i < 16; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], t[i] * c2);
-          } else {
-#pragma unroll
-            for (int i = 0; i < 16; ++i)
-              if (g * 16 + i < n_c) mx4[i & 3] = fmaxf(mx4[i & 3], t[i] * c2);
-          }
+          tmem_st8(tS_row + g * 16, hi + g * 8);
+          tmem_st8(tS_row + g * 16 + 8, lo + g * 8);
         }
       }
-      const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      if (c == 0) {
-        m_run = mx;
-      } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
-        const float m_new = fmaxf(m_run, mx);
-        const float alpha = fast_exp2(m_run - m_new);
-        l_run *= alpha;
-#pragma unroll
-        for (int g = 0; g < HD / 16; ++g) {
-          float oc[16];
-          tmem_ld16(tO + lane_off + g * 16, oc);
-          uint32_t w[16];
-#pragma unroll
-          for (int i = 0; i < 16; ++i) w[i] = __float_as_uint(oc[i] * alpha);
-          tmem_st8(tO + lane_off + g * 16, w);
-          tmem_st8(tO + lane_off + g * 16 + 8, w + 8);
-        }
-        m_run = m_new;
-      }
-      float l4[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-      for (int g = 0; g < BN / 16; ++g) {
-        if (g * 16 < nk16) {
-          float t[16];
-          tmem_ld16(tS + lane_off + g * 16, t);
-          uint32_t hi[8], lo[8];
-#pragma unroll
-          for (int i = 0; i < 8; ++i) {
-            const int j = g * 16 + 2 * i;
-            float p0 = fast_exp2(fmaf(t[2 * i], c2, -m_run));
-            float p1 = fast_exp2(fmaf(t[2 * i + 1], c2, -m_run));
-            if (!full) {
-              p0 = (j < n_c) ? p0 : 0.f;
-              p1 = (j + 1 < n_c) ? p1 : 0.f;
-            }
-            l4[(2 * i) & 3] += p0;
-            l4[(2 * i + 1) & 3] += p1;
-            split2<BF == 1>(p0, p1, hi[i], lo[i]);
-          }
-          tmem_st8(tS + lane_off + g * 16, hi);
-          tmem_st8(tS + lane_off + g * 16 + 8, lo);
-        }
-      }
-      l_run += (l4[0] + l4[1]) + (l4[2] + l4[3]);
       tmem_st_wait();
     }
     tc_fence_before();
@@ -524,7 +597,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       }
     }
     if (c == cur.nchunks - 1) {
-      m_run = -INFINITY;
+      m_run = 0.f;
       l_run = 0.f;
     }
     // All TMEM reads of S/P and O are done before the next S MMA.
@@ -533,7 +606,6 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
 
     cur = nxt;
     c = nc;
-    qslot = nqslot;
     stage ^= 1;
   }
 
@@ -542,6 +614,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     // Give our own copies and MMAs in flight a bounded chance to land.
     for (int st = 0; st < STAGES; ++st)
       if (load_pending[st]) mbar_wait(bar_load(st), ph_load[st], WAIT_LIMIT_CYCLES / 8);
+    if (q_pending) mbar_wait(bar_q, ph_q, WAIT_LIMIT_CYCLES / 8);
     if (mma_pending) mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES / 8);
   }
   tc_fence_before();
