@@ -474,27 +474,30 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     const bool full = (n_c == BN);
     const bool rows_here = warp * 32 < cur.rows_q;   // warp-uniform
 
-    if (c == 0) {
-      bad |= !mbar_wait(bar_q, ph_q, WAIT_LIMIT_CYCLES);
-      if (!bad) { ph_q ^= 1; q_pending = false; }
-    }
-    bad |= !mbar_wait(bar_load(stage), ph_load[stage], WAIT_LIMIT_CYCLES);
-    if (!bad) { ph_load[stage] ^= 1; load_pending[stage] = false; }
-    // V rows [n_c, nk16) enter the MMA with p = 0: make them exact zeros.
-    if (tid < (nk16 - n_c) * 8)
-      st_shared_v4(sV(stage) + (n_c + (tid >> 3)) * 128 + (tid & 7) * 16, 0u, 0u, 0u, 0u);
-    fence_proxy_async();
-    if (__syncthreads_or(bad)) { abort = true; break; }
-
-    // S = Q K^T -> TMEM columns [0, nk16)
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
+    // Warp 0 alone waits for the loads, zeroes the V rows [n_c, nk16) that
+    // enter the MMA with p = 0, and thread 0 issues S = Q K^T -> TMEM
+    // columns [0, nk16).  The other warps go straight to the MMA barrier.
+    if (warp == 0) {
+      if (c == 0) {
+        bad |= !mbar_wait(bar_q, ph_q, WAIT_LIMIT_CYCLES);
+        if (!bad) { ph_q ^= 1; q_pending = false; }
+      }
+      bad |= !mbar_wait(bar_load(stage), ph_load[stage], WAIT_LIMIT_CYCLES);
+      if (!bad) { ph_load[stage] ^= 1; load_pending[stage] = false; }
+      const int zvec = (nk16 - n_c) * 8;
+      for (int zi = tid; zi < zvec; zi += 32)
+        st_shared_v4(sV(stage) + (n_c + (zi >> 3)) * 128 + (zi & 7) * 16, 0u, 0u, 0u, 0u);
+      fence_proxy_async();
+      __syncwarp();
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
 #pragma unroll
-      for (int kk = 0; kk < HD / 16; ++kk)
-        umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(stage) + kk * 32, 16, 1024), idesc_s,
-                 kk > 0 ? 1u : 0u);
-      umma_commit(bar_mma);
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(stage) + kk * 32, 16, 1024), idesc_s,
+                   kk > 0 ? 1u : 0u);
+        umma_commit(bar_mma);
+      }
     }
     mma_pending = true;
     bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
@@ -600,9 +603,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       m_run = 0.f;
       l_run = 0.f;
     }
-    // All TMEM reads of S/P and O are done before the next S MMA.
-    tc_fence_before();
-    if (__syncthreads_or(bad)) { abort = true; break; }
+    // No barrier here: the next S product overwrites S/P only after thread 0
+    // has seen this P.V product complete, and the next unit's first P.V
+    // (which overwrites O) waits behind the next P-ready barrier.
 
     cur = nxt;
     c = nc;
@@ -612,9 +615,11 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   if (abort) {
     if (tid == 0) record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
     // Give our own copies and MMAs in flight a bounded chance to land.
-    for (int st = 0; st < STAGES; ++st)
-      if (load_pending[st]) mbar_wait(bar_load(st), ph_load[st], WAIT_LIMIT_CYCLES / 8);
-    if (q_pending) mbar_wait(bar_q, ph_q, WAIT_LIMIT_CYCLES / 8);
+    if (warp == 0) {
+      for (int st = 0; st < STAGES; ++st)
+        if (load_pending[st]) mbar_wait(bar_load(st), ph_load[st], WAIT_LIMIT_CYCLES / 8);
+      if (q_pending) mbar_wait(bar_q, ph_q, WAIT_LIMIT_CYCLES / 8);
+    }
     if (mma_pending) mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES / 8);
   }
   tc_fence_before();
