@@ -7,7 +7,7 @@
 // (attention computed directly on the compact buffer).
 //
 // Work unit = (image b, head h, tile of 128 query rows).  Persistent CTAs of
-// 128 threads (three per SM) walk the units with a grid stride; a unit whose
+// 128 threads (four per SM) walk the units with a grid stride; a unit whose
 // tile starts past the image's length (read from cu_seqlens on the device)
 // costs two loads and is skipped.  Per unit, keys stream in chunks of 64:
 //
@@ -50,7 +50,7 @@ constexpr int BN = 64;         // keys per chunk
 constexpr int HD = 64;         // head dim
 constexpr int THREADS = 128;
 constexpr int BOX = 32;        // rows per TMA box
-constexpr int CTAS_PER_SM = 3;
+constexpr int CTAS_PER_SM = 4;
 constexpr int STAGES = 2;      // K/V chunk ring
 
 constexpr uint32_t Q_BYTES = BM * 128;                 // 128 rows x 128 B
@@ -218,6 +218,14 @@ __device__ __forceinline__ void split2(float x, float y, uint32_t& hi, uint32_t&
   }
 }
 
+__device__ __forceinline__ void st_shared_u32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
 __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t b, uint32_t c, uint32_t d) {
   asm volatile("st.shared.v4.b32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "r"(a), "r"(b), "r"(c), "r"(d)
                : "memory");
@@ -309,13 +317,14 @@ __device__ __forceinline__ void split2_bf16_trunc(float p0, float p1, uint32_t& 
   lo = *reinterpret_cast<uint32_t*>(&l);
 }
 
-// Exponentials of one S row chunk against reference mref, packed as P hi/lo
-// pairs in registers; returns the chunk's row sum.  With ref_first the
+// Exponentials of one S row chunk against reference mref, written back over
+// S in TMEM as P hi/lo pairs (each 16-column piece of S becomes 8 hi + 8 lo
+// columns in place); returns the chunk's row sum.  With ref_first the
 // reference is replaced by this row's first score (so that weight is exactly
 // 1: a one-token image returns V bit for bit) and written back to mref.
 template <bool BF16>
 __device__ __forceinline__ float chunk_weights(uint32_t tS_row, int nk16, int n_c, bool full, float c2, float& mref,
-                                               bool ref_first, uint32_t (&hi)[32], uint32_t (&lo)[32]) {
+                                               bool ref_first) {
   float l4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
   for (int g = 0; g < BN / 16; ++g) {
@@ -323,6 +332,7 @@ __device__ __forceinline__ float chunk_weights(uint32_t tS_row, int nk16, int n_
       float t[16];
       tmem_ld16(tS_row + g * 16, t);
       if (g == 0 && ref_first) mref = t[0] * c2;
+      uint32_t hi[8], lo[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
         const int j = g * 16 + 2 * i;
@@ -334,9 +344,11 @@ __device__ __forceinline__ float chunk_weights(uint32_t tS_row, int nk16, int n_
         }
         l4[(2 * i) & 3] += p0;
         l4[(2 * i + 1) & 3] += p1;
-        if constexpr (BF16) split2_bf16_trunc(p0, p1, hi[g * 8 + i], lo[g * 8 + i]);
-        else split2<false>(p0, p1, hi[g * 8 + i], lo[g * 8 + i]);
+        if constexpr (BF16) split2_bf16_trunc(p0, p1, hi[i], lo[i]);
+        else split2<false>(p0, p1, hi[i], lo[i]);
       }
+      tmem_st8(tS_row + g * 16, hi);
+      tmem_st8(tS_row + g * 16 + 8, lo);
     }
   }
   return (l4[0] + l4[1]) + (l4[2] + l4[3]);
@@ -453,6 +465,12 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     load_pending[0] = true;
   }
   float m_run = 0.f, l_run = 0.f;   // this row's reference max (log2 units) and sum
+  uint32_t iter = 0;                // chunk iterations done (selects the redo flag word)
+  if (tid == 0) {
+    st_shared_u32(base + OFF_BAR + 40, 0u);
+    st_shared_u32(base + OFF_BAR + 44, 0u);
+  }
+  __syncthreads();
 
   while (cur.u < units) {
     // Prefetch the next item's K/V into the other stage while this one computes.
@@ -503,38 +521,25 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
     if (!bad) { ph_mma ^= 1; mma_pending = false; }
     tc_fence_after();
-    // The unit's last S product is done: its Q buffer can take the next unit's tile.
-    if (nc == 0 && have_next) {
-      if (tid == 0 && !bad) issue_q(nxt);
-      q_pending = true;
-    }
-
     // Softmax on this thread's row (TMEM lane).  Exponentials are taken
     // against a per-row reference m_run (log2 units) and O accumulates in
     // TMEM across chunks.  bf16: one pass, the reference being the row's first
-    // score on the first chunk and the running reference after; only when a
-    // row's chunk sum exceeds 2^32 is the chunk redone exactly (true max, O
-    // rescaled).  fp16 (narrower
-    // range for P): max pass first, rescale when the max grows by > 8.
+    // score on the first chunk and the running reference after, P written
+    // over S at once; a row whose chunk sum exceeds 2^32 flags a redo, and
+    // then the whole CTA recomputes S and this chunk (exact max and O rescale
+    // for the flagged rows).  fp16 (narrower range for P): max pass first,
+    // rescale when the max grows by > 8.
+    const uint32_t tS_row = tS + lane_off, tO_row = tO + lane_off;
+    const float l_before = l_run, m_before = m_run;
+    // Redo flag of this chunk: two words used alternately, set to iter + 1,
+    // so a stale value from two chunks back never reads as set (no reset).
+    const uint32_t flag = base + OFF_BAR + 40 + (iter & 1) * 4;
+    bool redo_row = false;
     if (rows_here) {
-      const uint32_t tS_row = tS + lane_off, tO_row = tO + lane_off;
-      uint32_t hi[32], lo[32];
-      float lc;
       if constexpr (BF) {
-        lc = chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0, hi, lo);
-        const bool valid_row = tid < cur.rows_q;
-        const bool redo = valid_row && !(lc <= 0x1p32f);
-        if (__any_sync(0xffffffffu, redo)) {
-          const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
-          const float m_new = (c == 0) ? mx : fmaxf(m_run, mx);
-          if (c > 0) {
-            const float alpha = fast_exp2(m_run - m_new);
-            l_run *= alpha;
-            rescale_o(tO_row, alpha);
-          }
-          m_run = m_new;
-          lc = chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, false, hi, lo);
-        }
+        l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0);
+        redo_row = (tid < cur.rows_q) && !(l_run - l_before <= 0x1p32f);
+        if (__any_sync(0xffffffffu, redo_row) && (tid & 31) == 0) st_shared_u32(flag, iter + 1u);
       } else {
         const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
         if (c == 0) {
@@ -546,20 +551,54 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           rescale_o(tO_row, alpha);
           m_run = m_new;
         }
-        lc = chunk_weights<false>(tS_row, nk16, n_c, full, c2, m_run, false, hi, lo);
-      }
-      l_run += lc;
-#pragma unroll
-      for (int g = 0; g < BN / 16; ++g) {
-        if (g * 16 < nk16) {
-          tmem_st8(tS_row + g * 16, hi + g * 8);
-          tmem_st8(tS_row + g * 16 + 8, lo + g * 8);
-        }
+        l_run += chunk_weights<false>(tS_row, nk16, n_c, full, c2, m_run, false);
       }
       tmem_st_wait();
     }
     tc_fence_before();
     if (__syncthreads_or(bad)) { abort = true; break; }
+    if (BF && ld_shared_u32(flag) == iter + 1u) {
+      // Rare: recompute S, then every warp rewrites its P; flagged warps
+      // switch to the exact max (rescaling O for later chunks).
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk)
+          umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(stage) + kk * 32, 16, 1024), idesc_s,
+                   kk > 0 ? 1u : 0u);
+        umma_commit(bar_mma);
+      }
+      mma_pending = true;
+      bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
+      if (!bad) { ph_mma ^= 1; mma_pending = false; }
+      tc_fence_after();
+      if (rows_here) {
+        l_run = l_before;
+        m_run = m_before;
+        if (__any_sync(0xffffffffu, redo_row)) {
+          const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
+          const float m_new = (c == 0) ? mx : fmaxf(m_before, mx);
+          if (c > 0) {
+            const float alpha = fast_exp2(m_before - m_new);
+            l_run *= alpha;
+            rescale_o(tO_row, alpha);
+          }
+          m_run = m_new;
+          l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, false);
+        } else {
+          l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0);
+        }
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      if (__syncthreads_or(bad)) { abort = true; break; }
+    }
+    // The unit's last S product is final: its Q buffer can take the next unit's tile.
+    if (nc == 0 && have_next) {
+      if (tid == 0 && !bad) issue_q(nxt);
+      q_pending = true;
+    }
 
     // O += P_hi V + P_lo V in TMEM columns [64, 128) (fresh on a unit's first chunk)
     if (tid == 0) {
@@ -610,6 +649,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     cur = nxt;
     c = nc;
     stage ^= 1;
+    ++iter;
   }
 
   if (abort) {
