@@ -68,13 +68,14 @@ def make_case(name: str, pruning: float | None = None):
 
 
 def case_bytes(case, out_bytes_per_el=None):
-    """Algorithmic bytes per launch (attend, pack, fused minimum) and attention FLOPs."""
+    """Algorithmic bytes per launch (attend, index pass, pack with copy, fused minimum) and FLOPs."""
     B, N, H, d = case.B, case.N, case.H, case.d
     s = case.q.element_size()
     so = out_bytes_per_el or s
     T = case.kept_tokens
     return dict(
         attend=3 * T * H * d * s + T * H * d * so,
+        index=B * N + (B * N - T) * H * d * so + 4 * (B + 1) + 4 * B * N + 4 * T,
         pack=B * N + 2 * 3 * T * H * d * s + (B * N - T) * H * d * so + 4 * (B + 1) + 4 * B * N + 4 * T,
         fused_min=B * N + 3 * T * H * d * s + B * N * H * d * so + 12 * B * N,
         flops=4 * H * d * sum(n * n for n in case.lengths),
@@ -202,26 +203,44 @@ def graph_time_per_launch(fn_list, stream, reps=5):
     return statistics.median(times)
 
 
-def kernel_times(case, sets, rra, stream, n_launch=None):
-    """Per-launch device µs of the pack kernel and the attention kernel (cold inputs)."""
+def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
+    """Per-launch device µs of the pipeline's two kernels on cold inputs.
+
+    index: rra_pack without the row copy (indices + zero fill of pruned rows);
+    attend: rra_attend_gather (rows gathered from the padded q/k/v).
+    With packed=True also the packed path: rra_pack with the row copy and
+    rra_attend on the packed buffers."""
     B, N, H, d = case.B, case.N, case.H, case.d
     R = sets.R
     n_launch = n_launch or max(R, 64)
     views = [rra.workspace_views(s[5], B, N, H, d, case.dtype) for s in sets.sets]
 
-    def pack_fn(i):
+    def index_fn(i):
         keep, q, k, v, out, ws = sets.sets[i % R]
         cu, dst, src, qp, kp, vp = views[i % R]
-        return lambda: rra.pack(keep, q, k, v, cu, dst, src, qp, kp, vp, out, stream=stream)
+        return lambda: rra.pack(keep, q, k, v, cu, dst, src, out_zero_fill=out, stream=stream)
 
-    def attend_fn(i):
+    def gather_fn(i):
         keep, q, k, v, out, ws = sets.sets[i % R]
         cu, dst, src, qp, kp, vp = views[i % R]
-        return lambda: rra.attend(qp, kp, vp, cu, B, N, out, scale=SCALE, src_idx=src, N=N, stream=stream)
+        return lambda: rra.attend_gather(q, k, v, cu, src, out, scale=SCALE, stream=stream)
 
-    t_pack = graph_time_per_launch([pack_fn(i) for i in range(n_launch)], stream)
-    t_attend = graph_time_per_launch([attend_fn(i) for i in range(n_launch)], stream)
-    return t_pack, t_attend
+    res = {"index_us": graph_time_per_launch([index_fn(i) for i in range(n_launch)], stream),
+           "attend_us": graph_time_per_launch([gather_fn(i) for i in range(n_launch)], stream)}
+    if packed:
+        def pack_fn(i):
+            keep, q, k, v, out, ws = sets.sets[i % R]
+            cu, dst, src, qp, kp, vp = views[i % R]
+            return lambda: rra.pack(keep, q, k, v, cu, dst, src, qp, kp, vp, out, stream=stream)
+
+        def attend_fn(i):
+            keep, q, k, v, out, ws = sets.sets[i % R]
+            cu, dst, src, qp, kp, vp = views[i % R]
+            return lambda: rra.attend(qp, kp, vp, cu, B, N, out, scale=SCALE, src_idx=src, N=N, stream=stream)
+
+        res["pack_copy_us"] = graph_time_per_launch([pack_fn(i) for i in range(n_launch)], stream)
+        res["attend_packed_us"] = graph_time_per_launch([attend_fn(i) for i in range(n_launch)], stream)
+    return res
 
 
 def roofline_obj(bytes_alg, flops, us, peaks):
@@ -450,13 +469,18 @@ def run_rra(args, world, rank, local):
     e2e_value = T * args.steps * world / (e2e_ms * 1e-3)
 
     # per-kernel device time (graph of back-to-back launches on cold inputs)
-    t_pack, t_attend = kernel_times(case, sets, rra, stream)
+    mma = args.attend_kernel == "mma_sync"
+    kt = kernel_times(case, sets, rra, stream, packed=mma)
+    if mma:   # the pipeline runs the packed path: pack with the row copy, then mma.sync attention
+        kt = {"index_us": kt["pack_copy_us"], "attend_us": kt["attend_packed_us"]}
     by = case_bytes(case)
-    kern = {"pack_us": round(t_pack, 3), "attend_us": round(t_attend, 3)}
-    if t_attend >= t_pack:
-        dom, roof = "attend", roofline_obj(by["attend"], by["flops"], t_attend, peaks)
+    if mma:
+        by["index"] = by["pack"]
+    kern = {k: round(v, 3) for k, v in kt.items()}
+    if kt["attend_us"] >= kt["index_us"]:
+        dom, roof = "attend_tc_kernel (gather)", roofline_obj(by["attend"], by["flops"], kt["attend_us"], peaks)
     else:
-        dom, roof = "pack", roofline_obj(by["pack"], 0, t_pack, peaks)
+        dom, roof = "pack_kernel (index pass)", roofline_obj(by["index"], 0, kt["index_us"], peaks)
     roof["kernel"] = dom
     roof["peak_source"] = peaks["source"]
 
@@ -465,11 +489,13 @@ def run_rra(args, world, rank, local):
         extra["host_us"] = {f"bs{b}": host_latency(rra, b, stream) for b in W.SERVING_BATCHES}
         big, big_desc = make_case("batched")
         big_sets = InputSets(big, device, rra, big.dtype)
-        bp, ba = kernel_times(big, big_sets, rra, stream)
+        bk = kernel_times(big, big_sets, rra, stream)
         bb = case_bytes(big)
-        extra["batched_b64_p80"] = {"workload": big_desc, "pack_us": round(bp, 3), "attend_us": round(ba, 3),
-                                    "attend_roofline": roofline_obj(bb["attend"], bb["flops"], ba, peaks),
-                                    "pipeline_tokens_per_s": round(big.kept_tokens / ((bp + ba) * 1e-6), 1)}
+        extra["batched_b64_p80"] = {"workload": big_desc, "index_us": round(bk["index_us"], 3),
+                                    "attend_us": round(bk["attend_us"], 3),
+                                    "attend_roofline": roofline_obj(bb["attend"], bb["flops"], bk["attend_us"], peaks),
+                                    "pipeline_tokens_per_s": round(big.kept_tokens /
+                                                                   ((bk["index_us"] + bk["attend_us"]) * 1e-6), 1)}
         del big_sets
 
     cpu = None
@@ -525,17 +551,22 @@ def run_sweep(args):
     cases += [W.make_progressive_layer(L, masks) for L in (1, 4, 7, 10)]
     for case in cases:
         sets = InputSets(case, device, rra, case.dtype)
-        tp, ta = kernel_times(case, sets, rra, stream)
+        mma = args.attend_kernel == "mma_sync"
+        kt = kernel_times(case, sets, rra, stream, packed=True)
+        if mma:   # the pipeline runs the packed path with the mma.sync attention
+            kt = {"index_us": kt["pack_copy_us"], "attend_us": kt["attend_packed_us"]}
         by = case_bytes(case)
         roof_t = max(by["attend"] / (peaks["hbm_gbs"] * 1e9), by["flops"] / (peaks["bf16_tflops"] * 1e12)) * 1e6
         fused_t = by["fused_min"] / (peaks["hbm_gbs"] * 1e9) * 1e6
-        print(json.dumps({"kernel": args.attend_kernel, "case": case.name, "B": case.B, "N": case.N, "H": case.H, "T": case.kept_tokens,
-                          "pack_us": round(tp, 3), "attend_us": round(ta, 3),
-                          "attend_roofline_us": round(roof_t, 3), "attend_frac": round(roof_t / ta, 4),
-                          "attend": roofline_obj(by["attend"], by["flops"], ta, peaks),
-                          "pipeline_us": round(tp + ta, 3), "pipeline_fused_min_us": round(fused_t, 3),
-                          "pipeline_frac_of_fused_min": round(fused_t / (tp + ta), 4),
-                          "tokens_per_s": round(case.kept_tokens / ((tp + ta) * 1e-6), 1)}), flush=True)
+        pipe = kt["index_us"] + kt["attend_us"]
+        line = {"kernel": args.attend_kernel, "case": case.name, "B": case.B, "N": case.N, "H": case.H,
+                "T": case.kept_tokens, **{k: round(v, 3) for k, v in kt.items()},
+                "attend_roofline_us": round(roof_t, 3), "attend_frac": round(roof_t / kt["attend_us"], 4),
+                "attend": roofline_obj(by["attend"], by["flops"], kt["attend_us"], peaks),
+                "pipeline_us": round(pipe, 3), "pipeline_fused_min_us": round(fused_t, 3),
+                "pipeline_frac_of_fused_min": round(fused_t / pipe, 4),
+                "tokens_per_s": round(case.kept_tokens / (pipe * 1e-6), 1)}
+        print(json.dumps(line), flush=True)
         del sets
     return 0
 

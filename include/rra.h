@@ -96,7 +96,9 @@ RRA_API rra_status rra_workspace_offsets(int B, int N, int H, int d, rra_dtype i
  *   out_zero_fill   = optional [B, N, H, d] tensor of `out_dtype`: its rows at
  *                     pruned positions are set to +0 (the unpack's fill, done
  *                     here so a scattering rra_attend completes the output).
- * Packed order is images in batch order, tokens in original order. */
+ * Packed order is images in batch order, tokens in original order.  With
+ * qp, kp and vp all NULL only the indices and the zero fill are produced
+ * (q, k and v are then not read) -- the index pass of rra_pipeline. */
 RRA_API rra_status rra_pack(const uint8_t* keep, int B, int N, int H, int d, rra_dtype in_dtype,
                             const void* q, const void* k, const void* v,
                             int32_t* cu_seqlens, int32_t* dst_idx, int32_t* src_idx,
@@ -122,17 +124,36 @@ RRA_API rra_status rra_attend(const void* qp, const void* kp, const void* vp,
                               float scale, rra_dtype in_dtype, void* o, rra_dtype out_dtype,
                               const int32_t* src_idx, int N, void* stream);
 
+/* The same attention without a packed copy of the inputs: row t of image
+ * b's sequence is read straight from the padded q/k/v [B, N, H, d] at flat
+ * position src_idx[t] (TMA gather of 4 rows at a time) and the output row
+ * is written to out [B, N, H, d] at the same position (rows at pruned
+ * positions untouched).  cu_seqlens and src_idx are rra_pack's; every
+ * image's length must be <= N.  This is rra_pipeline's attention step
+ * (method overview, bullets 2-3, with the pack's row copy folded into the
+ * attention's tile loads). */
+RRA_API rra_status rra_attend_gather(const void* q, const void* k, const void* v,
+                                     const int32_t* cu_seqlens, const int32_t* src_idx, int B, int N,
+                                     int H, int d, float scale, rra_dtype in_dtype, void* out,
+                                     rra_dtype out_dtype, void* stream);
+
 /* Unpack (method overview, bullet 3): out[b, j] = op[dst_idx[b*N+j]] when
  * dst_idx >= 0, else +0.  `op` is packed [cap, H, d] and `out` padded
  * [B, N, H, d], both of `dtype` (F16, BF16 or F32). */
 RRA_API rra_status rra_unpack(const void* op, const int32_t* dst_idx, int B, int N, int H, int d,
                               rra_dtype dtype, void* out, void* stream);
 
-/* The whole path: rra_pack (with out_zero_fill = out) then rra_attend
- * scattering into `out` [B, N, H, d] of out_dtype.  Two kernel launches, no
- * host synchronisation.  `workspace` holds rra_workspace_bytes() bytes laid
- * out as rra_workspace_offsets() states; after the call it holds
- * cu_seqlens, the pack indices and the packed Q/K/V. */
+/* The whole path, two kernel launches, no host synchronisation, `out`
+ * [B, N, H, d] of out_dtype.  With the default tcgen05 attention kernel:
+ * an index pass (rra_pack's cu_seqlens / dst_idx / src_idx and zero fill of
+ * pruned output rows, without the row copy), then attention that gathers
+ * the kept Q/K/V rows straight from q/k/v (TMA gather4 on rows src_idx)
+ * and scatters its rows into `out`; the packed sections of the workspace
+ * are not written.  With RRA_ATTEND_MMA_SYNC selected: rra_pack (with the
+ * row copy) then rra_attend on the packed buffers.  `workspace` holds
+ * rra_workspace_bytes() bytes laid out as rra_workspace_offsets() states;
+ * after the call its first three sections hold cu_seqlens and the pack
+ * indices. */
 RRA_API rra_status rra_pipeline(const uint8_t* keep, const void* q, const void* k, const void* v,
                                 int B, int N, int H, int d, float scale, rra_dtype in_dtype,
                                 void* out, rra_dtype out_dtype,

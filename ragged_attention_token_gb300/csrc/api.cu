@@ -119,7 +119,7 @@ rra_status enqueue_pack(const DeviceState& st, const uint8_t* keep, int B, int N
   a.keep = keep;
   a.B = B;
   a.N = N;
-  a.row_vecs = H * d * dtype_bytes(in) / 16;
+  a.row_vecs = (qp != nullptr) ? H * d * dtype_bytes(in) / 16 : 0;   // 0: indices and zero fill only
   a.out_row_vecs = outz ? H * d * dtype_bytes(out_dt) / 16 : 0;
   a.q = static_cast<const uint4*>(q);
   a.k = static_cast<const uint4*>(k);
@@ -202,6 +202,30 @@ rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaSt
   int32_t* cu = reinterpret_cast<int32_t*>(ws + off[0]);
   int32_t* dst = reinterpret_cast<int32_t*>(ws + off[1]);
   int32_t* src = reinterpret_cast<int32_t*>(ws + off[2]);
+  if (g_attend_kernel.load() == RRA_ATTEND_TCGEN05) {
+    // Index pass (cu_seqlens, pack indices, zero fill of pruned output rows),
+    // then attention gathering the kept rows straight from q/k/v.
+    if (!attend_tc_available())
+      return fail(RRA_ERR_CUDA, "pipeline: the driver's tensor-map encoder is unavailable");
+    RRA_TRY(enqueue_pack(st, p.keep, p.B, p.N, p.H, p.d, p.in, p.q, p.k, p.v, cu, dst, src, nullptr, nullptr,
+                         nullptr, p.out, p.out_dt, s));
+    AttendArgs a{};
+    a.qp = p.q;
+    a.kp = p.k;
+    a.vp = p.v;
+    a.cu_seqlens = cu;
+    a.src_idx = src;
+    a.o = p.out;
+    a.B = p.B;
+    a.H = p.H;
+    a.N = p.N;
+    a.max_seqlen = p.N;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    a.err = st.err;
+    cudaError_t e = launch_attend_tc_gather(a, p.in, p.out_dt, st.num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "attend (gather) launch");
+    return RRA_OK;
+  }
   void* qp = ws + off[3];
   void* kp = ws + off[4];
   void* vp = ws + off[5];
@@ -273,12 +297,15 @@ rra_status rra_pack(const uint8_t* keep, int B, int N, int H, int d, rra_dtype i
   if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
   if (out_zero_fill && !valid_out(out_dtype)) return fail(RRA_ERR_INVALID_ARG, "output dtype invalid");
   if (keep == nullptr) return fail(RRA_ERR_INVALID_ARG, "keep is null");
-  RRA_CHECK_PTR(q);
-  RRA_CHECK_PTR(k);
-  RRA_CHECK_PTR(v);
-  RRA_CHECK_PTR(qp);
-  RRA_CHECK_PTR(kp);
-  RRA_CHECK_PTR(vp);
+  const bool index_only = (qp == nullptr && kp == nullptr && vp == nullptr);
+  if (!index_only) {
+    RRA_CHECK_PTR(q);
+    RRA_CHECK_PTR(k);
+    RRA_CHECK_PTR(v);
+    RRA_CHECK_PTR(qp);
+    RRA_CHECK_PTR(kp);
+    RRA_CHECK_PTR(vp);
+  }
   if (cu_seqlens == nullptr || dst_idx == nullptr || src_idx == nullptr)
     return fail(RRA_ERR_INVALID_ARG, "index buffer is null");
   if (out_zero_fill && !aligned16(out_zero_fill))
@@ -308,6 +335,40 @@ rra_status rra_attend(const void* qp, const void* kp, const void* vp, const int3
   RRA_TRY(device_state(&st));
   RRA_TRY(enqueue_attend(*st, qp, kp, vp, cu_seqlens, B, max_seqlen, H, scale, in_dtype, o, out_dtype,
                          src_idx, src_idx ? N : 0, static_cast<cudaStream_t>(stream)));
+  g_launches += 1;
+  return RRA_OK;
+}
+
+rra_status rra_attend_gather(const void* q, const void* k, const void* v, const int32_t* cu_seqlens,
+                             const int32_t* src_idx, int B, int N, int H, int d, float scale, rra_dtype in_dtype,
+                             void* out, rra_dtype out_dtype, void* stream) {
+  RRA_TRY(check_shape(B, N, H, d));
+  if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
+  if (!valid_out(out_dtype)) return fail(RRA_ERR_INVALID_ARG, "output dtype invalid");
+  if (!finite(scale)) return fail(RRA_ERR_INVALID_ARG, "scale is not finite");
+  RRA_CHECK_PTR(q);
+  RRA_CHECK_PTR(k);
+  RRA_CHECK_PTR(v);
+  RRA_CHECK_PTR(out);
+  if (cu_seqlens == nullptr || src_idx == nullptr) return fail(RRA_ERR_INVALID_ARG, "index buffer is null");
+  if (!attend_tc_available()) return fail(RRA_ERR_CUDA, "attend_gather: tensor-map encoder unavailable");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  AttendArgs a{};
+  a.qp = q;
+  a.kp = k;
+  a.vp = v;
+  a.cu_seqlens = cu_seqlens;
+  a.src_idx = src_idx;
+  a.o = out;
+  a.B = B;
+  a.H = H;
+  a.N = N;
+  a.max_seqlen = N;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = st->err;
+  cudaError_t e = launch_attend_tc_gather(a, in_dtype, out_dtype, st->num_sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attend (gather) launch");
   g_launches += 1;
   return RRA_OK;
 }

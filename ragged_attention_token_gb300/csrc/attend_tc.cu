@@ -109,6 +109,15 @@ __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map
       "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
       : "memory");
 }
+// TMA gather of 4 rows (row coordinates r[0..3]) of a 2-D map whose box is
+// one row of 64 elements; the rows land consecutively (4 x 128 B) at dst.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, const int (&r)[4], uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes [%0], [%1, {%2, "
+      "%3, %4, %5, %6}], [%7];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(0), "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(bar)
+      : "memory");
+}
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -389,7 +398,7 @@ __device__ __forceinline__ void rescale_o(uint32_t tO_row, float alpha) {
   }
 }
 
-template <typename Tin, typename Tout, bool SCATTER>
+template <typename Tin, typename Tout, bool SCATTER, bool GATHER>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const AttendArgs a, int qtiles, int units) {
@@ -429,22 +438,56 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   const float c2 = a.scale_log2;
   (void)qtiles;
 
-  // TMA issue (thread 0 only): K/V rows of (unit x, chunk c) into stage st;
-  // the unit's Q tile into the single Q buffer.
+  // TMA issue, called by all 32 lanes of warp 0: K/V rows of (unit x, chunk
+  // c) into stage st; the unit's Q tile into the single Q buffer.  Packed
+  // inputs: 32-row boxes of the [T, H, 64] map (lane 0).  Gathered inputs:
+  // rows src_idx[t] * H + h of the padded [B*N*H, 64] map, 4 per gather4
+  // (one lane per group); the last group repeats the chunk's last row so
+  // every row the MMA reads is a finite input row.
+  const int lane = tid & 31;
   auto issue_kv = [&](const Unit& x, int c, int st) {
     const int k0 = c * BN;
     const int n_c = min(BN, x.n - k0);
-    const int kboxes = (n_c + BOX - 1) / BOX;
-    mbar_expect_tx(bar_load(st), static_cast<uint32_t>(2 * kboxes * BOX * 128));
-    for (int j = 0; j < kboxes; ++j) {
-      tma_load_3d(sK(st) + j * BOX * 128, &tmap_k, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
-      tma_load_3d(sV(st) + j * BOX * 128, &tmap_v, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
+    if constexpr (GATHER) {
+      const int groups = ((n_c + 15) & ~15) / 4;
+      if (lane == 0) mbar_expect_tx(bar_load(st), static_cast<uint32_t>(2 * groups * 4 * 128));
+      __syncwarp();
+      const int g = lane & 15;
+      if (g < groups) {
+        int rows[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          rows[i] = __ldg(a.src_idx + x.s0 + min(k0 + 4 * g + i, k0 + n_c - 1)) * a.H + x.h;
+        if (lane < 16) tma_gather4(sK(st) + g * 512, &tmap_k, rows, bar_load(st));
+        else tma_gather4(sV(st) + g * 512, &tmap_v, rows, bar_load(st));
+      }
+    } else if (lane == 0) {
+      const int kboxes = (n_c + BOX - 1) / BOX;
+      mbar_expect_tx(bar_load(st), static_cast<uint32_t>(2 * kboxes * BOX * 128));
+      for (int j = 0; j < kboxes; ++j) {
+        tma_load_3d(sK(st) + j * BOX * 128, &tmap_k, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
+        tma_load_3d(sV(st) + j * BOX * 128, &tmap_v, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
+      }
     }
   };
   auto issue_q = [&](const Unit& x) {
-    const int qboxes = (x.rows_q + BOX - 1) / BOX;
-    mbar_expect_tx(bar_q, static_cast<uint32_t>(qboxes * BOX * 128));
-    for (int j = 0; j < qboxes; ++j) tma_load_3d(sQ + j * BOX * 128, &tmap_q, 0, x.h, x.s0 + x.q0 + j * BOX, bar_q);
+    if constexpr (GATHER) {
+      const int groups = (x.rows_q + 3) / 4;
+      if (lane == 0) mbar_expect_tx(bar_q, static_cast<uint32_t>(groups * 4 * 128));
+      __syncwarp();
+      if (lane < groups) {
+        int rows[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          rows[i] = __ldg(a.src_idx + x.s0 + min(x.q0 + 4 * lane + i, x.q0 + x.rows_q - 1)) * a.H + x.h;
+        tma_gather4(sQ + lane * 512, &tmap_q, rows, bar_q);
+      }
+    } else if (lane == 0) {
+      const int qboxes = (x.rows_q + BOX - 1) / BOX;
+      mbar_expect_tx(bar_q, static_cast<uint32_t>(qboxes * BOX * 128));
+      for (int j = 0; j < qboxes; ++j)
+        tma_load_3d(sQ + j * BOX * 128, &tmap_q, 0, x.h, x.s0 + x.q0 + j * BOX, bar_q);
+    }
   };
 
   uint32_t ph_load[STAGES] = {0u, 0u};
@@ -457,7 +500,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   Unit cur = next_unit(blockIdx.x, step, units, BH, a, tid);
   int c = 0, stage = 0;
   if (cur.u < units) {
-    if (tid == 0) {
+    if (warp == 0) {
       issue_q(cur);
       issue_kv(cur, 0, 0);
     }
@@ -481,10 +524,6 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       nc = 0;
     }
     const bool have_next = nxt.u < units;
-    if (have_next) {
-      if (tid == 0) issue_kv(nxt, nc, stage ^ 1);
-      load_pending[stage ^ 1] = true;
-    }
 
     const int k0 = c * BN;
     const int n_c = min(BN, cur.n - k0);
@@ -502,10 +541,12 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       }
       bad |= !mbar_wait(bar_load(stage), ph_load[stage], WAIT_LIMIT_CYCLES);
       if (!bad) { ph_load[stage] ^= 1; load_pending[stage] = false; }
-      const int zvec = (nk16 - n_c) * 8;
-      for (int zi = tid; zi < zvec; zi += 32)
-        st_shared_v4(sV(stage) + (n_c + (zi >> 3)) * 128 + (zi & 7) * 16, 0u, 0u, 0u, 0u);
-      fence_proxy_async();
+      if constexpr (!GATHER) {
+        const int zvec = (nk16 - n_c) * 8;
+        for (int zi = tid; zi < zvec; zi += 32)
+          st_shared_v4(sV(stage) + (n_c + (zi >> 3)) * 128 + (zi & 7) * 16, 0u, 0u, 0u, 0u);
+        fence_proxy_async();
+      }
       __syncwarp();
       if (tid == 0) {
         tc_fence_after();
@@ -516,7 +557,12 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
                    kk > 0 ? 1u : 0u);
         umma_commit(bar_mma);
       }
+      __syncwarp();
+      // Prefetch the next item's K/V into the other stage (its last reader,
+      // the P.V product two items back, has completed) while S computes.
+      if (have_next) issue_kv(nxt, nc, stage ^ 1);
     }
+    if (have_next) load_pending[stage ^ 1] = true;
     mma_pending = true;
     bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
     if (!bad) { ph_mma ^= 1; mma_pending = false; }
@@ -596,7 +642,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     }
     // The unit's last S product is final: its Q buffer can take the next unit's tile.
     if (nc == 0 && have_next) {
-      if (tid == 0 && !bad) issue_q(nxt);
+      if (warp == 0) issue_q(nxt);
       q_pending = true;
     }
 
@@ -702,7 +748,20 @@ cudaError_t make_map(CUtensorMap* map, const void* ptr, int H, long long rows, b
 
 constexpr int kMaxDev = 64;
 
-template <typename Tin, typename Tout, bool SCATTER>
+// 2-D map over a padded [B*N*H, 64] tensor with a one-row box, for gather4.
+cudaError_t make_gather_map(CUtensorMap* map, const void* ptr, long long rows, bool bf16) {
+  cuuint64_t dims[2] = {static_cast<cuuint64_t>(HD), static_cast<cuuint64_t>(rows)};
+  cuuint64_t strides[1] = {static_cast<cuuint64_t>(HD * 2)};
+  cuuint32_t box[2] = {HD, 1};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = g_encode(map, bf16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2,
+                        const_cast<void*>(ptr), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                        CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                        CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
+template <typename Tin, typename Tout, bool SCATTER, bool GATHER>
 cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t stream) {
   static bool attr_set[kMaxDev] = {};
   static std::mutex m;
@@ -713,31 +772,46 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
   {
     std::lock_guard<std::mutex> lock(m);
     if (!attr_set[dev]) {
-      e = cudaFuncSetAttribute(attend_tc_kernel<Tin, Tout, SCATTER>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                               static_cast<int>(SMEM_ALLOC));
+      e = cudaFuncSetAttribute(attend_tc_kernel<Tin, Tout, SCATTER, GATHER>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_ALLOC));
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }
   }
   const bool bf16 = IsBf16<Tin>::value == 1;
-  const long long rows = static_cast<long long>(a.B) * a.max_seqlen;
   CUtensorMap mq, mk, mv;
-  if ((e = make_map(&mq, a.qp, a.H, rows, bf16)) != cudaSuccess) return e;
-  if ((e = make_map(&mk, a.kp, a.H, rows, bf16)) != cudaSuccess) return e;
-  if ((e = make_map(&mv, a.vp, a.H, rows, bf16)) != cudaSuccess) return e;
+  if constexpr (GATHER) {
+    const long long rows = static_cast<long long>(a.B) * a.N * a.H;
+    if ((e = make_gather_map(&mq, a.qp, rows, bf16)) != cudaSuccess) return e;
+    if ((e = make_gather_map(&mk, a.kp, rows, bf16)) != cudaSuccess) return e;
+    if ((e = make_gather_map(&mv, a.vp, rows, bf16)) != cudaSuccess) return e;
+  } else {
+    const long long rows = static_cast<long long>(a.B) * a.max_seqlen;
+    if ((e = make_map(&mq, a.qp, a.H, rows, bf16)) != cudaSuccess) return e;
+    if ((e = make_map(&mk, a.kp, a.H, rows, bf16)) != cudaSuccess) return e;
+    if ((e = make_map(&mv, a.vp, a.H, rows, bf16)) != cudaSuccess) return e;
+  }
   const int qtiles = (a.max_seqlen + BM - 1) / BM;
   const long long units = static_cast<long long>(a.B) * a.H * qtiles;
   const long long cap = static_cast<long long>(CTAS_PER_SM) * (num_sms > 0 ? num_sms : 152);
   const int grid = static_cast<int>(units < cap ? units : cap);
-  attend_tc_kernel<Tin, Tout, SCATTER><<<grid, THREADS, SMEM_ALLOC, stream>>>(mq, mk, mv, a, qtiles,
-                                                                              static_cast<int>(units));
+  attend_tc_kernel<Tin, Tout, SCATTER, GATHER><<<grid, THREADS, SMEM_ALLOC, stream>>>(
+      mq, mk, mv, a, qtiles, static_cast<int>(units));
   return cudaGetLastError();
 }
 
 template <typename Tin, typename Tout>
-cudaError_t launch_tc_out(const AttendArgs& a, int num_sms, cudaStream_t stream) {
-  if (a.src_idx != nullptr) return launch_tc_typed<Tin, Tout, true>(a, num_sms, stream);
-  return launch_tc_typed<Tin, Tout, false>(a, num_sms, stream);
+cudaError_t launch_tc_out(const AttendArgs& a, bool gather, int num_sms, cudaStream_t stream) {
+  if (gather) return launch_tc_typed<Tin, Tout, true, true>(a, num_sms, stream);
+  if (a.src_idx != nullptr) return launch_tc_typed<Tin, Tout, true, false>(a, num_sms, stream);
+  return launch_tc_typed<Tin, Tout, false, false>(a, num_sms, stream);
+}
+
+template <typename Tin>
+cudaError_t launch_tc_in(const AttendArgs& a, rra_dtype out, bool gather, int num_sms, cudaStream_t stream) {
+  if (out == RRA_BF16) return launch_tc_out<Tin, __nv_bfloat16>(a, gather, num_sms, stream);
+  if (out == RRA_F16) return launch_tc_out<Tin, __half>(a, gather, num_sms, stream);
+  return launch_tc_out<Tin, float>(a, gather, num_sms, stream);
 }
 
 }  // namespace
@@ -747,14 +821,16 @@ bool attend_tc_available() { return encode_fn(); }
 cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream) {
   if (!encode_fn()) return cudaErrorNotSupported;
   if (static_cast<long long>(a.B) * a.max_seqlen >= (1LL << 31)) return cudaErrorInvalidValue;
-  if (in == RRA_BF16) {
-    if (out == RRA_BF16) return launch_tc_out<__nv_bfloat16, __nv_bfloat16>(a, num_sms, stream);
-    if (out == RRA_F16) return launch_tc_out<__nv_bfloat16, __half>(a, num_sms, stream);
-    return launch_tc_out<__nv_bfloat16, float>(a, num_sms, stream);
-  }
-  if (out == RRA_BF16) return launch_tc_out<__half, __nv_bfloat16>(a, num_sms, stream);
-  if (out == RRA_F16) return launch_tc_out<__half, __half>(a, num_sms, stream);
-  return launch_tc_out<__half, float>(a, num_sms, stream);
+  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, false, num_sms, stream);
+  return launch_tc_in<__half>(a, out, false, num_sms, stream);
+}
+
+cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
+                                    cudaStream_t stream) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  if (a.src_idx == nullptr) return cudaErrorInvalidValue;
+  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, true, num_sms, stream);
+  return launch_tc_in<__half>(a, out, true, num_sms, stream);
 }
 
 }  // namespace rra

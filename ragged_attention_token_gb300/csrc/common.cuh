@@ -67,5 +67,9 @@ cudaError_t launch_unpack(const UnpackArgs& a, cudaStream_t stream);
 // tcgen05 + TMA attention; needs the driver's tensor-map encoder.
 bool attend_tc_available();
 cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream);
+// Same kernel reading Q/K/V rows straight from the padded [B, N, H, 64]
+// tensors (a.qp/kp/vp) at rows src_idx[t], scattering to the padded output.
+cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
+                                    cudaStream_t stream);
 
 }  // namespace rra

@@ -35,6 +35,7 @@ _SIGNATURES = {
     "rra_workspace_offsets": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "rra_pack": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp]),
     "rra_attend": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp]),
+    "rra_attend_gather": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "rra_unpack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "rra_pipeline": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
     "rra_pipeline_static": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
@@ -139,7 +140,9 @@ def workspace_views(ws: torch.Tensor, B: int, N: int, H: int, d: int, dtype: tor
     return (cu, dst, src, *packed)
 
 
-def pack(keep, q, k, v, cu_seqlens, dst_idx, src_idx, qp, kp, vp, out_zero_fill=None, stream=None):
+def pack(keep, q, k, v, cu_seqlens, dst_idx, src_idx, qp=None, kp=None, vp=None, out_zero_fill=None,
+         stream=None):
+    """rra_pack; with qp = kp = vp = None only the indices and the zero fill are produced."""
     B, N, H, d = q.shape
     out_dt = _DTYPE[out_zero_fill.dtype] if out_zero_fill is not None else RRA_F32
     _check(lib().rra_pack(_ptr(keep), B, N, H, d, _DTYPE[q.dtype], _ptr(q), _ptr(k), _ptr(v),
@@ -153,6 +156,13 @@ def attend(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, scale: float = 0.
     _check(lib().rra_attend(_ptr(qp), _ptr(kp), _ptr(vp), _ptr(cu_seqlens), B, max_seqlen, H, d,
                             float(scale), _DTYPE[qp.dtype], _ptr(o), _DTYPE[o.dtype], _ptr(src_idx), N,
                             _stream(stream)))
+
+
+def attend_gather(q, k, v, cu_seqlens, src_idx, out, scale: float = 0.125, stream=None):
+    """rra_attend_gather: attention reading rows src_idx of padded q/k/v, writing padded out."""
+    B, N, H, d = q.shape
+    _check(lib().rra_attend_gather(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(src_idx), B, N, H, d,
+                                   float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], _stream(stream)))
 
 
 def unpack(op, dst_idx, B: int, N: int, out, stream=None):

@@ -72,13 +72,33 @@ def run_pipeline(case, out_dtype=None, poison=True):
                 qp=qp.cpu(), kp=kp.cpu(), vp=vp.cpu(), err=err)
 
 
-def check_indices_and_packing(got, ref):
+def check_indices(got, ref):
     T = int(ref["cu"][-1])
     assert np.array_equal(got["cu"], ref["cu"]), "cu_seqlens differ"
     assert np.array_equal(got["dst"], ref["dst"]), "dst_idx differ"
     assert np.array_equal(got["src"][:T], ref["src"]), "src_idx differ"
+
+
+def check_indices_and_packing(got, ref):
+    check_indices(got, ref)
+    T = int(ref["cu"][-1])
     for name, g, r in zip(("q", "k", "v"), (got["qp"], got["kp"], got["vp"]), ref["packed_bits"]):
         assert np.array_equal(bits(g)[:T], r), f"packed {name} differs"
+
+
+def run_pack(case):
+    """rra_pack alone (row copy + indices + zero fill); CPU copies of its outputs."""
+    keep, q, k, v = to_device(case)
+    B, N, H, d = case.B, case.N, case.H, case.d
+    cu = torch.full((B + 1,), -9, dtype=torch.int32, device="cuda")
+    dst = torch.full((B * N,), -9, dtype=torch.int32, device="cuda")
+    src = torch.full((B * N,), -9, dtype=torch.int32, device="cuda")
+    qp, kp, vp = (torch.full((B * N, H, d), float("nan"), dtype=case.dtype, device="cuda") for _ in range(3))
+    out = torch.full((B, N, H, d), float("nan"), dtype=case.dtype, device="cuda")
+    rra.pack(keep, q, k, v, cu, dst, src, qp, kp, vp, out_zero_fill=out)
+    torch.cuda.synchronize()
+    return dict(cu=cu.cpu().numpy(), dst=dst.cpu().numpy(), src=src.cpu().numpy(), qp=qp.cpu(), kp=kp.cpu(),
+                vp=vp.cpu(), out=out.cpu())
 
 
 def check_output(out: torch.Tensor, keep: np.ndarray, ref_out: np.ndarray):

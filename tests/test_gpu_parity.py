@@ -14,7 +14,8 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import ATOL, SCALE, bits, check_indices_and_packing, check_output, oracle_result, run_pipeline
+from gpu_util import (ATOL, SCALE, bits, check_indices, check_indices_and_packing, check_output, oracle_result,
+                      run_pack, run_pipeline)
 from ragged_attention_token_gb300 import rra
 from ragged_attention_token_gb300 import workloads as W
 
@@ -66,7 +67,7 @@ def test_pipeline_full_size(name, make, kernel):
     for out_dtype in (case.dtype, torch.float32):
         got = run_pipeline(case, out_dtype)
         assert got["err"] == 0
-        check_indices_and_packing(got, ref)
+        check_indices(got, ref)
         err = check_output(got["out"], keep, ref["out"])
         if out_dtype == torch.float32:
             assert err <= ATOL
@@ -107,7 +108,7 @@ def test_pipeline_edge_cases(name, make, kernel):
     for out_dtype in (case.dtype, torch.float32):
         got = run_pipeline(case, out_dtype)
         assert got["err"] == 0
-        check_indices_and_packing(got, ref)
+        check_indices(got, ref)
         check_output(got["out"], keep, ref["out"])
 
 
@@ -203,7 +204,21 @@ def test_mask_values_any_nonzero_keeps():
     case.keep = (case.keep.to(torch.int32) * mult).to(torch.uint8)
     assert ((case.keep != 0).numpy() == (ref["dst"].reshape(case.B, case.N) >= 0)).all()
     got = run_pipeline(case)
+    check_indices(got, ref)
+
+
+@pytest.mark.parametrize("name,make", CASES + EDGE, ids=[c[0] for c in CASES + EDGE])
+def test_pack_bit_exact(name, make):
+    """rra_pack: indices, packed rows and the zero fill are bit copies of the oracle's."""
+    case = make()
+    ref = oracle_result(case)
+    got = run_pack(case)
     check_indices_and_packing(got, ref)
+    T = int(ref["cu"][-1])
+    assert (torch.from_numpy(got["src"][T:]) == -9).all()          # rows >= T untouched
+    m = case.keep.numpy() != 0
+    assert np.all(bits(got["out"])[~m] == 0)                        # pruned rows +0
+    assert np.all(np.isnan(got["out"].float().numpy()[m]))          # kept rows untouched
 
 
 def test_device_error_codes(kernel):
