@@ -320,6 +320,16 @@ def dist_setup(args):
     return world, rank, local
 
 
+def image_shard(B: int, rank: int, world: int) -> tuple[int, int]:
+    """Contiguous image range [start, end) of `rank` when B images split over `world` ranks.
+
+    Images are independent (attention never crosses images), so any split
+    needs no exchange; the first B % world ranks take one extra image."""
+    base, extra = divmod(B, world)
+    start = rank * base + min(rank, extra)
+    return start, start + base + (1 if rank < extra else 0)
+
+
 def barrier(world):
     if world > 1:
         import torch.distributed as dist
