@@ -387,7 +387,8 @@ def run_rra(args, world, rank, local):
             _build.build()
         barrier(world)
     from ragged_attention_token_gb300 import rra
-    rra.set_attend_kernel(rra.ATTEND_TCGEN05 if args.attend_kernel == "tcgen05" else rra.ATTEND_MMA_SYNC)
+    rra.set_attend_kernel({"auto": rra.ATTEND_AUTO, "tcgen05": rra.ATTEND_TCGEN05,
+                           "mma_sync": rra.ATTEND_MMA_SYNC}[args.attend_kernel])
 
     device = torch.device("cuda", local)
     torch.cuda.set_device(device)
@@ -479,7 +480,8 @@ def run_rra(args, world, rank, local):
     e2e_value = T * args.steps * world / (e2e_ms * 1e-3)
 
     # per-kernel device time (graph of back-to-back launches on cold inputs)
-    mma = args.attend_kernel == "mma_sync"
+    n_sms = torch.cuda.get_device_properties(device).multi_processor_count
+    mma = args.attend_kernel == "mma_sync" or (args.attend_kernel == "auto" and B * H < n_sms)
     kt = kernel_times(case, sets, rra, stream, packed=mma)
     if mma:   # the pipeline runs the packed path: pack with the row copy, then mma.sync attention
         kt = {"index_us": kt["pack_copy_us"], "attend_us": kt["attend_packed_us"]}
@@ -551,8 +553,10 @@ def run_sweep(args):
     from ragged_attention_token_gb300 import build as _build
     _build.build()
     from ragged_attention_token_gb300 import rra
-    rra.set_attend_kernel(rra.ATTEND_TCGEN05 if args.attend_kernel == "tcgen05" else rra.ATTEND_MMA_SYNC)
+    rra.set_attend_kernel({"auto": rra.ATTEND_AUTO, "tcgen05": rra.ATTEND_TCGEN05,
+                           "mma_sync": rra.ATTEND_MMA_SYNC}[args.attend_kernel])
     device = torch.device("cuda", 0)
+    n_sms = torch.cuda.get_device_properties(device).multi_processor_count
     stream = torch.cuda.Stream(device=device)
     peaks = measured_peaks()
     cases = [W.make_tiny()] + [W.make_serving(b) for b in W.SERVING_BATCHES] + \
@@ -561,7 +565,7 @@ def run_sweep(args):
     cases += [W.make_progressive_layer(L, masks) for L in (1, 4, 7, 10)]
     for case in cases:
         sets = InputSets(case, device, rra, case.dtype)
-        mma = args.attend_kernel == "mma_sync"
+        mma = args.attend_kernel == "mma_sync" or (args.attend_kernel == "auto" and case.B * case.H < n_sms)
         kt = kernel_times(case, sets, rra, stream, packed=True)
         if mma:   # the pipeline runs the packed path with the mma.sync attention
             kt = {"index_us": kt["pack_copy_us"], "attend_us": kt["attend_packed_us"]}
@@ -595,8 +599,8 @@ def main(argv=None):
     ap.add_argument("--clock-window", type=float, default=1.5, help="seconds of load before the timed region")
     ap.add_argument("--pruning", type=float, default=None,
                     help="pruning rate for the batched / hires workloads (their sweep values)")
-    ap.add_argument("--attend-kernel", choices=("tcgen05", "mma_sync"), default="tcgen05",
-                    help="attention kernel behind rra_attend")
+    ap.add_argument("--attend-kernel", choices=("auto", "tcgen05", "mma_sync"), default="auto",
+                    help="attention kernel behind rra_attend / rra_pipeline")
     args = ap.parse_args(argv)
     world, rank, local = dist_setup(args)
     if args.impl == "reference":

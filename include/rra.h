@@ -210,12 +210,18 @@ RRA_API rra_status rra_plan_create(const uint8_t* keep, const void* q, const voi
 RRA_API rra_status rra_plan_launch(rra_plan* plan, void* stream);
 RRA_API void rra_plan_destroy(rra_plan* plan);
 
-/* Which kernel rra_attend (and everything built on it) launches; process-
- * wide, returns the previous choice (or -1 for an unknown value).
- *   RRA_ATTEND_TCGEN05  (default) TMA tile loads + tcgen05.mma with TMEM
- *                       accumulators, persistent CTAs;
- *   RRA_ATTEND_MMA_SYNC warp-level mma.sync kernel, kept for comparison. */
-typedef enum { RRA_ATTEND_TCGEN05 = 0, RRA_ATTEND_MMA_SYNC = 1 } rra_attend_kernel;
+/* Which kernel rra_attend and rra_pipeline launch; process-wide, returns
+ * the previous choice (or -1 for an unknown value).
+ *   RRA_ATTEND_TCGEN05  TMA tile loads + tcgen05.mma with TMEM accumulators,
+ *                       persistent CTAs; rra_pipeline gathers rows from the
+ *                       padded inputs (no packed copy);
+ *   RRA_ATTEND_MMA_SYNC warp-level mma.sync kernel on packed buffers;
+ *                       rra_pipeline packs with the row copy first;
+ *   RRA_ATTEND_AUTO     (default) MMA_SYNC when B*H is below the device's SM
+ *                       count (too few (image, head) pairs to fill the GPU:
+ *                       the shorter per-CTA latency chain wins), TCGEN05
+ *                       otherwise. */
+typedef enum { RRA_ATTEND_TCGEN05 = 0, RRA_ATTEND_MMA_SYNC = 1, RRA_ATTEND_AUTO = 2 } rra_attend_kernel;
 RRA_API int rra_set_attend_kernel(int kernel);
 
 /* Reads (and with clear != 0 resets) the device-side error code of the

@@ -20,7 +20,8 @@ __global__ void null_kernel() {}
 
 thread_local char g_last_message[256] = "";
 std::atomic<uint64_t> g_launches{0};
-std::atomic<int> g_attend_kernel{RRA_ATTEND_TCGEN05};
+std::atomic<int> g_attend_kernel{RRA_ATTEND_AUTO};
+
 
 rra_status fail(rra_status s, const char* fmt, ...) {
   va_list ap;
@@ -111,6 +112,14 @@ void workspace_layout(int B, int N, int H, int d, rra_dtype in, size_t off[6], s
 
 // ---------------------------------------------------------------- enqueue
 
+// The kernel a call with B images of H heads runs under the current choice.
+bool use_tcgen05(const DeviceState& st, int B, int H) {
+  const int k = g_attend_kernel.load();
+  if (k == RRA_ATTEND_TCGEN05) return true;
+  if (k == RRA_ATTEND_MMA_SYNC) return false;
+  return static_cast<long long>(B) * H >= st.num_sms;
+}
+
 rra_status enqueue_pack(const DeviceState& st, const uint8_t* keep, int B, int N, int H, int d,
                         rra_dtype in, const void* q, const void* k, const void* v, int32_t* cu,
                         int32_t* dst, int32_t* src, void* qp, void* kp, void* vp, void* outz,
@@ -154,7 +163,7 @@ rra_status enqueue_attend(const DeviceState& st, const void* qp, const void* kp,
   a.scale_log2 = scale * 1.4426950408889634f;
   a.err = st.err;
   cudaError_t e;
-  if (g_attend_kernel.load() == RRA_ATTEND_TCGEN05) {
+  if (use_tcgen05(st, B, H)) {
     if (!attend_tc_available())
       return fail(RRA_ERR_CUDA, "attend: the driver's tensor-map encoder is unavailable");
     e = launch_attend_tc(a, in, out_dt, st.num_sms, s);
@@ -202,7 +211,7 @@ rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaSt
   int32_t* cu = reinterpret_cast<int32_t*>(ws + off[0]);
   int32_t* dst = reinterpret_cast<int32_t*>(ws + off[1]);
   int32_t* src = reinterpret_cast<int32_t*>(ws + off[2]);
-  if (g_attend_kernel.load() == RRA_ATTEND_TCGEN05) {
+  if (use_tcgen05(st, p.B, p.H)) {
     // Index pass (cu_seqlens, pack indices, zero fill of pruned output rows),
     // then attention gathering the kept rows straight from q/k/v.
     if (!attend_tc_available())
@@ -269,7 +278,7 @@ const char* rra_last_error_message(void) { return g_last_message; }
 uint64_t rra_launch_count(void) { return g_launches.load(); }
 
 int rra_set_attend_kernel(int kernel) {
-  if (kernel != RRA_ATTEND_TCGEN05 && kernel != RRA_ATTEND_MMA_SYNC) return -1;
+  if (kernel != RRA_ATTEND_TCGEN05 && kernel != RRA_ATTEND_MMA_SYNC && kernel != RRA_ATTEND_AUTO) return -1;
   return g_attend_kernel.exchange(kernel);
 }
 

@@ -48,8 +48,9 @@ namespace {
 constexpr int BM = 128;        // query rows per unit (= TMEM lanes)
 constexpr int BN = 64;         // keys per chunk
 constexpr int HD = 64;         // head dim
-constexpr int THREADS = 128;
-constexpr int BOX = 32;        // rows per TMA box
+constexpr int CONSUMERS = 128;   // warps 0-3: MMA issue (thread 0) and softmax, one query row each
+constexpr int THREADS = CONSUMERS + 32;   // warp 4: TMA producer
+constexpr int BOX = 32;        // rows per TMA box (packed inputs)
 constexpr int CTAS_PER_SM = 4;
 constexpr int STAGES = 2;      // K/V chunk ring
 
@@ -58,8 +59,11 @@ constexpr uint32_t KV_BYTES = BN * 128;                //  64 rows x 128 B
 constexpr uint32_t OFF_Q = 0;                          // one Q tile
 constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;            // K[STAGES]
 constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;  // V[STAGES]
-constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;  // load[STAGES], q, mma, TMEM slot
-constexpr uint32_t SMEM_USED = OFF_BAR + 64;
+constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
+// mbarriers: full[2] +0/+8, empty[2] +16/+24, qempty +32, mma +40; TMEM slot +48;
+// abort flag +52; redo flags +56/+60; item descriptors (2 x 32 B) +64.
+constexpr uint32_t OFF_DESC = OFF_BAR + 64;
+constexpr uint32_t SMEM_USED = OFF_DESC + STAGES * 32;
 constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;      // slack to align the base to 1024 B
 constexpr uint32_t TMEM_COLS = 128;                    // S/P: cols [0,64), O: cols [64,128)
 constexpr uint32_t WAIT_SUSPEND_NS = 20000;            // try_wait suspend hint
@@ -285,7 +289,7 @@ struct Unit {
 
 // First unit at index >= u (stride `step`) whose query tile holds rows; a
 // unit with an inconsistent length records an error and is skipped.
-__device__ __forceinline__ Unit next_unit(int u, int step, int units, int BH, const AttendArgs& a, int tid) {
+__device__ __forceinline__ Unit next_unit(int u, int step, int units, int BH, const AttendArgs& a, bool record) {
   Unit x;
   for (; u < units; u += step) {
     const int qt = u / BH;
@@ -295,7 +299,7 @@ __device__ __forceinline__ Unit next_unit(int u, int step, int units, int BH, co
     const int s0 = __ldg(a.cu_seqlens + b);
     const int n = __ldg(a.cu_seqlens + b + 1) - s0;
     if (n < 0 || n > a.max_seqlen) {
-      if (qt == 0 && h == 0 && tid == 0)
+      if (qt == 0 && h == 0 && record)
         record_error(a.err, n < 0 ? RRA_DEVERR_SEQ_NEGATIVE : RRA_DEVERR_SEQ_TOO_LONG);
       continue;
     }
@@ -398,6 +402,35 @@ __device__ __forceinline__ void rescale_o(uint32_t tO_row, float alpha) {
   }
 }
 
+// Consumer-only barrier (named barrier 1, the 128 consumer threads) that
+// also ORs a predicate across them.
+__device__ __forceinline__ bool consumer_sync_or(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.or.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
+      : "=r"(r)
+      : "r"(pred ? 1u : 0u)
+      : "memory");
+  return r != 0;
+}
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ uint32_t ld_shared_volatile_u32(uint32_t addr) {
+  uint32_t v;
+  asm volatile("ld.volatile.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr) : "memory");
+  return v;
+}
+// Bounded wait that also gives up as soon as the CTA's abort flag is set.
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, uint32_t abort_flag) {
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (ld_shared_volatile_u32(abort_flag) != 0u) return false;
+    if (clock64() - t0 > WAIT_LIMIT_CYCLES) return false;
+  }
+  return true;
+}
+
 template <typename Tin, typename Tout, bool SCATTER, bool GATHER>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -410,303 +443,322 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   const uint32_t sQ = base + OFF_Q;
   auto sK = [&](int i) { return base + OFF_K + i * KV_BYTES; };
   auto sV = [&](int i) { return base + OFF_V + i * KV_BYTES; };
-  auto bar_load = [&](int i) { return base + OFF_BAR + i * 8; };
-  const uint32_t bar_q = base + OFF_BAR + 16, bar_mma = base + OFF_BAR + 24, slot = base + OFF_BAR + 32;
-  const volatile uint32_t* slot_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + 32);
+  auto bar_full = [&](int i) { return base + OFF_BAR + i * 8; };
+  auto bar_empty = [&](int i) { return base + OFF_BAR + 16 + i * 8; };
+  const uint32_t bar_qempty = base + OFF_BAR + 32, bar_mma = base + OFF_BAR + 40;
+  const uint32_t slot = base + OFF_BAR + 48, abort_flag = base + OFF_BAR + 52;
+  auto desc_addr = [&](int i) { return base + OFF_DESC + i * 32; };
+  const volatile uint32_t* slot_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + 48);
 
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp == 0) {
     tmem_alloc(slot, TMEM_COLS);
     tmem_relinquish();
   }
   if (tid == 32) {
-    mbar_init(bar_load(0), 1);
-    mbar_init(bar_load(1), 1);
-    mbar_init(bar_q, 1);
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(bar_full(i), 1);
+      mbar_init(bar_empty(i), 1);
+    }
+    mbar_init(bar_qempty, 1);
     mbar_init(bar_mma, 1);
+    st_shared_u32(abort_flag, 0u);
+    st_shared_u32(base + OFF_BAR + 56, 0u);
+    st_shared_u32(base + OFF_BAR + 60, 0u);
     fence_barrier_init();
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *slot_ptr;
-  const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-  const uint32_t tS = tmem, tO = tmem + 64;
-  const uint32_t idesc_pv = idesc_f16(BF ? 1u : 0u, 1, BM, HD);
   const int BH = a.B * a.H;
   const int step = gridDim.x;
-  const float c2 = a.scale_log2;
   (void)qtiles;
+  bool bad = false;
 
-  // TMA issue, called by all 32 lanes of warp 0: K/V rows of (unit x, chunk
-  // c) into stage st; the unit's Q tile into the single Q buffer.  Packed
-  // inputs: 32-row boxes of the [T, H, 64] map (lane 0).  Gathered inputs:
-  // rows src_idx[t] * H + h of the padded [B*N*H, 64] map, 4 per gather4
-  // (one lane per group); the last group repeats the chunk's last row so
-  // every row the MMA reads is a finite input row.
-  const int lane = tid & 31;
-  auto issue_kv = [&](const Unit& x, int c, int st) {
-    const int k0 = c * BN;
-    const int n_c = min(BN, x.n - k0);
-    if constexpr (GATHER) {
-      const int groups = ((n_c + 15) & ~15) / 4;
-      if (lane == 0) mbar_expect_tx(bar_load(st), static_cast<uint32_t>(2 * groups * 4 * 128));
-      __syncwarp();
-      const int g = lane & 15;
-      if (g < groups) {
-        int rows[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          rows[i] = __ldg(a.src_idx + x.s0 + min(k0 + 4 * g + i, k0 + n_c - 1)) * a.H + x.h;
-        if (lane < 16) tma_gather4(sK(st) + g * 512, &tmap_k, rows, bar_load(st));
-        else tma_gather4(sV(st) + g * 512, &tmap_v, rows, bar_load(st));
-      }
-    } else if (lane == 0) {
-      const int kboxes = (n_c + BOX - 1) / BOX;
-      mbar_expect_tx(bar_load(st), static_cast<uint32_t>(2 * kboxes * BOX * 128));
-      for (int j = 0; j < kboxes; ++j) {
-        tma_load_3d(sK(st) + j * BOX * 128, &tmap_k, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
-        tma_load_3d(sV(st) + j * BOX * 128, &tmap_v, 0, x.h, x.s0 + k0 + j * BOX, bar_load(st));
-      }
-    }
-  };
-  auto issue_q = [&](const Unit& x) {
-    if constexpr (GATHER) {
-      const int groups = (x.rows_q + 3) / 4;
-      if (lane == 0) mbar_expect_tx(bar_q, static_cast<uint32_t>(groups * 4 * 128));
-      __syncwarp();
-      if (lane < groups) {
-        int rows[4];
-#pragma unroll
-        for (int i = 0; i < 4; ++i)
-          rows[i] = __ldg(a.src_idx + x.s0 + min(x.q0 + 4 * lane + i, x.q0 + x.rows_q - 1)) * a.H + x.h;
-        tma_gather4(sQ + lane * 512, &tmap_q, rows, bar_q);
-      }
-    } else if (lane == 0) {
-      const int qboxes = (x.rows_q + BOX - 1) / BOX;
-      mbar_expect_tx(bar_q, static_cast<uint32_t>(qboxes * BOX * 128));
-      for (int j = 0; j < qboxes; ++j)
-        tma_load_3d(sQ + j * BOX * 128, &tmap_q, 0, x.h, x.s0 + x.q0 + j * BOX, bar_q);
-    }
-  };
-
-  uint32_t ph_load[STAGES] = {0u, 0u};
-  uint32_t ph_q = 0, ph_mma = 0;
-  bool load_pending[STAGES] = {false, false};
-  bool q_pending = false, mma_pending = false;
-  bool bad = false;      // this thread saw a wait time out
-  bool abort = false;    // some thread did: the whole CTA stops
-
-  Unit cur = next_unit(blockIdx.x, step, units, BH, a, tid);
-  int c = 0, stage = 0;
-  if (cur.u < units) {
-    if (warp == 0) {
-      issue_q(cur);
-      issue_kv(cur, 0, 0);
-    }
-    q_pending = true;
-    load_pending[0] = true;
-  }
-  float m_run = 0.f, l_run = 0.f;   // this row's reference max (log2 units) and sum
-  uint32_t iter = 0;                // chunk iterations done (selects the redo flag word)
-  if (tid == 0) {
-    st_shared_u32(base + OFF_BAR + 40, 0u);
-    st_shared_u32(base + OFF_BAR + 44, 0u);
-  }
-  __syncthreads();
-
-  while (cur.u < units) {
-    // Prefetch the next item's K/V into the other stage while this one computes.
-    Unit nxt = cur;
-    int nc = c + 1;
-    if (nc >= cur.nchunks) {
-      nxt = next_unit(cur.u + step, step, units, BH, a, tid);
-      nc = 0;
-    }
-    const bool have_next = nxt.u < units;
-
-    const int k0 = c * BN;
-    const int n_c = min(BN, cur.n - k0);
-    const int nk16 = (n_c + 15) & ~15;
-    const bool full = (n_c == BN);
-    const bool rows_here = warp * 32 < cur.rows_q;   // warp-uniform
-
-    // Warp 0 alone waits for the loads, zeroes the V rows [n_c, nk16) that
-    // enter the MMA with p = 0, and thread 0 issues S = Q K^T -> TMEM
-    // columns [0, nk16).  The other warps go straight to the MMA barrier.
-    if (warp == 0) {
-      if (c == 0) {
-        bad |= !mbar_wait(bar_q, ph_q, WAIT_LIMIT_CYCLES);
-        if (!bad) { ph_q ^= 1; q_pending = false; }
-      }
-      bad |= !mbar_wait(bar_load(stage), ph_load[stage], WAIT_LIMIT_CYCLES);
-      if (!bad) { ph_load[stage] ^= 1; load_pending[stage] = false; }
-      if constexpr (!GATHER) {
-        const int zvec = (nk16 - n_c) * 8;
-        for (int zi = tid; zi < zvec; zi += 32)
-          st_shared_v4(sV(stage) + (n_c + (zi >> 3)) * 128 + (zi & 7) * 16, 0u, 0u, 0u, 0u);
-        fence_proxy_async();
-      }
-      __syncwarp();
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(stage) + kk * 32, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-        umma_commit(bar_mma);
-      }
-      __syncwarp();
-      // Prefetch the next item's K/V into the other stage (its last reader,
-      // the P.V product two items back, has completed) while S computes.
-      if (have_next) issue_kv(nxt, nc, stage ^ 1);
-    }
-    if (have_next) load_pending[stage ^ 1] = true;
-    mma_pending = true;
-    bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
-    if (!bad) { ph_mma ^= 1; mma_pending = false; }
-    tc_fence_after();
-    // Softmax on this thread's row (TMEM lane).  Exponentials are taken
-    // against a per-row reference m_run (log2 units) and O accumulates in
-    // TMEM across chunks.  bf16: one pass, the reference being the row's first
-    // score on the first chunk and the running reference after, P written
-    // over S at once; a row whose chunk sum exceeds 2^32 flags a redo, and
-    // then the whole CTA recomputes S and this chunk (exact max and O rescale
-    // for the flagged rows).  fp16 (narrower range for P): max pass first,
-    // rescale when the max grows by > 8.
-    const uint32_t tS_row = tS + lane_off, tO_row = tO + lane_off;
-    const float l_before = l_run, m_before = m_run;
-    // Redo flag of this chunk: two words used alternately, set to iter + 1,
-    // so a stale value from two chunks back never reads as set (no reset).
-    const uint32_t flag = base + OFF_BAR + 40 + (iter & 1) * 4;
-    bool redo_row = false;
-    if (rows_here) {
-      if constexpr (BF) {
-        l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0);
-        redo_row = (tid < cur.rows_q) && !(l_run - l_before <= 0x1p32f);
-        if (__any_sync(0xffffffffu, redo_row) && (tid & 31) == 0) st_shared_u32(flag, iter + 1u);
-      } else {
-        const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
-        if (c == 0) {
-          m_run = mx;
-        } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
-          const float m_new = fmaxf(m_run, mx);
-          const float alpha = fast_exp2(m_run - m_new);
-          l_run *= alpha;
-          rescale_o(tO_row, alpha);
-          m_run = m_new;
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    // Walks this CTA's items (unit, key chunk) in order.  For each: waits
+    // until its stage (and, on a unit's first chunk, the Q buffer) is free,
+    // publishes the item's descriptor, and issues the TMA loads that
+    // complete the stage's full barrier.  Ends with a sentinel descriptor.
+    uint32_t j = 0, uidx = 0;
+    Unit U = next_unit(blockIdx.x, step, units, BH, a, lane == 0);
+    bool done = false;
+    while (!done && !bad) {
+      const int nch = (U.u < units) ? U.nchunks : 1;
+      for (int c = 0; c < nch && !bad; ++c) {
+        const int st = j & 1;
+        if (j >= STAGES) bad |= !mbar_wait_or_abort(bar_empty(st), ((j >> 1) - 1) & 1, abort_flag);
+        if (U.u < units && c == 0 && uidx >= 1)
+          bad |= !mbar_wait_or_abort(bar_qempty, (uidx - 1) & 1, abort_flag);
+        bad = __any_sync(0xffffffffu, bad);
+        if (bad) break;
+        if (U.u >= units) {
+          // Sentinel: no more items.
+          if (lane == 0) {
+            st_shared_u32(desc_addr(st), static_cast<uint32_t>(units));
+            mbar_arrive(bar_full(st));
+          }
+          done = true;
+          break;
         }
-        l_run += chunk_weights<false>(tS_row, nk16, n_c, full, c2, m_run, false);
-      }
-      tmem_st_wait();
-    }
-    tc_fence_before();
-    if (__syncthreads_or(bad)) { abort = true; break; }
-    if (BF && ld_shared_u32(flag) == iter + 1u) {
-      // Rare: recompute S, then every warp rewrites its P; flagged warps
-      // switch to the exact max (rescaling O for later chunks).
-      if (tid == 0) {
-        tc_fence_after();
-        const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
+        const int k0 = c * BN;
+        const int n_c = min(BN, U.n - k0);
+        if (lane == 0) {
+          const uint32_t d = desc_addr(st);
+          st_shared_u32(d + 0, static_cast<uint32_t>(U.u));
+          st_shared_u32(d + 4, static_cast<uint32_t>(U.h));
+          st_shared_u32(d + 8, static_cast<uint32_t>(U.s0));
+          st_shared_u32(d + 12, static_cast<uint32_t>(U.n));
+          st_shared_u32(d + 16, static_cast<uint32_t>(U.q0));
+          st_shared_u32(d + 20, static_cast<uint32_t>(U.rows_q));
+          st_shared_u32(d + 24, static_cast<uint32_t>(U.nchunks));
+          st_shared_u32(d + 28, static_cast<uint32_t>(c));
+        }
+        if constexpr (GATHER) {
+          const int kgroups = ((n_c + 15) & ~15) / 4;
+          const int qgroups = (c == 0) ? (U.rows_q + 3) / 4 : 0;
+          if (lane == 0) mbar_expect_tx(bar_full(st), static_cast<uint32_t>((2 * kgroups + qgroups) * 512));
+          __syncwarp();
+          if (lane < qgroups) {
+            int rows[4];
 #pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk)
-          umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(stage) + kk * 32, 16, 1024), idesc_s,
-                   kk > 0 ? 1u : 0u);
-        umma_commit(bar_mma);
+            for (int i = 0; i < 4; ++i)
+              rows[i] = __ldg(a.src_idx + U.s0 + min(U.q0 + 4 * lane + i, U.q0 + U.rows_q - 1)) * a.H + U.h;
+            tma_gather4(sQ + lane * 512, &tmap_q, rows, bar_full(st));
+          }
+          const int g = lane & 15;
+          if (g < kgroups) {
+            int rows[4];
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+              rows[i] = __ldg(a.src_idx + U.s0 + min(k0 + 4 * g + i, k0 + n_c - 1)) * a.H + U.h;
+            if (lane < 16) tma_gather4(sK(st) + g * 512, &tmap_k, rows, bar_full(st));
+            else tma_gather4(sV(st) + g * 512, &tmap_v, rows, bar_full(st));
+          }
+        } else if (lane == 0) {
+          const int kboxes = (n_c + BOX - 1) / BOX;
+          const int qboxes = (c == 0) ? (U.rows_q + BOX - 1) / BOX : 0;
+          mbar_expect_tx(bar_full(st), static_cast<uint32_t>((2 * kboxes + qboxes) * BOX * 128));
+          for (int jj = 0; jj < qboxes; ++jj)
+            tma_load_3d(sQ + jj * BOX * 128, &tmap_q, 0, U.h, U.s0 + U.q0 + jj * BOX, bar_full(st));
+          for (int jj = 0; jj < kboxes; ++jj) {
+            tma_load_3d(sK(st) + jj * BOX * 128, &tmap_k, 0, U.h, U.s0 + k0 + jj * BOX, bar_full(st));
+            tma_load_3d(sV(st) + jj * BOX * 128, &tmap_v, 0, U.h, U.s0 + k0 + jj * BOX, bar_full(st));
+          }
+        }
+        __syncwarp();
+        ++j;
       }
-      mma_pending = true;
-      bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
-      if (!bad) { ph_mma ^= 1; mma_pending = false; }
+      if (done || bad) break;
+      ++uidx;
+      U = next_unit(U.u + step, step, units, BH, a, lane == 0);
+    }
+    if (!bad) {
+      // Tail: wait for the consumers' last stage and Q releases, so that no
+      // asynchronous arrive lands after the CTA has gone.
+      if (j >= 1) bad |= !mbar_wait_or_abort(bar_empty((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag);
+      if (uidx >= 1) bad |= !mbar_wait_or_abort(bar_qempty, (uidx - 1) & 1, abort_flag);
+      bad = __any_sync(0xffffffffu, bad);
+    }
+    if (bad) {
+      if (lane == 0) {
+        st_shared_u32(abort_flag, 1u);
+        record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
+      }
+    }
+  } else {
+    // ------------------------------------------------------------ consumers
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t tS = tmem, tO = tmem + 64;
+    const uint32_t tS_row = tS + lane_off, tO_row = tO + lane_off;
+    const uint32_t idesc_pv = idesc_f16(BF ? 1u : 0u, 1, BM, HD);
+    const float c2 = a.scale_log2;
+    uint32_t ph_mma = 0;
+    float m_run = 0.f, l_run = 0.f;   // this row's reference max (log2 units) and sum
+    for (uint32_t j = 0;; ++j) {
+      const int st = j & 1;
+      bad |= !mbar_wait_or_abort(bar_full(st), (j >> 1) & 1, abort_flag);
+      if (consumer_sync_or(bad)) { bad = true; break; }
+      const uint32_t d = desc_addr(st);
+      const int u = static_cast<int>(ld_shared_u32(d + 0));
+      if (u >= units) break;   // sentinel
+      const int h = static_cast<int>(ld_shared_u32(d + 4));
+      const int s0 = static_cast<int>(ld_shared_u32(d + 8));
+      const int n = static_cast<int>(ld_shared_u32(d + 12));
+      const int q0 = static_cast<int>(ld_shared_u32(d + 16));
+      const int rows_q = static_cast<int>(ld_shared_u32(d + 20));
+      const int nchunks = static_cast<int>(ld_shared_u32(d + 24));
+      const int c = static_cast<int>(ld_shared_u32(d + 28));
+      const int k0 = c * BN;
+      const int n_c = min(BN, n - k0);
+      const int nk16 = (n_c + 15) & ~15;
+      const bool full = (n_c == BN);
+      const bool rows_here = warp * 32 < rows_q;   // warp-uniform
+      const bool last = (c == nchunks - 1);
+
+      // S = Q K^T -> TMEM columns [0, nk16).  Packed inputs: warp 0 first
+      // zeroes the V rows [n_c, nk16) that enter the MMA with p = 0 (the
+      // gathered path repeats a finite row there instead).
+      if (warp == 0) {
+        if constexpr (!GATHER) {
+          const int zvec = (nk16 - n_c) * 8;
+          for (int zi = lane; zi < zvec; zi += 32)
+            st_shared_v4(sV(st) + (n_c + (zi >> 3)) * 128 + (zi & 7) * 16, 0u, 0u, 0u, 0u);
+          fence_proxy_async();
+          __syncwarp();
+        }
+        if (tid == 0) {
+          tc_fence_after();
+          const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
+#pragma unroll
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(st) + kk * 32, 16, 1024), idesc_s,
+                     kk > 0 ? 1u : 0u);
+          umma_commit(bar_mma);
+        }
+      }
+      bad |= !mbar_wait_or_abort(bar_mma, ph_mma, abort_flag);
+      if (!bad) ph_mma ^= 1;
+      bad = __any_sync(0xffffffffu, bad);   // warp-uniform before warp-collective TMEM access
       tc_fence_after();
-      if (rows_here) {
-        l_run = l_before;
-        m_run = m_before;
-        if (__any_sync(0xffffffffu, redo_row)) {
+
+      // Softmax on this thread's row (TMEM lane).  Exponentials are taken
+      // against a per-row reference m_run (log2 units) and O accumulates in
+      // TMEM across chunks.  bf16: one pass, the reference being the row's
+      // first score on the first chunk and the running reference after, P
+      // written over S at once; a row whose chunk sum exceeds 2^32 flags a
+      // redo, and then the consumers recompute S and this chunk (exact max
+      // and O rescale for the flagged rows).  fp16 (narrower range for P):
+      // max pass first, rescale when the max grows by > 8.
+      const float l_before = l_run, m_before = m_run;
+      // Redo flag of this item: two words used alternately, set to j + 1,
+      // so a stale value from two items back never reads as set.
+      const uint32_t flag = base + OFF_BAR + 56 + (j & 1) * 4;
+      bool redo_row = false;
+      if (rows_here && !bad) {
+        if constexpr (BF) {
+          l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0);
+          redo_row = (tid < rows_q) && !(l_run - l_before <= 0x1p32f);
+          if (__any_sync(0xffffffffu, redo_row) && lane == 0) st_shared_u32(flag, j + 1u);
+        } else {
           const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
-          const float m_new = (c == 0) ? mx : fmaxf(m_before, mx);
-          if (c > 0) {
-            const float alpha = fast_exp2(m_before - m_new);
+          if (c == 0) {
+            m_run = mx;
+          } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
+            const float m_new = fmaxf(m_run, mx);
+            const float alpha = fast_exp2(m_run - m_new);
             l_run *= alpha;
             rescale_o(tO_row, alpha);
+            m_run = m_new;
           }
-          m_run = m_new;
-          l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, false);
-        } else {
-          l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0);
+          l_run += chunk_weights<false>(tS_row, nk16, n_c, full, c2, m_run, false);
         }
         tmem_st_wait();
       }
       tc_fence_before();
-      if (__syncthreads_or(bad)) { abort = true; break; }
-    }
-    // The unit's last S product is final: its Q buffer can take the next unit's tile.
-    if (nc == 0 && have_next) {
-      if (warp == 0) issue_q(nxt);
-      q_pending = true;
-    }
-
-    // O += P_hi V + P_lo V in TMEM columns [64, 128) (fresh on a unit's first chunk)
-    if (tid == 0) {
-      tc_fence_after();
-      const int ksteps = nk16 / 16;
-      for (int kk = 0; kk < ksteps; ++kk)
-        umma_f16_tmem_a(tO, tS + kk * 16, sdesc(sV(stage) + kk * 2048, KV_BYTES, 1024), idesc_pv,
-                        (kk > 0 || c > 0) ? 1u : 0u);
-      for (int kk = 0; kk < ksteps; ++kk)
-        umma_f16_tmem_a(tO, tS + kk * 16 + 8, sdesc(sV(stage) + kk * 2048, KV_BYTES, 1024), idesc_pv, 1u);
-      umma_commit(bar_mma);
-    }
-    mma_pending = true;
-    bad |= !mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES);
-    if (!bad) { ph_mma ^= 1; mma_pending = false; }
-    tc_fence_after();
-
-    if (c == cur.nchunks - 1 && rows_here) {
-      // Epilogue: this thread's row, normalised, to the packed or padded output.
-      float o_acc[HD];
+      if (consumer_sync_or(bad)) { bad = true; break; }
+      if (BF && ld_shared_u32(flag) == j + 1u) {
+        // Rare: recompute S, then every warp rewrites its P; flagged warps
+        // switch to the exact max (rescaling O for later chunks).
+        if (tid == 0) {
+          tc_fence_after();
+          const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
 #pragma unroll
-      for (int g = 0; g < HD / 16; ++g) tmem_ld16(tO + lane_off + g * 16, o_acc + g * 16);
-      const int i = cur.q0 + tid;
-      if (i < cur.n) {
-        long long dst_row = static_cast<long long>(cur.s0) + i;
-        bool ok = true;
-        if constexpr (SCATTER) {
-          dst_row = __ldg(a.src_idx + dst_row);
-          if (dst_row < 0 || dst_row >= static_cast<long long>(a.B) * a.N) {
-            record_error(a.err, RRA_DEVERR_INDEX_RANGE);
-            ok = false;
+          for (int kk = 0; kk < HD / 16; ++kk)
+            umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(st) + kk * 32, 16, 1024), idesc_s,
+                     kk > 0 ? 1u : 0u);
+          umma_commit(bar_mma);
+        }
+        bad |= !mbar_wait_or_abort(bar_mma, ph_mma, abort_flag);
+        if (!bad) ph_mma ^= 1;
+        bad = __any_sync(0xffffffffu, bad);
+        tc_fence_after();
+        if (rows_here && !bad) {
+          l_run = l_before;
+          m_run = m_before;
+          if (__any_sync(0xffffffffu, redo_row)) {
+            const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
+            const float m_new = (c == 0) ? mx : fmaxf(m_before, mx);
+            if (c > 0) {
+              const float alpha = fast_exp2(m_before - m_new);
+              l_run *= alpha;
+              rescale_o(tO_row, alpha);
+            }
+            m_run = m_new;
+            l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, false);
+          } else {
+            l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0);
+          }
+          tmem_st_wait();
+        }
+        tc_fence_before();
+        if (consumer_sync_or(bad)) { bad = true; break; }
+      }
+
+      // O += P_hi V + P_lo V in TMEM columns [64, 128) (fresh on a unit's
+      // first chunk).  Its completion frees this K/V stage for the producer
+      // and, on the unit's last chunk, the Q buffer.
+      if (tid == 0) {
+        tc_fence_after();
+        const int ksteps = nk16 / 16;
+        for (int kk = 0; kk < ksteps; ++kk)
+          umma_f16_tmem_a(tO, tS + kk * 16, sdesc(sV(st) + kk * 2048, KV_BYTES, 1024), idesc_pv,
+                          (kk > 0 || c > 0) ? 1u : 0u);
+        for (int kk = 0; kk < ksteps; ++kk)
+          umma_f16_tmem_a(tO, tS + kk * 16 + 8, sdesc(sV(st) + kk * 2048, KV_BYTES, 1024), idesc_pv, 1u);
+        umma_commit(bar_empty(st));
+        if (last) umma_commit(bar_qempty);
+        umma_commit(bar_mma);
+      }
+      bad |= !mbar_wait_or_abort(bar_mma, ph_mma, abort_flag);
+      if (!bad) ph_mma ^= 1;
+      bad = __any_sync(0xffffffffu, bad);
+      tc_fence_after();
+
+      if (last && rows_here && !bad) {
+        // Epilogue: this thread's row, normalised, to the packed or padded output.
+        float o_acc[HD];
+#pragma unroll
+        for (int g = 0; g < HD / 16; ++g) tmem_ld16(tO_row + g * 16, o_acc + g * 16);
+        const int i = q0 + tid;
+        if (i < n) {
+          long long dst_row = static_cast<long long>(s0) + i;
+          bool ok = true;
+          if constexpr (SCATTER) {
+            dst_row = __ldg(a.src_idx + dst_row);
+            if (dst_row < 0 || dst_row >= static_cast<long long>(a.B) * a.N) {
+              record_error(a.err, RRA_DEVERR_INDEX_RANGE);
+              ok = false;
+            }
+          }
+          if (ok) {
+            Tout* out = static_cast<Tout*>(a.o) + (static_cast<size_t>(dst_row) * a.H + h) * HD;
+            store_row<Tout>(out, o_acc, 1.f / l_run);
           }
         }
-        if (ok) {
-          Tout* out = static_cast<Tout*>(a.o) + (static_cast<size_t>(dst_row) * a.H + cur.h) * HD;
-          store_row<Tout>(out, o_acc, 1.f / l_run);
-        }
       }
+      if (last) {
+        m_run = 0.f;
+        l_run = 0.f;
+      }
+      // No barrier here: the next S product overwrites S/P only after thread
+      // 0 has seen this P.V product complete, and the next unit's first P.V
+      // (which overwrites O) waits behind the next P-ready barrier.
     }
-    if (c == cur.nchunks - 1) {
-      m_run = 0.f;
-      l_run = 0.f;
+    if (bad && tid == 0) {
+      st_shared_u32(abort_flag, 1u);
+      record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
     }
-    // No barrier here: the next S product overwrites S/P only after thread 0
-    // has seen this P.V product complete, and the next unit's first P.V
-    // (which overwrites O) waits behind the next P-ready barrier.
-
-    cur = nxt;
-    c = nc;
-    stage ^= 1;
-    ++iter;
   }
 
-  if (abort) {
-    if (tid == 0) record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
-    // Give our own copies and MMAs in flight a bounded chance to land.
-    if (warp == 0) {
-      for (int st = 0; st < STAGES; ++st)
-        if (load_pending[st]) mbar_wait(bar_load(st), ph_load[st], WAIT_LIMIT_CYCLES / 8);
-      if (q_pending) mbar_wait(bar_q, ph_q, WAIT_LIMIT_CYCLES / 8);
+  // Teardown.  After an abort, copies or MMAs still in flight get a bounded
+  // grace period (~1 ms) to land before the TMEM is released and the CTA exits.
+  if (ld_shared_volatile_u32(abort_flag) != 0u && tid == 0) {
+    const long long t0 = clock64();
+    while (clock64() - t0 < 2000000LL) {
     }
-    if (mma_pending) mbar_wait(bar_mma, ph_mma, WAIT_LIMIT_CYCLES / 8);
   }
   tc_fence_before();
   __syncthreads();

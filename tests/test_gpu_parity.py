@@ -41,6 +41,7 @@ CASES = (
 
 
 KERNELS = [("tcgen05", rra.ATTEND_TCGEN05), ("mma_sync", rra.ATTEND_MMA_SYNC)]
+DEFAULT_KERNEL = rra.ATTEND_AUTO
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -49,7 +50,7 @@ def _lib():
     rra.lib()
     rra.get_device_error(clear=True)
     yield
-    rra.set_attend_kernel(rra.ATTEND_TCGEN05)
+    rra.set_attend_kernel(DEFAULT_KERNEL)
 
 
 @pytest.fixture(params=KERNELS, ids=[k[0] for k in KERNELS])
@@ -297,6 +298,22 @@ def test_launch_count_counts_kernels():
 
 def test_attend_kernel_selector():
     prev = rra.set_attend_kernel(rra.ATTEND_MMA_SYNC)
-    assert rra.set_attend_kernel(prev) == rra.ATTEND_MMA_SYNC
+    assert prev == DEFAULT_KERNEL
+    assert rra.set_attend_kernel(rra.ATTEND_AUTO) == rra.ATTEND_MMA_SYNC
     with pytest.raises(ValueError):
         rra.set_attend_kernel(7)
+    rra.set_attend_kernel(prev)
+
+
+@pytest.mark.parametrize("make", [lambda: W.make_serving(4), lambda: W.make_batched(0.8)], ids=["small", "large"])
+def test_auto_kernel_matches_explicit(make):
+    """The automatic choice gives the explicit kernel's output bit for bit."""
+    case = make()
+    small = case.B * case.H < torch.cuda.get_device_properties(0).multi_processor_count
+    outs = {}
+    for k in (rra.ATTEND_AUTO, rra.ATTEND_MMA_SYNC if small else rra.ATTEND_TCGEN05):
+        prev = rra.set_attend_kernel(k)
+        outs[k] = run_pipeline(case)["out"]
+        rra.set_attend_kernel(prev)
+    a, b = outs.values()
+    assert np.array_equal(bits(a), bits(b))
