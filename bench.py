@@ -204,42 +204,43 @@ def graph_time_per_launch(fn_list, stream, reps=5):
 
 
 def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
-    """Per-launch device µs of the pipeline's two kernels on cold inputs.
+    """Per-launch device µs on cold inputs (graphs of back-to-back launches).
 
-    index: rra_pack without the row copy (indices + zero fill of pruned rows);
-    attend: rra_attend_gather (rows gathered from the padded q/k/v).
-    With packed=True also the packed path: rra_pack with the row copy and
-    rra_attend on the packed buffers."""
+    fused_us: rra_pipeline with the tcgen05 kernel -- ONE launch (mask scan,
+    gather, attention, every output row written).  With packed=True also the
+    two-launch packed path: pack_copy_us (rra_pack with the row copy and zero
+    fill) and attend_packed_us (rra_attend on the packed buffers with the
+    mma.sync kernel), plus attend_packed_tc_us (the same with tcgen05)."""
     B, N, H, d = case.B, case.N, case.H, case.d
     R = sets.R
     n_launch = n_launch or max(R, 64)
     views = [rra.workspace_views(s[5], B, N, H, d, case.dtype) for s in sets.sets]
 
-    def index_fn(i):
+    def fused_fn(i):
         keep, q, k, v, out, ws = sets.sets[i % R]
-        cu, dst, src, qp, kp, vp = views[i % R]
-        return lambda: rra.pack(keep, q, k, v, cu, dst, src, out_zero_fill=out, stream=stream)
+        return lambda: rra.pipeline(keep, q, k, v, out, ws, scale=SCALE, stream=stream)
 
-    def gather_fn(i):
-        keep, q, k, v, out, ws = sets.sets[i % R]
-        cu, dst, src, qp, kp, vp = views[i % R]
-        return lambda: rra.attend_gather(q, k, v, cu, src, out, scale=SCALE, stream=stream)
+    prev = rra.set_attend_kernel(rra.ATTEND_TCGEN05)
+    try:
+        res = {"fused_us": graph_time_per_launch([fused_fn(i) for i in range(n_launch)], stream)}
+        if packed:
+            def pack_fn(i):
+                keep, q, k, v, out, ws = sets.sets[i % R]
+                cu, dst, src, qp, kp, vp = views[i % R]
+                return lambda: rra.pack(keep, q, k, v, cu, dst, src, qp, kp, vp, out, stream=stream)
 
-    res = {"index_us": graph_time_per_launch([index_fn(i) for i in range(n_launch)], stream),
-           "attend_us": graph_time_per_launch([gather_fn(i) for i in range(n_launch)], stream)}
-    if packed:
-        def pack_fn(i):
-            keep, q, k, v, out, ws = sets.sets[i % R]
-            cu, dst, src, qp, kp, vp = views[i % R]
-            return lambda: rra.pack(keep, q, k, v, cu, dst, src, qp, kp, vp, out, stream=stream)
+            def attend_fn(i):
+                keep, q, k, v, out, ws = sets.sets[i % R]
+                cu, dst, src, qp, kp, vp = views[i % R]
+                return lambda: rra.attend(qp, kp, vp, cu, B, N, out, scale=SCALE, src_idx=src, N=N,
+                                          stream=stream)
 
-        def attend_fn(i):
-            keep, q, k, v, out, ws = sets.sets[i % R]
-            cu, dst, src, qp, kp, vp = views[i % R]
-            return lambda: rra.attend(qp, kp, vp, cu, B, N, out, scale=SCALE, src_idx=src, N=N, stream=stream)
-
-        res["pack_copy_us"] = graph_time_per_launch([pack_fn(i) for i in range(n_launch)], stream)
-        res["attend_packed_us"] = graph_time_per_launch([attend_fn(i) for i in range(n_launch)], stream)
+            res["pack_copy_us"] = graph_time_per_launch([pack_fn(i) for i in range(n_launch)], stream)
+            res["attend_packed_tc_us"] = graph_time_per_launch([attend_fn(i) for i in range(n_launch)], stream)
+            rra.set_attend_kernel(rra.ATTEND_MMA_SYNC)
+            res["attend_packed_us"] = graph_time_per_launch([attend_fn(i) for i in range(n_launch)], stream)
+    finally:
+        rra.set_attend_kernel(prev)
     return res
 
 
@@ -400,7 +401,6 @@ def run_rra(args, world, rank, local):
     T = case.kept_tokens
     sets = InputSets(case, device, rra, case.dtype)
     plans = [rra.Plan(*s, scale=SCALE) for s in sets.sets]
-    launches_per_step = 2
 
     # The timed steps replay CUDA graphs that each hold R consecutive steps
     # (one per rotating input set): the host dispatches once per R steps.
@@ -410,6 +410,7 @@ def run_rra(args, world, rank, local):
     n_cap0 = rra.launch_count()
     g_full = capture([step_fn(s) for s in sets.sets], stream)
     per_full = (rra.launch_count() - n_cap0) // 2            # eager pass + capture each count once
+    launches_per_step = per_full // sets.R
     g_rem, per_rem = None, 0
     if rem:
         n_cap0 = rra.launch_count()
@@ -481,19 +482,22 @@ def run_rra(args, world, rank, local):
 
     # per-kernel device time (graph of back-to-back launches on cold inputs)
     n_sms = torch.cuda.get_device_properties(device).multi_processor_count
-    mma = args.attend_kernel == "mma_sync" or (args.attend_kernel == "auto" and B * H < n_sms)
-    kt = kernel_times(case, sets, rra, stream, packed=mma)
-    if mma:   # the pipeline runs the packed path: pack with the row copy, then mma.sync attention
-        kt = {"index_us": kt["pack_copy_us"], "attend_us": kt["attend_packed_us"]}
+    fused = args.attend_kernel != "mma_sync"     # rra_pipeline: fused tcgen05 unless mma.sync is forced
+    kt = kernel_times(case, sets, rra, stream, packed=not fused)
     by = case_bytes(case)
-    if mma:
-        by["index"] = by["pack"]
-    kern = {k: round(v, 3) for k, v in kt.items()}
-    if kt["attend_us"] >= kt["index_us"]:
-        dom, roof = "attend_tc_kernel (gather)", roofline_obj(by["attend"], by["flops"], kt["attend_us"], peaks)
+    if fused:
+        kern = {"fused_us": round(kt["fused_us"], 3)}
+        roof = roofline_obj(by["fused_min"], by["flops"], kt["fused_us"], peaks)
+        roof["kernel"] = "attend_tc_kernel (fused pipeline: mask scan, gather, attention, zero fill)"
     else:
-        dom, roof = "pack_kernel (index pass)", roofline_obj(by["index"], 0, kt["index_us"], peaks)
-    roof["kernel"] = dom
+        kern = {"pack_copy_us": round(kt["pack_copy_us"], 3), "attend_packed_us": round(kt["attend_packed_us"], 3),
+                "fused_tcgen05_us": round(kt["fused_us"], 3)}
+        if kt["attend_packed_us"] >= kt["pack_copy_us"]:
+            roof = roofline_obj(by["attend"], by["flops"], kt["attend_packed_us"], peaks)
+            roof["kernel"] = "attend_mma_kernel (packed)"
+        else:
+            roof = roofline_obj(by["pack"], 0, kt["pack_copy_us"], peaks)
+            roof["kernel"] = "pack_kernel (row copy + indices + zero fill)"
     roof["peak_source"] = peaks["source"]
 
     extra = {}
@@ -503,11 +507,9 @@ def run_rra(args, world, rank, local):
         big_sets = InputSets(big, device, rra, big.dtype)
         bk = kernel_times(big, big_sets, rra, stream)
         bb = case_bytes(big)
-        extra["batched_b64_p80"] = {"workload": big_desc, "index_us": round(bk["index_us"], 3),
-                                    "attend_us": round(bk["attend_us"], 3),
-                                    "attend_roofline": roofline_obj(bb["attend"], bb["flops"], bk["attend_us"], peaks),
-                                    "pipeline_tokens_per_s": round(big.kept_tokens /
-                                                                   ((bk["index_us"] + bk["attend_us"]) * 1e-6), 1)}
+        extra["batched_b64_p80"] = {"workload": big_desc, "fused_us": round(bk["fused_us"], 3),
+                                    "roofline": roofline_obj(bb["fused_min"], bb["flops"], bk["fused_us"], peaks),
+                                    "pipeline_tokens_per_s": round(big.kept_tokens / (bk["fused_us"] * 1e-6), 1)}
         del big_sets
 
     cpu = None
@@ -523,8 +525,7 @@ def run_rra(args, world, rank, local):
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if case.dtype == torch.bfloat16 else "f16",
             "data": "synthetic (seeded N(0,1) Q/K/V, seeded keep masks)",
             "config": {"workload": desc, "B": B, "N": N, "H": H, "d": d, "kept_tokens_per_step": T,
-                       "path": f"CUDA graphs of {sets.R} pipeline steps (pack + attention with fused unpack), "
-                               "replayed back to back",
+                       "path": f"CUDA graphs of {sets.R} rra_pipeline steps, replayed back to back",
                        "l2": f"{sets.R} rotating input sets of {sets.per_set / 2**20:.1f} MiB "
                              f"({sets.R * sets.per_set / 2**20:.0f} MiB > L2)",
                        "parallelism": f"replicas x{world}"},
@@ -565,21 +566,16 @@ def run_sweep(args):
     cases += [W.make_progressive_layer(L, masks) for L in (1, 4, 7, 10)]
     for case in cases:
         sets = InputSets(case, device, rra, case.dtype)
-        mma = args.attend_kernel == "mma_sync" or (args.attend_kernel == "auto" and case.B * case.H < n_sms)
         kt = kernel_times(case, sets, rra, stream, packed=True)
-        if mma:   # the pipeline runs the packed path with the mma.sync attention
-            kt = {"index_us": kt["pack_copy_us"], "attend_us": kt["attend_packed_us"]}
         by = case_bytes(case)
-        roof_t = max(by["attend"] / (peaks["hbm_gbs"] * 1e9), by["flops"] / (peaks["bf16_tflops"] * 1e12)) * 1e6
-        fused_t = by["fused_min"] / (peaks["hbm_gbs"] * 1e9) * 1e6
-        pipe = kt["index_us"] + kt["attend_us"]
-        line = {"kernel": args.attend_kernel, "case": case.name, "B": case.B, "N": case.N, "H": case.H,
-                "T": case.kept_tokens, **{k: round(v, 3) for k, v in kt.items()},
-                "attend_roofline_us": round(roof_t, 3), "attend_frac": round(roof_t / kt["attend_us"], 4),
-                "attend": roofline_obj(by["attend"], by["flops"], kt["attend_us"], peaks),
-                "pipeline_us": round(pipe, 3), "pipeline_fused_min_us": round(fused_t, 3),
-                "pipeline_frac_of_fused_min": round(fused_t / pipe, 4),
-                "tokens_per_s": round(case.kept_tokens / (pipe * 1e-6), 1)}
+        fused_min_t = by["fused_min"] / (peaks["hbm_gbs"] * 1e9) * 1e6
+        two = kt["pack_copy_us"] + kt["attend_packed_us"]
+        line = {"case": case.name, "B": case.B, "N": case.N, "H": case.H, "T": case.kept_tokens,
+                **{k: round(v, 3) for k, v in kt.items()},
+                "fused_min_us": round(fused_min_t, 3), "fused_frac": round(fused_min_t / kt["fused_us"], 4),
+                "fused": roofline_obj(by["fused_min"], by["flops"], kt["fused_us"], peaks),
+                "two_launch_mma_us": round(two, 3),
+                "fused_tokens_per_s": round(case.kept_tokens / (kt["fused_us"] * 1e-6), 1)}
         print(json.dumps(line), flush=True)
         del sets
     return 0

@@ -143,17 +143,15 @@ RRA_API rra_status rra_attend_gather(const void* q, const void* k, const void* v
 RRA_API rra_status rra_unpack(const void* op, const int32_t* dst_idx, int B, int N, int H, int d,
                               rra_dtype dtype, void* out, void* stream);
 
-/* The whole path, two kernel launches, no host synchronisation, `out`
- * [B, N, H, d] of out_dtype.  With the default tcgen05 attention kernel:
- * an index pass (rra_pack's cu_seqlens / dst_idx / src_idx and zero fill of
- * pruned output rows, without the row copy), then attention that gathers
- * the kept Q/K/V rows straight from q/k/v (TMA gather4 on rows src_idx)
- * and scatters its rows into `out`; the packed sections of the workspace
- * are not written.  With RRA_ATTEND_MMA_SYNC selected: rra_pack (with the
- * row copy) then rra_attend on the packed buffers.  `workspace` holds
- * rra_workspace_bytes() bytes laid out as rra_workspace_offsets() states;
- * after the call its first three sections hold cu_seqlens and the pack
- * indices. */
+/* The whole path, no host synchronisation, `out` [B, N, H, d] of out_dtype.
+ * With the tcgen05 attention kernel (RRA_ATTEND_TCGEN05 or AUTO): ONE kernel launch that scans each image's keep row on the
+ * device, gathers the kept Q/K/V rows straight from q/k/v (TMA gather4),
+ * computes the attention and writes every output row -- kept positions get
+ * the attention, pruned ones +0; the workspace is not touched.  With the
+ * mma.sync kernel: rra_pack (with the row copy) then rra_attend on the
+ * packed buffers, two launches; after the call the workspace holds
+ * cu_seqlens, the pack indices and the packed Q/K/V.  `workspace` must hold
+ * rra_workspace_bytes() bytes in either case. */
 RRA_API rra_status rra_pipeline(const uint8_t* keep, const void* q, const void* k, const void* v,
                                 int B, int N, int H, int d, float scale, rra_dtype in_dtype,
                                 void* out, rra_dtype out_dtype,
@@ -217,10 +215,12 @@ RRA_API void rra_plan_destroy(rra_plan* plan);
  *                       padded inputs (no packed copy);
  *   RRA_ATTEND_MMA_SYNC warp-level mma.sync kernel on packed buffers;
  *                       rra_pipeline packs with the row copy first;
- *   RRA_ATTEND_AUTO     (default) MMA_SYNC when B*H is below the device's SM
- *                       count (too few (image, head) pairs to fill the GPU:
- *                       the shorter per-CTA latency chain wins), TCGEN05
- *                       otherwise. */
+ *   RRA_ATTEND_AUTO     (default) rra_attend: MMA_SYNC when B*H is below the
+ *                       device's SM count (too few (image, head) pairs to
+ *                       fill the GPU: the shorter per-CTA latency chain
+ *                       wins), TCGEN05 otherwise; rra_pipeline: always the
+ *                       fused one-launch TCGEN05 path (one launch beats two
+ *                       at every measured size). */
 typedef enum { RRA_ATTEND_TCGEN05 = 0, RRA_ATTEND_MMA_SYNC = 1, RRA_ATTEND_AUTO = 2 } rra_attend_kernel;
 RRA_API int rra_set_attend_kernel(int kernel);
 

@@ -204,6 +204,14 @@ rra_status check_pipeline(const PipelineArgs& p) {
   return RRA_OK;
 }
 
+// rra_pipeline's choice: the fused one-launch tcgen05 kernel unless the
+// mma.sync kernel was selected explicitly (one launch beats pack + attend
+// even where the batch is too small to fill the GPU).
+bool pipeline_fused() { return g_attend_kernel.load() != RRA_ATTEND_MMA_SYNC; }
+
+// Kernel launches one rra_pipeline call makes: 1 fused, 2 packed.
+int pipeline_launches(const DeviceState&, const PipelineArgs&) { return pipeline_fused() ? 1 : 2; }
+
 rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaStream_t s) {
   size_t off[6], total = 0;
   workspace_layout(p.B, p.N, p.H, p.d, p.in, off, &total);
@@ -211,19 +219,16 @@ rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaSt
   int32_t* cu = reinterpret_cast<int32_t*>(ws + off[0]);
   int32_t* dst = reinterpret_cast<int32_t*>(ws + off[1]);
   int32_t* src = reinterpret_cast<int32_t*>(ws + off[2]);
-  if (use_tcgen05(st, p.B, p.H)) {
-    // Index pass (cu_seqlens, pack indices, zero fill of pruned output rows),
-    // then attention gathering the kept rows straight from q/k/v.
+  if (pipeline_fused()) {
+    // One launch: the attention kernel scans the keep mask per image,
+    // gathers the kept rows straight from q/k/v and writes every output row.
     if (!attend_tc_available())
       return fail(RRA_ERR_CUDA, "pipeline: the driver's tensor-map encoder is unavailable");
-    RRA_TRY(enqueue_pack(st, p.keep, p.B, p.N, p.H, p.d, p.in, p.q, p.k, p.v, cu, dst, src, nullptr, nullptr,
-                         nullptr, p.out, p.out_dt, s));
     AttendArgs a{};
+    a.keep = p.keep;
     a.qp = p.q;
     a.kp = p.k;
     a.vp = p.v;
-    a.cu_seqlens = cu;
-    a.src_idx = src;
     a.o = p.out;
     a.B = p.B;
     a.H = p.H;
@@ -231,8 +236,8 @@ rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaSt
     a.max_seqlen = p.N;
     a.scale_log2 = p.scale * 1.4426950408889634f;
     a.err = st.err;
-    cudaError_t e = launch_attend_tc_gather(a, p.in, p.out_dt, st.num_sms, s);
-    if (e != cudaSuccess) return cuda_fail(e, "attend (gather) launch");
+    cudaError_t e = launch_attend_tc_fused(a, p.in, p.out_dt, st.num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "fused pipeline launch");
     return RRA_OK;
   }
   void* qp = ws + off[3];
@@ -413,7 +418,7 @@ rra_status rra_pipeline(const uint8_t* keep, const void* q, const void* k, const
   DeviceState* st = nullptr;
   RRA_TRY(device_state(&st));
   RRA_TRY(enqueue_pipeline(*st, p, static_cast<cudaStream_t>(stream)));
-  g_launches += 2;
+  g_launches += pipeline_launches(*st, p);
   return RRA_OK;
 }
 
@@ -442,7 +447,7 @@ rra_status rra_pipeline_host(const uint8_t* keep_h, const void* q_h, const void*
   if ((e = cudaMemcpyAsync(v_d, v_h, in_bytes, cudaMemcpyHostToDevice, s)) != cudaSuccess)
     return cuda_fail(e, "v H2D");
   RRA_TRY(enqueue_pipeline(*st, p, s));
-  g_launches += 2;
+  g_launches += pipeline_launches(*st, p);
   if ((e = cudaMemcpyAsync(out_h, out_d, out_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
     return cuda_fail(e, "out D2H");
   return RRA_OK;
@@ -464,7 +469,7 @@ rra_status rra_plan_create(const uint8_t* keep, const void* q, const void* k, co
   if (e != cudaSuccess) return cuda_fail(e, "cudaStreamCreate");
   rra_status rs = enqueue_pipeline(*st, p, s);
   if (rs == RRA_OK) {
-    g_launches += 2;
+    g_launches += pipeline_launches(*st, p);
     e = cudaStreamSynchronize(s);
     if (e != cudaSuccess) rs = cuda_fail(e, "plan warm-up");
   }
@@ -493,7 +498,7 @@ rra_status rra_plan_create(const uint8_t* keep, const void* q, const void* k, co
   rra_plan* pl = new rra_plan;
   pl->graph = graph;
   pl->exec = exec;
-  pl->launches = 2;
+  pl->launches = pipeline_launches(*st, p);
   *plan = pl;
   return RRA_OK;
 }

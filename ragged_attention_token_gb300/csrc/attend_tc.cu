@@ -61,10 +61,15 @@ constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;            // K[STAGES]
 constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;  // V[STAGES]
 constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
 // mbarriers: full[2] +0/+8, empty[2] +16/+24, qempty +32, mma +40; TMEM slot +48;
-// abort flag +52; redo flags +56/+60; item descriptors (2 x 32 B) +64.
+// abort flag +52; redo flags +56/+60; item descriptors (2 x 48 B) +64; then,
+// for the fused pipeline, POS_SLOTS lists of kept positions (int16, N each).
+constexpr uint32_t DESC_BYTES = 48;
 constexpr uint32_t OFF_DESC = OFF_BAR + 64;
-constexpr uint32_t SMEM_USED = OFF_DESC + STAGES * 32;
-constexpr uint32_t SMEM_ALLOC = SMEM_USED + 1024;      // slack to align the base to 1024 B
+constexpr uint32_t OFF_POS = OFF_DESC + STAGES * DESC_BYTES;
+constexpr int POS_SLOTS = 3;
+constexpr uint32_t SMEM_ALLOC = OFF_POS + 1024;        // + position lists; slack to align the base to 1024 B
+
+enum { MODE_PACKED = 0, MODE_GATHER = 1, MODE_FUSED = 2 };
 constexpr uint32_t TMEM_COLS = 128;                    // S/P: cols [0,64), O: cols [64,128)
 constexpr uint32_t WAIT_SUSPEND_NS = 20000;            // try_wait suspend hint
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
@@ -284,7 +289,7 @@ __device__ __forceinline__ void store_row<__half>(__half* dst, const float* o, f
 
 // One unit of work as every thread of the CTA sees it (all fields uniform).
 struct Unit {
-  int u, h, s0, n, q0, rows_q, nchunks;
+  int u, b, h, s0, n, q0, rows_q, nchunks;
 };
 
 // First unit at index >= u (stride `step`) whose query tile holds rows; a
@@ -306,12 +311,98 @@ __device__ __forceinline__ Unit next_unit(int u, int step, int units, int BH, co
     const int q0 = qt * BM;
     if (q0 >= n) continue;
     x.u = u;
+    x.b = b;
     x.h = h;
     x.s0 = s0;
     x.n = n;
     x.q0 = q0;
     x.rows_q = min(BM, n - q0);
     x.nchunks = (n + BN - 1) / BN;
+    return x;
+  }
+  x.u = units;
+  return x;
+}
+
+__device__ __forceinline__ void st_shared_u16(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u16 [%0], %1;" ::"r"(addr), "h"(static_cast<unsigned short>(v)) : "memory");
+}
+__device__ __forceinline__ int ld_shared_u16(uint32_t addr) {
+  unsigned short v;
+  asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(addr) : "memory");
+  return static_cast<int>(v);
+}
+
+// Fused pipeline, called by the 32 lanes of the producer warp: the next unit
+// at index >= u (stride `step`) whose query tile holds rows.  For every
+// candidate the warp scans its image's keep row with ballots: the kept
+// positions go, in order, to the int16 list at shared address `pos`; on the
+// (image, head)'s first query tile the output rows of pruned positions are
+// set to +0 (so every output row is written exactly once, images with no
+// kept token included).
+// Output rows (b, j, h) of pruned positions j -> +0 (producer warp, 32 lanes).
+template <typename Tout>
+__device__ __forceinline__ void zero_pruned_rows(const AttendArgs& a, int b, int h, int lane) {
+  constexpr int OUT_VECS = HD * static_cast<int>(sizeof(Tout)) / 16;
+  const uint8_t* krow = a.keep + static_cast<size_t>(b) * a.N;
+  for (int j = lane; j < a.N; j += 32) {
+    if (__ldg(krow + j) == 0) {
+      uint4* row =
+          reinterpret_cast<uint4*>(static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.N + j) * a.H + h) * HD);
+#pragma unroll
+      for (int v = 0; v < OUT_VECS; ++v) row[v] = make_uint4(0u, 0u, 0u, 0u);
+    }
+  }
+}
+
+// Fused pipeline, called by the 32 lanes of the producer warp: the next unit
+// at index >= u (stride `step`) whose query tile holds rows.  For every
+// candidate the warp scans its image's keep row with ballots; the kept
+// positions go, in order, to the int16 list at shared address `pos`.  A
+// candidate skipped for having no rows in its tile zeroes its (image, head)'s
+// pruned output rows here if it is the first query tile; the producer does
+// the same for a returned first-tile unit once its loads are in flight, so
+// every output row is written exactly once (images with no kept token too).
+template <typename Tout>
+__device__ Unit next_unit_fused(int u, int step, int units, int BH, const AttendArgs& a, int lane, uint32_t pos) {
+  Unit x;
+  const unsigned lt = (1u << lane) - 1u;
+  for (; u < units; u += step) {
+    const int qt = u / BH;
+    const int bh = u - qt * BH;
+    const int h = bh % a.H;
+    const int b = bh / a.H;
+    const uint8_t* krow = a.keep + static_cast<size_t>(b) * a.N;
+    int cnt = 0;
+    for (int j0 = 0; j0 < a.N; j0 += 8 * 32) {
+      bool flag[8];
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int j = j0 + r * 32 + lane;
+        flag[r] = (j < a.N) && (__ldg(krow + j) != 0);
+      }
+#pragma unroll
+      for (int r = 0; r < 8; ++r) {
+        const int j = j0 + r * 32 + lane;
+        const unsigned m = __ballot_sync(0xffffffffu, flag[r]);
+        if (flag[r]) st_shared_u16(pos + 2u * static_cast<uint32_t>(cnt + __popc(m & lt)), static_cast<uint32_t>(j));
+        cnt += __popc(m);
+      }
+    }
+    const int q0 = qt * BM;
+    if (q0 >= cnt) {
+      if (qt == 0) zero_pruned_rows<Tout>(a, b, h, lane);
+      continue;
+    }
+    x.u = u;
+    x.b = b;
+    x.h = h;
+    x.s0 = 0;
+    x.n = cnt;
+    x.q0 = q0;
+    x.rows_q = min(BM, cnt - q0);
+    x.nchunks = (cnt + BN - 1) / BN;
+    __syncwarp();
     return x;
   }
   x.u = units;
@@ -431,11 +522,14 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
   return true;
 }
 
-template <typename Tin, typename Tout, bool SCATTER, bool GATHER>
+template <typename Tin, typename Tout, bool SCATTER, int MODE>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v, const AttendArgs a, int qtiles, int units) {
+                     const __grid_constant__ CUtensorMap tmap_v, const AttendArgs a, int qtiles, int units,
+                     int pos_stride) {
   constexpr bool BF = IsBf16<Tin>::value == 1;
+  constexpr bool GATHER = MODE != MODE_PACKED;
+  constexpr bool FUSED = MODE == MODE_FUSED;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -447,7 +541,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   auto bar_empty = [&](int i) { return base + OFF_BAR + 16 + i * 8; };
   const uint32_t bar_qempty = base + OFF_BAR + 32, bar_mma = base + OFF_BAR + 40;
   const uint32_t slot = base + OFF_BAR + 48, abort_flag = base + OFF_BAR + 52;
-  auto desc_addr = [&](int i) { return base + OFF_DESC + i * 32; };
+  auto desc_addr = [&](int i) { return base + OFF_DESC + i * DESC_BYTES; };
+  auto pos_addr = [&](int slot) { return base + OFF_POS + slot * pos_stride; };
   const volatile uint32_t* slot_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + 48);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -483,7 +578,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     // publishes the item's descriptor, and issues the TMA loads that
     // complete the stage's full barrier.  Ends with a sentinel descriptor.
     uint32_t j = 0, uidx = 0;
-    Unit U = next_unit(blockIdx.x, step, units, BH, a, lane == 0);
+    Unit U;
+    if constexpr (FUSED) U = next_unit_fused<Tout>(blockIdx.x, step, units, BH, a, lane, pos_addr(0));
+    else U = next_unit(blockIdx.x, step, units, BH, a, lane == 0);
     bool done = false;
     while (!done && !bad) {
       const int nch = (U.u < units) ? U.nchunks : 1;
@@ -515,6 +612,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           st_shared_u32(d + 20, static_cast<uint32_t>(U.rows_q));
           st_shared_u32(d + 24, static_cast<uint32_t>(U.nchunks));
           st_shared_u32(d + 28, static_cast<uint32_t>(c));
+          st_shared_u32(d + 32, static_cast<uint32_t>(U.b));
+          st_shared_u32(d + 36, static_cast<uint32_t>(uidx % POS_SLOTS));
         }
         if constexpr (GATHER) {
           const int kgroups = ((n_c + 15) & ~15) / 4;
@@ -524,16 +623,26 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           if (lane < qgroups) {
             int rows[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              rows[i] = __ldg(a.src_idx + U.s0 + min(U.q0 + 4 * lane + i, U.q0 + U.rows_q - 1)) * a.H + U.h;
+            for (int i = 0; i < 4; ++i) {
+              const int t = min(U.q0 + 4 * lane + i, U.q0 + U.rows_q - 1);
+              if constexpr (FUSED)
+                rows[i] = (U.b * a.N + ld_shared_u16(pos_addr(uidx % POS_SLOTS) + 2 * t)) * a.H + U.h;
+              else
+                rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+            }
             tma_gather4(sQ + lane * 512, &tmap_q, rows, bar_full(st));
           }
           const int g = lane & 15;
           if (g < kgroups) {
             int rows[4];
 #pragma unroll
-            for (int i = 0; i < 4; ++i)
-              rows[i] = __ldg(a.src_idx + U.s0 + min(k0 + 4 * g + i, k0 + n_c - 1)) * a.H + U.h;
+            for (int i = 0; i < 4; ++i) {
+              const int t = min(k0 + 4 * g + i, k0 + n_c - 1);
+              if constexpr (FUSED)
+                rows[i] = (U.b * a.N + ld_shared_u16(pos_addr(uidx % POS_SLOTS) + 2 * t)) * a.H + U.h;
+              else
+                rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+            }
             if (lane < 16) tma_gather4(sK(st) + g * 512, &tmap_k, rows, bar_full(st));
             else tma_gather4(sV(st) + g * 512, &tmap_v, rows, bar_full(st));
           }
@@ -549,11 +658,17 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           }
         }
         __syncwarp();
+        if constexpr (FUSED) {
+          // The unit's first loads are in flight: now zero its (image,
+          // head)'s pruned output rows if this is the first query tile.
+          if (c == 0 && U.q0 == 0) zero_pruned_rows<Tout>(a, U.b, U.h, lane);
+        }
         ++j;
       }
       if (done || bad) break;
       ++uidx;
-      U = next_unit(U.u + step, step, units, BH, a, lane == 0);
+      if constexpr (FUSED) U = next_unit_fused<Tout>(U.u + step, step, units, BH, a, lane, pos_addr(uidx % POS_SLOTS));
+      else U = next_unit(U.u + step, step, units, BH, a, lane == 0);
     }
     if (!bad) {
       // Tail: wait for the consumers' last stage and Q releases, so that no
@@ -591,6 +706,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       const int rows_q = static_cast<int>(ld_shared_u32(d + 20));
       const int nchunks = static_cast<int>(ld_shared_u32(d + 24));
       const int c = static_cast<int>(ld_shared_u32(d + 28));
+      const int b = static_cast<int>(ld_shared_u32(d + 32));
+      const int pslot = static_cast<int>(ld_shared_u32(d + 36));
       const int k0 = c * BN;
       const int n_c = min(BN, n - k0);
       const int nk16 = (n_c + 15) & ~15;
@@ -726,7 +843,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         if (i < n) {
           long long dst_row = static_cast<long long>(s0) + i;
           bool ok = true;
-          if constexpr (SCATTER) {
+          if constexpr (FUSED) {
+            dst_row = static_cast<long long>(b) * a.N + ld_shared_u16(pos_addr(pslot) + 2 * i);
+          } else if constexpr (SCATTER) {
             dst_row = __ldg(a.src_idx + dst_row);
             if (dst_row < 0 || dst_row >= static_cast<long long>(a.B) * a.N) {
               record_error(a.err, RRA_DEVERR_INDEX_RANGE);
@@ -813,8 +932,11 @@ cudaError_t make_gather_map(CUtensorMap* map, const void* ptr, long long rows, b
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <typename Tin, typename Tout, bool SCATTER, bool GATHER>
+template <typename Tin, typename Tout, bool SCATTER, int MODE>
 cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t stream) {
+  // Largest dynamic shared memory any launch of this instantiation asks for
+  // (position lists for N <= 1024 in the fused mode).
+  constexpr uint32_t kMaxSmem = SMEM_ALLOC + (MODE == MODE_FUSED ? POS_SLOTS * 2048u : 0u);
   static bool attr_set[kMaxDev] = {};
   static std::mutex m;
   int dev = 0;
@@ -824,15 +946,15 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
   {
     std::lock_guard<std::mutex> lock(m);
     if (!attr_set[dev]) {
-      e = cudaFuncSetAttribute(attend_tc_kernel<Tin, Tout, SCATTER, GATHER>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(SMEM_ALLOC));
+      e = cudaFuncSetAttribute(attend_tc_kernel<Tin, Tout, SCATTER, MODE>,
+                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxSmem));
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }
   }
   const bool bf16 = IsBf16<Tin>::value == 1;
   CUtensorMap mq, mk, mv;
-  if constexpr (GATHER) {
+  if constexpr (MODE != MODE_PACKED) {
     const long long rows = static_cast<long long>(a.B) * a.N * a.H;
     if ((e = make_gather_map(&mq, a.qp, rows, bf16)) != cudaSuccess) return e;
     if ((e = make_gather_map(&mk, a.kp, rows, bf16)) != cudaSuccess) return e;
@@ -843,27 +965,30 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
     if ((e = make_map(&mk, a.kp, a.H, rows, bf16)) != cudaSuccess) return e;
     if ((e = make_map(&mv, a.vp, a.H, rows, bf16)) != cudaSuccess) return e;
   }
+  const int pos_stride = (MODE == MODE_FUSED) ? ((2 * a.N + 15) & ~15) : 0;
+  const uint32_t smem = SMEM_ALLOC + static_cast<uint32_t>(POS_SLOTS * pos_stride);
   const int qtiles = (a.max_seqlen + BM - 1) / BM;
   const long long units = static_cast<long long>(a.B) * a.H * qtiles;
   const long long cap = static_cast<long long>(CTAS_PER_SM) * (num_sms > 0 ? num_sms : 152);
   const int grid = static_cast<int>(units < cap ? units : cap);
-  attend_tc_kernel<Tin, Tout, SCATTER, GATHER><<<grid, THREADS, SMEM_ALLOC, stream>>>(
-      mq, mk, mv, a, qtiles, static_cast<int>(units));
+  attend_tc_kernel<Tin, Tout, SCATTER, MODE><<<grid, THREADS, smem, stream>>>(mq, mk, mv, a, qtiles,
+                                                                             static_cast<int>(units), pos_stride);
   return cudaGetLastError();
 }
 
 template <typename Tin, typename Tout>
-cudaError_t launch_tc_out(const AttendArgs& a, bool gather, int num_sms, cudaStream_t stream) {
-  if (gather) return launch_tc_typed<Tin, Tout, true, true>(a, num_sms, stream);
-  if (a.src_idx != nullptr) return launch_tc_typed<Tin, Tout, true, false>(a, num_sms, stream);
-  return launch_tc_typed<Tin, Tout, false, false>(a, num_sms, stream);
+cudaError_t launch_tc_out(const AttendArgs& a, int mode, int num_sms, cudaStream_t stream) {
+  if (mode == MODE_FUSED) return launch_tc_typed<Tin, Tout, true, MODE_FUSED>(a, num_sms, stream);
+  if (mode == MODE_GATHER) return launch_tc_typed<Tin, Tout, true, MODE_GATHER>(a, num_sms, stream);
+  if (a.src_idx != nullptr) return launch_tc_typed<Tin, Tout, true, MODE_PACKED>(a, num_sms, stream);
+  return launch_tc_typed<Tin, Tout, false, MODE_PACKED>(a, num_sms, stream);
 }
 
 template <typename Tin>
-cudaError_t launch_tc_in(const AttendArgs& a, rra_dtype out, bool gather, int num_sms, cudaStream_t stream) {
-  if (out == RRA_BF16) return launch_tc_out<Tin, __nv_bfloat16>(a, gather, num_sms, stream);
-  if (out == RRA_F16) return launch_tc_out<Tin, __half>(a, gather, num_sms, stream);
-  return launch_tc_out<Tin, float>(a, gather, num_sms, stream);
+cudaError_t launch_tc_in(const AttendArgs& a, rra_dtype out, int mode, int num_sms, cudaStream_t stream) {
+  if (out == RRA_BF16) return launch_tc_out<Tin, __nv_bfloat16>(a, mode, num_sms, stream);
+  if (out == RRA_F16) return launch_tc_out<Tin, __half>(a, mode, num_sms, stream);
+  return launch_tc_out<Tin, float>(a, mode, num_sms, stream);
 }
 
 }  // namespace
@@ -873,16 +998,24 @@ bool attend_tc_available() { return encode_fn(); }
 cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream) {
   if (!encode_fn()) return cudaErrorNotSupported;
   if (static_cast<long long>(a.B) * a.max_seqlen >= (1LL << 31)) return cudaErrorInvalidValue;
-  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, false, num_sms, stream);
-  return launch_tc_in<__half>(a, out, false, num_sms, stream);
+  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, MODE_PACKED, num_sms, stream);
+  return launch_tc_in<__half>(a, out, MODE_PACKED, num_sms, stream);
 }
 
 cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
                                     cudaStream_t stream) {
   if (!encode_fn()) return cudaErrorNotSupported;
   if (a.src_idx == nullptr) return cudaErrorInvalidValue;
-  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, true, num_sms, stream);
-  return launch_tc_in<__half>(a, out, true, num_sms, stream);
+  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, MODE_GATHER, num_sms, stream);
+  return launch_tc_in<__half>(a, out, MODE_GATHER, num_sms, stream);
+}
+
+cudaError_t launch_attend_tc_fused(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
+                                   cudaStream_t stream) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  if (a.keep == nullptr || a.N > 1024) return cudaErrorInvalidValue;
+  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, MODE_FUSED, num_sms, stream);
+  return launch_tc_in<__half>(a, out, MODE_FUSED, num_sms, stream);
 }
 
 }  // namespace rra

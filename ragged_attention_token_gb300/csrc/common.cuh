@@ -37,6 +37,7 @@ struct PackArgs {
 };
 
 struct AttendArgs {
+  const uint8_t* keep;      // fused pipeline only: the mask, scanned on the device
   const void* qp;
   const void* kp;
   const void* vp;
@@ -71,5 +72,11 @@ cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, i
 // tensors (a.qp/kp/vp) at rows src_idx[t], scattering to the padded output.
 cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
                                     cudaStream_t stream);
+// The whole pipeline in one launch: the same kernel scanning the keep mask
+// per image, gathering from the padded q/k/v, writing every output row
+// (attention at kept positions, +0 at pruned ones).  a.keep, a.qp/kp/vp
+// (padded), a.o, a.B, a.N, a.H, a.scale_log2, a.err are used.
+cudaError_t launch_attend_tc_fused(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
+                                   cudaStream_t stream);
 
 }  // namespace rra

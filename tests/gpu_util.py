@@ -50,6 +50,16 @@ def out_tolerance(ref: np.ndarray, dtype: torch.dtype) -> np.ndarray:
     return ATOL + 2.0 ** (e - explicit - 1)
 
 
+def pair_tolerance(ref: np.ndarray, dtype: torch.dtype) -> np.ndarray:
+    """The same rule for two stored GPU results: each may sit half an output ulp
+    from the exact value on its own side, so together they may differ by one ulp."""
+    if dtype == torch.float32:
+        return np.full(ref.shape, ATOL)
+    explicit = 7 if dtype == torch.bfloat16 else 10
+    e = np.floor(np.log2(np.maximum(np.abs(ref), 2.0 ** -60)))
+    return ATOL + 2.0 ** (e - explicit)
+
+
 def to_device(case, device="cuda"):
     return (case.keep.to(device), case.q.to(device), case.k.to(device), case.v.to(device))
 
