@@ -1,5 +1,5 @@
-// Bidirectional ragged attention on the packed buffers, sm_103a tensor-core
-// version: TMA tile loads, tcgen05.mma with TMEM accumulators.
+// Bidirectional ragged attention, sm_103a tensor-core kernel: TMA tile
+// loads, tcgen05.mma with TMEM accumulators, warp-specialised.
 //
 // Follows "Dispatch-Aware Ragged Attention for Pruned Vision Transformers",
 // abstract (non-causal attention over pruned ViT sequences of at most 197 /
@@ -7,34 +7,41 @@
 // (attention computed directly on the compact buffer).
 //
 // Work unit = (image b, head h, tile of 128 query rows).  Persistent CTAs of
-// 128 threads (four per SM) walk the units with a grid stride; a unit whose
-// tile starts past the image's length (read from cu_seqlens on the device)
-// costs two loads and is skipped.  Per unit, keys stream in chunks of 64:
+// 192 threads walk the units with a grid stride; a unit whose tile starts
+// past the image's length is skipped.  Per unit, keys stream in chunks of
+// 32; an item is one (unit, key chunk).  Warp roles:
 //
-//   TMA   Q tile (once) and the chunk's K and V rows -> shared memory, in
-//         32-row boxes of the packed [T, H, 64] tensor with the 128-byte
-//         swizzle, so at most 31 rows past the image are fetched;
-//   MMA   S = Q K^T (M=128, N=chunk rounded up to 16, K=64) -> TMEM cols 0..63;
-//   SIMT  thread r owns query row r (TMEM lane r): it reads its S row, takes
-//         the softmax max in base 2, and writes P as two bf16/fp16 parts
-//         (hi = round(p), lo = round(p - hi)) back over S in TMEM;
-//   MMA   O += P_hi V + P_lo V (M=128, N=64, K=chunk), A read from TMEM,
-//         O accumulating in TMEM cols 64..127 across the unit's chunks.
+//   warp 4     loads: per item, TMA copies of the chunk's K and V rows into a
+//              4-stage ring (and, on a unit's first item, of the Q tile),
+//              128-byte swizzle.  In the fused pipeline this warp also scans
+//              the image's keep row (kept positions -> a shared list) and
+//              writes +0 to the output rows of pruned positions;
+//   warp 5     tensor-core products, issued by one elected lane of the
+//              converged warp: S = Q K^T (M=128,
+//              N=chunk rounded up to 16, K=64) into one of two 32-column TMEM
+//              buffers, and O += P_hi V + P_lo V (M=128, N=64, K=chunk), P
+//              read from TMEM, O accumulating in TMEM columns 64..127;
+//   warps 0-3  softmax, thread r owning query row r (TMEM lane r): the row's
+//              max over the chunk, exponentials in base 2 against a per-row
+//              reference, P written over S as two bf16/fp16 parts; after a
+//              unit's last item, the epilogue (normalise, store the row).
 //
-// The softmax is lazily rescaled: exponentials use a per-row reference max
-// that only moves (rescaling O in TMEM) when a chunk's max exceeds it by
-// more than 8 in the log2 domain (bf16: a single pass against the running
-// reference, redone exactly only when a row's chunk sum exceeds 2^32).
-// The next item's K/V loads are issued before the current item computes (two
-// stages) and the next unit's Q right after the current unit's last S product.
+// With two S buffers the product S(j+1) runs while chunk j's softmax runs,
+// and P(j)V runs during chunk j+1's softmax.  Every hand-off between the
+// roles is an mbarrier; no warp waits at a CTA-wide barrier inside the loop.
 //
-// P is split because one bf16 rounding of the weights alone leaves up to
-// ~2e-3 of output error at these lengths; hi + lo carries ~16 bits.  Keys
-// past the image's end are masked (p = 0) and the V rows the MMA reads past
-// the end are zeroed in shared memory, so whatever the buffer holds there
-// (even NaN) never reaches a kept output.  Every mbarrier wait is bounded
-// by a clock-cycle limit: on expiry the CTA records RRA_DEVERR_WAIT_TIMEOUT,
-// waits (bounded) for its own copies, frees its TMEM and returns.
+// The reference max of a row only moves (rescaling O in TMEM, once the
+// previous P.V product has finished) when a chunk's max exceeds it by more
+// than 8 in the log2 domain, so every weight is at most 2^8.  P is split
+// because one bf16 rounding of the weights alone leaves up to ~2e-3 of
+// output error at these lengths; hi + lo carries ~16 bits.  Keys past the
+// image's end are masked (p = 0), and the V rows the product reads past the
+// end are either a repeated finite row (gathered loads) or zeroed in shared
+// memory (packed loads), so whatever the buffer holds there (even NaN) never
+// reaches a kept output.  Every mbarrier wait is bounded by a clock-cycle
+// limit and gives up early once another warp has raised the CTA's abort
+// flag; then the CTA records RRA_DEVERR_WAIT_TIMEOUT, waits (bounded) for
+// its own copies and products to land, frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -46,33 +53,53 @@ namespace rra {
 namespace {
 
 constexpr int BM = 128;        // query rows per unit (= TMEM lanes)
-constexpr int BN = 64;         // keys per chunk
+constexpr int BN = 32;         // keys per chunk (= columns of one S buffer)
 constexpr int HD = 64;         // head dim
-constexpr int CONSUMERS = 128;   // warps 0-3: MMA issue (thread 0) and softmax, one query row each
-constexpr int THREADS = CONSUMERS + 32;   // warp 4: TMA producer
+constexpr int CONSUMERS = 128;             // warps 0-3: softmax and epilogue
+constexpr int PRODUCER_WARP = 4;           // TMA loads (+ mask scan, zero fill)
+constexpr int MMA_WARP = 5;                // tcgen05.mma issue
+constexpr int THREADS = CONSUMERS + 64;
 constexpr int BOX = 32;        // rows per TMA box (packed inputs)
 constexpr int CTAS_PER_SM = 4;
-constexpr int STAGES = 2;      // K/V chunk ring
+constexpr int STAGES = 4;      // K/V chunk ring
 
 constexpr uint32_t Q_BYTES = BM * 128;                 // 128 rows x 128 B
-constexpr uint32_t KV_BYTES = BN * 128;                //  64 rows x 128 B
+constexpr uint32_t KV_BYTES = BN * 128;                //  32 rows x 128 B
 constexpr uint32_t OFF_Q = 0;                          // one Q tile
 constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;            // K[STAGES]
 constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;  // V[STAGES]
 constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
-// mbarriers: full[2] +0/+8, empty[2] +16/+24, qempty +32, mma +40; TMEM slot +48;
-// abort flag +52; redo flags +56/+60; item descriptors (2 x 48 B) +64; then,
-// for the fused pipeline, POS_SLOTS lists of kept positions (int16, N each).
+// mbarriers (8 B each) and words, as offsets from OFF_BAR.
+constexpr uint32_t B_FULL = 0;        // [STAGES] item loaded (TMA bytes + producer arrive)
+constexpr uint32_t B_EMPTY = 32;      // [STAGES] item's K/V consumed (its P.V product done)
+constexpr uint32_t B_QEMPTY = 64;     // unit's last S product done: Q buffer free
+constexpr uint32_t B_SFULL = 72;      // [2] S product in buffer done (or end of work)
+constexpr uint32_t B_SFREE = 88;      // [2] P.V product reading buffer done
+constexpr uint32_t B_PREADY = 104;    // [2] P written to buffer (128 consumer arrivals)
+constexpr uint32_t B_OFULL = 120;     // unit's last P.V product done
+constexpr uint32_t B_OEMPTY = 128;    // unit's O read out (128 consumer arrivals)
+constexpr uint32_t B_DRAIN = 136;     // every product issued has completed
+constexpr uint32_t W_TMEM = 144;      // TMEM base written by tcgen05.alloc
+constexpr uint32_t W_ABORT = 148;     // abort flag
+// Item descriptors, one per stage, then (fused pipeline) POS_SLOTS lists of
+// kept positions (int16, N each).
 constexpr uint32_t DESC_BYTES = 48;
-constexpr uint32_t OFF_DESC = OFF_BAR + 64;
+constexpr uint32_t OFF_DESC = OFF_BAR + 160;
 constexpr uint32_t OFF_POS = OFF_DESC + STAGES * DESC_BYTES;
-constexpr int POS_SLOTS = 3;
+// Five lists: the producer scans unit u + 5 only after the P.V product of
+// unit u + 1 has started, i.e. after every consumer has finished unit u's
+// epilogue (the last reader of its list).
+constexpr int POS_SLOTS = 5;
 constexpr uint32_t SMEM_ALLOC = OFF_POS + 1024;        // + position lists; slack to align the base to 1024 B
 
 enum { MODE_PACKED = 0, MODE_GATHER = 1, MODE_FUSED = 2 };
-constexpr uint32_t TMEM_COLS = 128;                    // S/P: cols [0,64), O: cols [64,128)
+constexpr uint32_t TMEM_COLS = 128;                    // S: cols [0,32) and [32,64); O: cols [64,128)
+constexpr uint32_t TMEM_O = 2 * BN;
 constexpr uint32_t WAIT_SUSPEND_NS = 20000;            // try_wait suspend hint
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
+
+static_assert(OFF_POS % 16 == 0, "position lists must start 16-byte aligned");
+static_assert(OFF_DESC + STAGES * DESC_BYTES <= OFF_POS, "descriptor ring overlaps");
 
 template <typename T> struct IsBf16;
 template <> struct IsBf16<__nv_bfloat16> { static constexpr uint32_t value = 1; };
@@ -101,14 +128,6 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity), "r"(WAIT_SUSPEND_NS)
       : "memory");
   return ok != 0;
-}
-// Bounded wait for the phase with the given parity; false when the limit passed.
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, long long limit) {
-  const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > limit) return false;
-  }
-  return true;
 }
 __device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
                                             uint32_t bar) {
@@ -249,42 +268,44 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+// 16 consecutive output elements of one row, o[i] * inv, as Tout.
 template <typename Tout>
-__device__ __forceinline__ void store_row(Tout* dst, const float* o, float inv);
+__device__ __forceinline__ void store16(Tout* dst, const float* o, float inv);
 template <>
-__device__ __forceinline__ void store_row<float>(float* dst, const float* o, float inv) {
+__device__ __forceinline__ void store16<float>(float* dst, const float* o, float inv) {
   float4* p = reinterpret_cast<float4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) p[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv,
-                                                  o[4 * i + 3] * inv);
+  for (int i = 0; i < 4; ++i)
+    p[i] = make_float4(o[4 * i] * inv, o[4 * i + 1] * inv, o[4 * i + 2] * inv, o[4 * i + 3] * inv);
+}
+template <typename T2>
+__device__ __forceinline__ uint32_t pack2(float x, float y);
+template <>
+__device__ __forceinline__ uint32_t pack2<__nv_bfloat162>(float x, float y) {
+  __nv_bfloat162 t = __floats2bfloat162_rn(x, y);
+  return *reinterpret_cast<uint32_t*>(&t);
 }
 template <>
-__device__ __forceinline__ void store_row<__nv_bfloat16>(__nv_bfloat16* dst, const float* o, float inv) {
+__device__ __forceinline__ uint32_t pack2<__half2>(float x, float y) {
+  __half2 t = __floats2half2_rn(x, y);
+  return *reinterpret_cast<uint32_t*>(&t);
+}
+template <typename T2>
+__device__ __forceinline__ void store16_half(void* dst, const float* o, float inv) {
   uint4* p = reinterpret_cast<uint4*>(dst);
 #pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      __nv_bfloat162 t = __floats2bfloat162_rn(o[8 * i + 2 * j] * inv, o[8 * i + 2 * j + 1] * inv);
-      w[j] = *reinterpret_cast<uint32_t*>(&t);
-    }
-    p[i] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
+  for (int i = 0; i < 2; ++i)
+    p[i] = make_uint4(pack2<T2>(o[8 * i] * inv, o[8 * i + 1] * inv), pack2<T2>(o[8 * i + 2] * inv, o[8 * i + 3] * inv),
+                      pack2<T2>(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
+                      pack2<T2>(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
 }
 template <>
-__device__ __forceinline__ void store_row<__half>(__half* dst, const float* o, float inv) {
-  uint4* p = reinterpret_cast<uint4*>(dst);
-#pragma unroll
-  for (int i = 0; i < 8; ++i) {
-    uint32_t w[4];
-#pragma unroll
-    for (int j = 0; j < 4; ++j) {
-      __half2 t = __floats2half2_rn(o[8 * i + 2 * j] * inv, o[8 * i + 2 * j + 1] * inv);
-      w[j] = *reinterpret_cast<uint32_t*>(&t);
-    }
-    p[i] = make_uint4(w[0], w[1], w[2], w[3]);
-  }
+__device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* dst, const float* o, float inv) {
+  store16_half<__nv_bfloat162>(dst, o, inv);
+}
+template <>
+__device__ __forceinline__ void store16<__half>(__half* dst, const float* o, float inv) {
+  store16_half<__half2>(dst, o, inv);
 }
 
 // One unit of work as every thread of the CTA sees it (all fields uniform).
@@ -333,24 +354,28 @@ __device__ __forceinline__ int ld_shared_u16(uint32_t addr) {
   return static_cast<int>(v);
 }
 
-// Fused pipeline, called by the 32 lanes of the producer warp: the next unit
-// at index >= u (stride `step`) whose query tile holds rows.  For every
-// candidate the warp scans its image's keep row with ballots: the kept
-// positions go, in order, to the int16 list at shared address `pos`; on the
-// (image, head)'s first query tile the output rows of pruned positions are
-// set to +0 (so every output row is written exactly once, images with no
-// kept token included).
 // Output rows (b, j, h) of pruned positions j -> +0 (producer warp, 32 lanes).
+// The mask bytes of 256 positions are loaded together before any store, so
+// a row of 197 positions costs one round trip to L2.
 template <typename Tout>
 __device__ __forceinline__ void zero_pruned_rows(const AttendArgs& a, int b, int h, int lane) {
   constexpr int OUT_VECS = HD * static_cast<int>(sizeof(Tout)) / 16;
   const uint8_t* krow = a.keep + static_cast<size_t>(b) * a.N;
-  for (int j = lane; j < a.N; j += 32) {
-    if (__ldg(krow + j) == 0) {
-      uint4* row =
-          reinterpret_cast<uint4*>(static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.N + j) * a.H + h) * HD);
+  for (int j0 = 0; j0 < a.N; j0 += 8 * 32) {
+    bool pruned[8];
 #pragma unroll
-      for (int v = 0; v < OUT_VECS; ++v) row[v] = make_uint4(0u, 0u, 0u, 0u);
+    for (int r = 0; r < 8; ++r) {
+      const int j = j0 + r * 32 + lane;
+      pruned[r] = (j < a.N) && (__ldg(krow + j) == 0);
+    }
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+      if (pruned[r]) {
+        const size_t j = static_cast<size_t>(j0 + r * 32 + lane);
+        uint4* row = reinterpret_cast<uint4*>(static_cast<Tout*>(a.o) + ((static_cast<size_t>(b) * a.N + j) * a.H + h) * HD);
+#pragma unroll
+        for (int v = 0; v < OUT_VECS; ++v) row[v] = make_uint4(0u, 0u, 0u, 0u);
+      }
     }
   }
 }
@@ -360,9 +385,11 @@ __device__ __forceinline__ void zero_pruned_rows(const AttendArgs& a, int b, int
 // candidate the warp scans its image's keep row with ballots; the kept
 // positions go, in order, to the int16 list at shared address `pos`.  A
 // candidate skipped for having no rows in its tile zeroes its (image, head)'s
-// pruned output rows here if it is the first query tile; the producer does
-// the same for a returned first-tile unit once its loads are in flight, so
-// every output row is written exactly once (images with no kept token too).
+// pruned output rows here if it is the first query tile; for a returned
+// first-tile unit the producer does it later, after the loads of the item
+// that follows are in flight, so every output row is written exactly once
+// (images with no kept token too) and the zero fill stays off the path that
+// feeds the tensor cores.
 template <typename Tout>
 __device__ Unit next_unit_fused(int u, int step, int units, int BH, const AttendArgs& a, int lane, uint32_t pos) {
   Unit x;
@@ -421,62 +448,141 @@ __device__ __forceinline__ void split2_bf16_trunc(float p0, float p1, uint32_t& 
   lo = *reinterpret_cast<uint32_t*>(&l);
 }
 
-// Exponentials of one S row chunk against reference mref, written back over
-// S in TMEM as P hi/lo pairs (each 16-column piece of S becomes 8 hi + 8 lo
-// columns in place); returns the chunk's row sum.  With ref_first the
-// reference is replaced by this row's first score (so that weight is exactly
-// 1: a one-token image returns V bit for bit) and written back to mref.
+
+// 32 consecutive fp32 columns of this thread's TMEM lane (wait tied to the
+// destination registers, as in tmem_ld16).
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%"
+      "28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+        "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+        "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;"
+               : "+r"(r[0]), "+r"(r[1]), "+r"(r[2]), "+r"(r[3]), "+r"(r[4]), "+r"(r[5]), "+r"(r[6]), "+r"(r[7]),
+                 "+r"(r[8]), "+r"(r[9]), "+r"(r[10]), "+r"(r[11]), "+r"(r[12]), "+r"(r[13]), "+r"(r[14]),
+                 "+r"(r[15]), "+r"(r[16]), "+r"(r[17]), "+r"(r[18]), "+r"(r[19]), "+r"(r[20]), "+r"(r[21]),
+                 "+r"(r[22]), "+r"(r[23]), "+r"(r[24]), "+r"(r[25]), "+r"(r[26]), "+r"(r[27]), "+r"(r[28]),
+                 "+r"(r[29]), "+r"(r[30]), "+r"(r[31])
+               :
+               : "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+// Three-input max / min (one instruction each on sm_100 and later).
+__device__ __forceinline__ float max3f(float x, float y, float z) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(x), "f"(y), "f"(z));
+  return d;
+}
+__device__ __forceinline__ float min3f(float x, float y, float z) {
+  float d;
+  asm("min.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(x), "f"(y), "f"(z));
+  return d;
+}
+
+// Largest (LOW: smallest) raw score over the chunk's valid columns.  Columns
+// at or past n_c are first replaced by -inf (LOW: +inf), so that with the
+// scale's sign they also give a weight of exactly 0 below.
+template <bool LOW>
+__device__ __forceinline__ float chunk_extreme(float (&t)[32], int n_c, bool full) {
+  const float pad = LOW ? INFINITY : -INFINITY;
+  if (!full) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) t[i] = (i < n_c) ? t[i] : pad;
+  }
+  float e[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float* s = t + 8 * k;
+    if constexpr (LOW) {
+      e[k] = min3f(min3f(min3f(s[0], s[1], s[2]), s[3], s[4]), s[5], s[6]);
+      e[k] = fminf(e[k], s[7]);
+    } else {
+      e[k] = max3f(max3f(max3f(s[0], s[1], s[2]), s[3], s[4]), s[5], s[6]);
+      e[k] = fmaxf(e[k], s[7]);
+    }
+  }
+  return LOW ? fminf(min3f(e[0], e[1], e[2]), e[3]) : fmaxf(max3f(e[0], e[1], e[2]), e[3]);
+}
+
+// Packed pairs of fp32 (sm_100 and later execute fma/add/sub on both halves
+// of a 64-bit register pair in one instruction).
+__device__ __forceinline__ uint64_t pack_f2(float a, float b) {
+  uint64_t r;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(r) : "f"(a), "f"(b));
+  return r;
+}
+__device__ __forceinline__ void unpack_f2(uint64_t v, float& a, float& b) {
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(v));
+}
+__device__ __forceinline__ uint64_t fma_f2(uint64_t a, uint64_t b, uint64_t c) {
+  uint64_t d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
+__device__ __forceinline__ uint64_t add_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+__device__ __forceinline__ uint64_t sub_f2(uint64_t a, uint64_t b) {
+  uint64_t d;
+  asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  return d;
+}
+
+// Weights p = 2^(c2*s - mref) of one chunk row, written back over S in TMEM
+// as hi/lo pairs (each 16-column piece of S becomes 8 hi + 8 lo columns in
+// place); returns their sum.  Masked columns hold -inf*sign(c2) and give 0.
+// bf16: hi = p truncated to bf16 (exact), lo = p - hi (exact in fp32)
+// rounded to bf16; fp16: hi = p rounded to fp16, lo = p - hi rounded.
 template <bool BF16>
-__device__ __forceinline__ float chunk_weights(uint32_t tS_row, int nk16, int n_c, bool full, float c2, float& mref,
-                                               bool ref_first) {
-  float l4[4] = {0.f, 0.f, 0.f, 0.f};
+__device__ __forceinline__ float write_weights(uint32_t tS_row, const float (&t)[32], int nk16, float c2,
+                                              float mref) {
+  const uint64_t c2x2 = pack_f2(c2, c2), nm2 = pack_f2(-mref, -mref);
+  uint64_t acc[2] = {0ull, 0ull};   // packed partial sums (+0.0f pairs)
 #pragma unroll
   for (int g = 0; g < BN / 16; ++g) {
-    if (g * 16 < nk16) {
-      float t[16];
-      tmem_ld16(tS_row + g * 16, t);
-      if (g == 0 && ref_first) mref = t[0] * c2;
+    if (g == 0 || nk16 > 16) {
       uint32_t hi[8], lo[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
-        const int j = g * 16 + 2 * i;
-        float p0 = fast_exp2(fmaf(t[2 * i], c2, -mref));
-        float p1 = fast_exp2(fmaf(t[2 * i + 1], c2, -mref));
-        if (!full) {
-          p0 = (j < n_c) ? p0 : 0.f;
-          p1 = (j + 1 < n_c) ? p1 : 0.f;
+        float x0, x1;
+        unpack_f2(fma_f2(pack_f2(t[16 * g + 2 * i], t[16 * g + 2 * i + 1]), c2x2, nm2), x0, x1);
+        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+        const uint64_t pp = pack_f2(p0, p1);
+        acc[i & 1] = add_f2(acc[i & 1], pp);
+        float r0, r1;
+        if constexpr (BF16) {
+          const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
+          hi[i] = __byte_perm(b0, b1, 0x7632);
+          unpack_f2(sub_f2(pp, pack_f2(__uint_as_float(b0 & 0xFFFF0000u), __uint_as_float(b1 & 0xFFFF0000u))), r0,
+                    r1);
+          __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+          lo[i] = *reinterpret_cast<uint32_t*>(&l);
+        } else {
+          const __half2 h = __floats2half2_rn(p0, p1);
+          hi[i] = *reinterpret_cast<const uint32_t*>(&h);
+          unpack_f2(sub_f2(pp, pack_f2(__low2float(h), __high2float(h))), r0, r1);
+          const __half2 l = __floats2half2_rn(r0, r1);
+          lo[i] = *reinterpret_cast<const uint32_t*>(&l);
         }
-        l4[(2 * i) & 3] += p0;
-        l4[(2 * i + 1) & 3] += p1;
-        if constexpr (BF16) split2_bf16_trunc(p0, p1, hi[i], lo[i]);
-        else split2<false>(p0, p1, hi[i], lo[i]);
       }
       tmem_st8(tS_row + g * 16, hi);
       tmem_st8(tS_row + g * 16 + 8, lo);
     }
   }
-  return (l4[0] + l4[1]) + (l4[2] + l4[3]);
-}
-
-// Max of scale*S over the chunk's valid columns.
-__device__ __forceinline__ float chunk_max(uint32_t tS_row, int nk16, int n_c, bool full, float c2) {
-  float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
-#pragma unroll
-  for (int g = 0; g < BN / 16; ++g) {
-    if (g * 16 < nk16) {
-      float t[16];
-      tmem_ld16(tS_row + g * 16, t);
-      if (full) {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) mx4[i & 3] = fmaxf(mx4[i & 3], t[i] * c2);
-      } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i)
-          if (g * 16 + i < n_c) mx4[i & 3] = fmaxf(mx4[i & 3], t[i] * c2);
-      }
-    }
-  }
-  return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+  float s0, s1, s2, s3;
+  unpack_f2(acc[0], s0, s1);
+  unpack_f2(acc[1], s2, s3);
+  return (s0 + s1) + (s2 + s3);
 }
 
 // O row (TMEM) *= alpha.
@@ -493,17 +599,6 @@ __device__ __forceinline__ void rescale_o(uint32_t tO_row, float alpha) {
   }
 }
 
-// Consumer-only barrier (named barrier 1, the 128 consumer threads) that
-// also ORs a predicate across them.
-__device__ __forceinline__ bool consumer_sync_or(bool pred) {
-  uint32_t r;
-  asm volatile(
-      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n barrier.cta.red.or.pred q, 1, 128, p;\n selp.u32 %0, 1, 0, q;\n}\n"
-      : "=r"(r)
-      : "r"(pred ? 1u : 0u)
-      : "memory");
-  return r != 0;
-}
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
@@ -521,12 +616,25 @@ __device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity
   }
   return true;
 }
+// One lane of a converged warp (the same lane every time the full warp asks).
+// tcgen05.mma and tcgen05.commit are issued from converged warp code with
+// this predicate: issued from a single-thread branch instead, each costs
+// ~100 cycles of issue latency against ~45 here.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred = 0;
+  asm volatile(
+      "{\n .reg .pred p;\n elect.sync _|p, 0xffffffff;\n selp.u32 %0, 1, 0, p;\n}\n"
+      : "=r"(pred));
+  return pred != 0;
+}
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
 
 template <typename Tin, typename Tout, bool SCATTER, int MODE>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v, const AttendArgs a, int qtiles, int units,
-                     int pos_stride) {
+                     const __grid_constant__ CUtensorMap tmap_v, const AttendArgs a, int units, int pos_stride) {
   constexpr bool BF = IsBf16<Tin>::value == 1;
   constexpr bool GATHER = MODE != MODE_PACKED;
   constexpr bool FUSED = MODE == MODE_FUSED;
@@ -537,17 +645,21 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   const uint32_t sQ = base + OFF_Q;
   auto sK = [&](int i) { return base + OFF_K + i * KV_BYTES; };
   auto sV = [&](int i) { return base + OFF_V + i * KV_BYTES; };
-  auto bar_full = [&](int i) { return base + OFF_BAR + i * 8; };
-  auto bar_empty = [&](int i) { return base + OFF_BAR + 16 + i * 8; };
-  const uint32_t bar_qempty = base + OFF_BAR + 32, bar_mma = base + OFF_BAR + 40;
-  const uint32_t slot = base + OFF_BAR + 48, abort_flag = base + OFF_BAR + 52;
+  const uint32_t bars = base + OFF_BAR;
+  auto bar_full = [&](int i) { return bars + B_FULL + 8 * i; };
+  auto bar_empty = [&](int i) { return bars + B_EMPTY + 8 * i; };
+  auto bar_sfull = [&](int i) { return bars + B_SFULL + 8 * i; };
+  auto bar_sfree = [&](int i) { return bars + B_SFREE + 8 * i; };
+  auto bar_pready = [&](int i) { return bars + B_PREADY + 8 * i; };
+  const uint32_t bar_qempty = bars + B_QEMPTY, bar_ofull = bars + B_OFULL, bar_oempty = bars + B_OEMPTY;
+  const uint32_t bar_drain = bars + B_DRAIN, abort_flag = bars + W_ABORT;
   auto desc_addr = [&](int i) { return base + OFF_DESC + i * DESC_BYTES; };
-  auto pos_addr = [&](int slot) { return base + OFF_POS + slot * pos_stride; };
-  const volatile uint32_t* slot_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + 48);
+  auto pos_addr = [&](int s) { return base + OFF_POS + s * pos_stride; };
+  const volatile uint32_t* tmem_ptr = reinterpret_cast<const volatile uint32_t*>(gbase + OFF_BAR + W_TMEM);
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   if (warp == 0) {
-    tmem_alloc(slot, TMEM_COLS);
+    tmem_alloc(bars + W_TMEM, TMEM_COLS);
     tmem_relinquish();
   }
   if (tid == 32) {
@@ -556,45 +668,55 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       mbar_init(bar_empty(i), 1);
     }
     mbar_init(bar_qempty, 1);
-    mbar_init(bar_mma, 1);
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(bar_sfull(i), 1);
+      mbar_init(bar_sfree(i), 1);
+      mbar_init(bar_pready(i), CONSUMERS);
+    }
+    mbar_init(bar_ofull, 1);
+    mbar_init(bar_oempty, CONSUMERS);
+    mbar_init(bar_drain, 1);
     st_shared_u32(abort_flag, 0u);
-    st_shared_u32(base + OFF_BAR + 56, 0u);
-    st_shared_u32(base + OFF_BAR + 60, 0u);
     fence_barrier_init();
+  }
+  if (warp == PRODUCER_WARP && lane == 0) {
+    prefetch_tensormap(&tmap_q);
+    prefetch_tensormap(&tmap_k);
+    prefetch_tensormap(&tmap_v);
   }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  const uint32_t tmem = *slot_ptr;
+  const uint32_t tmem = *tmem_ptr;
   const int BH = a.B * a.H;
   const int step = gridDim.x;
-  (void)qtiles;
   bool bad = false;
 
-  if (warp == 4) {
-    // ------------------------------------------------------------ producer
-    // Walks this CTA's items (unit, key chunk) in order.  For each: waits
-    // until its stage (and, on a unit's first chunk, the Q buffer) is free,
-    // publishes the item's descriptor, and issues the TMA loads that
-    // complete the stage's full barrier.  Ends with a sentinel descriptor.
+  if (warp == PRODUCER_WARP) {
+    // ------------------------------------------------------------ loads
+    // Walks this CTA's items in order.  For each: waits until its stage
+    // (and, on a unit's first item, the Q buffer) is free, publishes the
+    // item's descriptor and issues the TMA loads that complete the stage's
+    // full barrier.  Ends with a sentinel descriptor (plain arrive).
     uint32_t j = 0, uidx = 0;
     Unit U;
     if constexpr (FUSED) U = next_unit_fused<Tout>(blockIdx.x, step, units, BH, a, lane, pos_addr(0));
     else U = next_unit(blockIdx.x, step, units, BH, a, lane == 0);
+    int zb = -1, zh = 0;   // fused: (image, head) whose pruned output rows are still to be zeroed
     bool done = false;
     while (!done && !bad) {
-      const int nch = (U.u < units) ? U.nchunks : 1;
-      for (int c = 0; c < nch && !bad; ++c) {
-        const int st = j & 1;
-        if (j >= STAGES) bad |= !mbar_wait_or_abort(bar_empty(st), ((j >> 1) - 1) & 1, abort_flag);
-        if (U.u < units && c == 0 && uidx >= 1)
-          bad |= !mbar_wait_or_abort(bar_qempty, (uidx - 1) & 1, abort_flag);
+      const bool sentinel = U.u >= units;
+      const int nch = sentinel ? 1 : U.nchunks;
+      for (int c = 0; c < nch; ++c) {
+        const int st = static_cast<int>(j % STAGES);
+        if (j >= STAGES) bad |= !mbar_wait_or_abort(bar_empty(st), ((j / STAGES) - 1) & 1, abort_flag);
+        if (!sentinel && c == 0 && uidx >= 1) bad |= !mbar_wait_or_abort(bar_qempty, (uidx - 1) & 1, abort_flag);
         bad = __any_sync(0xffffffffu, bad);
         if (bad) break;
-        if (U.u >= units) {
-          // Sentinel: no more items.
+        const uint32_t d = desc_addr(st);
+        if (sentinel) {
           if (lane == 0) {
-            st_shared_u32(desc_addr(st), static_cast<uint32_t>(units));
+            st_shared_u32(d + 0, static_cast<uint32_t>(units));
             mbar_arrive(bar_full(st));
           }
           done = true;
@@ -603,7 +725,6 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         const int k0 = c * BN;
         const int n_c = min(BN, U.n - k0);
         if (lane == 0) {
-          const uint32_t d = desc_addr(st);
           st_shared_u32(d + 0, static_cast<uint32_t>(U.u));
           st_shared_u32(d + 4, static_cast<uint32_t>(U.h));
           st_shared_u32(d + 8, static_cast<uint32_t>(U.s0));
@@ -616,19 +737,19 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           st_shared_u32(d + 36, static_cast<uint32_t>(uidx % POS_SLOTS));
         }
         if constexpr (GATHER) {
+          // K and V: lanes 0-7 and 16-23, one 4-row gather each; Q: up to 32 lanes.
           const int kgroups = ((n_c + 15) & ~15) / 4;
           const int qgroups = (c == 0) ? (U.rows_q + 3) / 4 : 0;
           if (lane == 0) mbar_expect_tx(bar_full(st), static_cast<uint32_t>((2 * kgroups + qgroups) * 512));
           __syncwarp();
+          const uint32_t pslot = pos_addr(static_cast<int>(uidx % POS_SLOTS));
           if (lane < qgroups) {
             int rows[4];
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int t = min(U.q0 + 4 * lane + i, U.q0 + U.rows_q - 1);
-              if constexpr (FUSED)
-                rows[i] = (U.b * a.N + ld_shared_u16(pos_addr(uidx % POS_SLOTS) + 2 * t)) * a.H + U.h;
-              else
-                rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+              if constexpr (FUSED) rows[i] = (U.b * a.N + ld_shared_u16(pslot + 2 * t)) * a.H + U.h;
+              else rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
             }
             tma_gather4(sQ + lane * 512, &tmap_q, rows, bar_full(st));
           }
@@ -638,250 +759,281 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
               const int t = min(k0 + 4 * g + i, k0 + n_c - 1);
-              if constexpr (FUSED)
-                rows[i] = (U.b * a.N + ld_shared_u16(pos_addr(uidx % POS_SLOTS) + 2 * t)) * a.H + U.h;
-              else
-                rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+              if constexpr (FUSED) rows[i] = (U.b * a.N + ld_shared_u16(pslot + 2 * t)) * a.H + U.h;
+              else rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
             }
             if (lane < 16) tma_gather4(sK(st) + g * 512, &tmap_k, rows, bar_full(st));
             else tma_gather4(sV(st) + g * 512, &tmap_v, rows, bar_full(st));
           }
         } else if (lane == 0) {
-          const int kboxes = (n_c + BOX - 1) / BOX;
+          // One 32-row box each for K and V; Q in up to four boxes.
           const int qboxes = (c == 0) ? (U.rows_q + BOX - 1) / BOX : 0;
-          mbar_expect_tx(bar_full(st), static_cast<uint32_t>((2 * kboxes + qboxes) * BOX * 128));
+          mbar_expect_tx(bar_full(st), static_cast<uint32_t>((2 + qboxes) * BOX * 128));
           for (int jj = 0; jj < qboxes; ++jj)
             tma_load_3d(sQ + jj * BOX * 128, &tmap_q, 0, U.h, U.s0 + U.q0 + jj * BOX, bar_full(st));
-          for (int jj = 0; jj < kboxes; ++jj) {
-            tma_load_3d(sK(st) + jj * BOX * 128, &tmap_k, 0, U.h, U.s0 + k0 + jj * BOX, bar_full(st));
-            tma_load_3d(sV(st) + jj * BOX * 128, &tmap_v, 0, U.h, U.s0 + k0 + jj * BOX, bar_full(st));
-          }
+          tma_load_3d(sK(st), &tmap_k, 0, U.h, U.s0 + k0, bar_full(st));
+          tma_load_3d(sV(st), &tmap_v, 0, U.h, U.s0 + k0, bar_full(st));
         }
         __syncwarp();
         if constexpr (FUSED) {
-          // The unit's first loads are in flight: now zero its (image,
-          // head)'s pruned output rows if this is the first query tile.
-          if (c == 0 && U.q0 == 0) zero_pruned_rows<Tout>(a, U.b, U.h, lane);
+          if (zb >= 0) {
+            zero_pruned_rows<Tout>(a, zb, zh, lane);
+            zb = -1;
+          }
         }
         ++j;
       }
       if (done || bad) break;
+      if constexpr (FUSED) {
+        if (U.q0 == 0) {
+          zb = U.b;
+          zh = U.h;
+        }
+      }
       ++uidx;
       if constexpr (FUSED) U = next_unit_fused<Tout>(U.u + step, step, units, BH, a, lane, pos_addr(uidx % POS_SLOTS));
       else U = next_unit(U.u + step, step, units, BH, a, lane == 0);
     }
+    if constexpr (FUSED) {
+      if (!bad && zb >= 0) zero_pruned_rows<Tout>(a, zb, zh, lane);
+    }
+  } else if (warp == MMA_WARP) {
+    // ------------------------------------------------------------ products
+    // Order: S(0); then for each item jp: S(jp+1) (needs its loads and the
+    // P.V product of item jp-1, which read the same S buffer), then, once the
+    // consumers have written P(jp), O += P(jp) V (a unit's first one waits
+    // until the consumers have read out the previous unit's O).
+    const uint32_t idesc_pv = idesc_f16(BF ? 1u : 0u, 1, BM, HD);
+    uint32_t k = 0, jp = 0, ustarted = 0;
+    int info0 = 0, info1 = 0;   // per S buffer: nk16 | first << 8 | last << 9
+    bool end = false;
+    auto issue_s = [&]() {
+      const int st = static_cast<int>(k % STAGES);
+      bad |= !mbar_wait_or_abort(bar_full(st), (k / STAGES) & 1, abort_flag);
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad) return;
+      const uint32_t d = desc_addr(st);
+      if (static_cast<int>(ld_shared_u32(d + 0)) >= units) {
+        // End of work: the consumers learn it from this buffer's S barrier.
+        end = true;
+        if (elect_one()) umma_commit(bar_sfull(k & 1));
+        return;
+      }
+      const int n = static_cast<int>(ld_shared_u32(d + 12));
+      const int nch = static_cast<int>(ld_shared_u32(d + 24));
+      const int c = static_cast<int>(ld_shared_u32(d + 28));
+      const int n_c = min(BN, n - c * BN);
+      const int nk16 = (n_c + 15) & ~15;
+      const bool last = c == nch - 1;
+      if (k >= 2) {
+        bad |= !mbar_wait_or_abort(bar_sfree(k & 1), ((k - 2) >> 1) & 1, abort_flag);
+        bad = __any_sync(0xffffffffu, bad);
+        if (bad) return;
+      }
+      if constexpr (!GATHER) {
+        // Packed boxes: V rows [n_c, nk16) enter the P.V product with p = 0;
+        // make them finite zeros (the gathered path repeats a valid row).
+        const int zvec = (nk16 - n_c) * 8;
+        for (int zi = lane; zi < zvec; zi += 32)
+          st_shared_v4(sV(st) + (n_c + (zi >> 3)) * 128 + (zi & 7) * 16, 0u, 0u, 0u, 0u);
+        fence_proxy_async();
+        __syncwarp();
+      }
+      tc_fence_after();
+      {
+        const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
+        const uint32_t tS = tmem + (k & 1) * BN;
+        const bool leader = elect_one();
+#pragma unroll
+        for (int kk = 0; kk < HD / 16; ++kk) {
+          const uint64_t da = sdesc(sQ + kk * 32, 16, 1024), db = sdesc(sK(st) + kk * 32, 16, 1024);
+          if (leader) umma_f16(tS, da, db, idesc_s, kk > 0 ? 1u : 0u);
+        }
+        if (leader) umma_commit(bar_sfull(k & 1));
+        if (leader && last) umma_commit(bar_qempty);
+      }
+      const int inf = nk16 | (c == 0 ? 256 : 0) | (last ? 512 : 0);
+      if (k & 1) info1 = inf;
+      else info0 = inf;
+      ++k;
+    };
+    issue_s();
+    while (!bad && jp < k) {
+      if (!end) {
+        issue_s();
+        if (bad) break;
+      }
+      const int b = static_cast<int>(jp & 1);
+      const int inf = b ? info1 : info0;
+      const bool first = (inf & 256) != 0, last = (inf & 512) != 0;
+      const int nk16 = inf & 255;
+      bad |= !mbar_wait_or_abort(bar_pready(b), (jp >> 1) & 1, abort_flag);
+      if (first && ustarted >= 1) bad |= !mbar_wait_or_abort(bar_oempty, (ustarted - 1) & 1, abort_flag);
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad) break;
+      if (first) ++ustarted;
+      tc_fence_after();
+      {
+        const int st = static_cast<int>(jp % STAGES);
+        const uint32_t tS = tmem + b * BN, tO = tmem + TMEM_O;
+        const bool leader = elect_one();
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          if (kk * 16 < nk16) {
+            const uint64_t db = sdesc(sV(st) + kk * 2048, KV_BYTES, 1024);
+            if (leader) umma_f16_tmem_a(tO, tS + kk * 16, db, idesc_pv, (kk > 0 || !first) ? 1u : 0u);
+          }
+        }
+#pragma unroll
+        for (int kk = 0; kk < BN / 16; ++kk) {
+          if (kk * 16 < nk16) {
+            const uint64_t db = sdesc(sV(st) + kk * 2048, KV_BYTES, 1024);
+            if (leader) umma_f16_tmem_a(tO, tS + kk * 16 + 8, db, idesc_pv, 1u);
+          }
+        }
+        if (leader) umma_commit(bar_empty(st));
+        if (leader) umma_commit(bar_sfree(b));
+        if (leader && last) umma_commit(bar_ofull);
+      }
+      ++jp;
+    }
     if (!bad) {
-      // Tail: wait for the consumers' last stage and Q releases, so that no
-      // asynchronous arrive lands after the CTA has gone.
-      if (j >= 1) bad |= !mbar_wait_or_abort(bar_empty((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag);
-      if (uidx >= 1) bad |= !mbar_wait_or_abort(bar_qempty, (uidx - 1) & 1, abort_flag);
+      // Every product issued has completed (and with it the arrivals above).
+      if (elect_one()) umma_commit(bar_drain);
+      bad |= !mbar_wait_or_abort(bar_drain, 0, abort_flag);
       bad = __any_sync(0xffffffffu, bad);
     }
-    if (bad) {
-      if (lane == 0) {
-        st_shared_u32(abort_flag, 1u);
-        record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
-      }
-    }
   } else {
-    // ------------------------------------------------------------ consumers
+    // ------------------------------------------------------------ softmax
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tS = tmem, tO = tmem + 64;
-    const uint32_t tS_row = tS + lane_off, tO_row = tO + lane_off;
-    const uint32_t idesc_pv = idesc_f16(BF ? 1u : 0u, 1, BM, HD);
-    const float c2 = a.scale_log2;
-    uint32_t ph_mma = 0;
-    float m_run = 0.f, l_run = 0.f;   // this row's reference max (log2 units) and sum
+    const uint32_t tO_row = tmem + TMEM_O + lane_off;
+    // A zero scale would make the masked -inf columns NaN; 1e-30 gives the
+    // same weights (all exactly 1) with the masking intact.
+    const float c2 = (a.scale_log2 == 0.f) ? 1e-30f : a.scale_log2;
+    uint32_t uidx = 0;
+    float m_run = 0.f, l_run = 0.f;   // this row's reference max (log2 units) and weight sum
+    long long out_elem = -1;          // this row's output offset in the current unit
     for (uint32_t j = 0;; ++j) {
-      const int st = j & 1;
-      bad |= !mbar_wait_or_abort(bar_full(st), (j >> 1) & 1, abort_flag);
-      if (consumer_sync_or(bad)) { bad = true; break; }
+      const int b = static_cast<int>(j & 1), st = static_cast<int>(j % STAGES);
+      bad |= !mbar_wait_or_abort(bar_sfull(b), (j >> 1) & 1, abort_flag);
+      bad |= !mbar_wait_or_abort(bar_full(st), (j / STAGES) & 1, abort_flag);
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad) break;
       const uint32_t d = desc_addr(st);
-      const int u = static_cast<int>(ld_shared_u32(d + 0));
-      if (u >= units) break;   // sentinel
-      const int h = static_cast<int>(ld_shared_u32(d + 4));
-      const int s0 = static_cast<int>(ld_shared_u32(d + 8));
+      if (static_cast<int>(ld_shared_u32(d + 0)) >= units) break;   // sentinel
       const int n = static_cast<int>(ld_shared_u32(d + 12));
-      const int q0 = static_cast<int>(ld_shared_u32(d + 16));
       const int rows_q = static_cast<int>(ld_shared_u32(d + 20));
       const int nchunks = static_cast<int>(ld_shared_u32(d + 24));
       const int c = static_cast<int>(ld_shared_u32(d + 28));
-      const int b = static_cast<int>(ld_shared_u32(d + 32));
-      const int pslot = static_cast<int>(ld_shared_u32(d + 36));
-      const int k0 = c * BN;
-      const int n_c = min(BN, n - k0);
+      const int n_c = min(BN, n - c * BN);
       const int nk16 = (n_c + 15) & ~15;
       const bool full = (n_c == BN);
       const bool rows_here = warp * 32 < rows_q;   // warp-uniform
       const bool last = (c == nchunks - 1);
-
-      // S = Q K^T -> TMEM columns [0, nk16).  Packed inputs: warp 0 first
-      // zeroes the V rows [n_c, nk16) that enter the MMA with p = 0 (the
-      // gathered path repeats a finite row there instead).
-      if (warp == 0) {
-        if constexpr (!GATHER) {
-          const int zvec = (nk16 - n_c) * 8;
-          for (int zi = lane; zi < zvec; zi += 32)
-            st_shared_v4(sV(st) + (n_c + (zi >> 3)) * 128 + (zi & 7) * 16, 0u, 0u, 0u, 0u);
-          fence_proxy_async();
-          __syncwarp();
-        }
-        if (tid == 0) {
-          tc_fence_after();
-          const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(st) + kk * 32, 16, 1024), idesc_s,
-                     kk > 0 ? 1u : 0u);
-          umma_commit(bar_mma);
-        }
-      }
-      bad |= !mbar_wait_or_abort(bar_mma, ph_mma, abort_flag);
-      if (!bad) ph_mma ^= 1;
-      bad = __any_sync(0xffffffffu, bad);   // warp-uniform before warp-collective TMEM access
-      tc_fence_after();
-
-      // Softmax on this thread's row (TMEM lane).  Exponentials are taken
-      // against a per-row reference m_run (log2 units) and O accumulates in
-      // TMEM across chunks.  bf16: one pass, the reference being the row's
-      // first score on the first chunk and the running reference after, P
-      // written over S at once; a row whose chunk sum exceeds 2^32 flags a
-      // redo, and then the consumers recompute S and this chunk (exact max
-      // and O rescale for the flagged rows).  fp16 (narrower range for P):
-      // max pass first, rescale when the max grows by > 8.
-      const float l_before = l_run, m_before = m_run;
-      // Redo flag of this item: two words used alternately, set to j + 1,
-      // so a stale value from two items back never reads as set.
-      const uint32_t flag = base + OFF_BAR + 56 + (j & 1) * 4;
-      bool redo_row = false;
-      if (rows_here && !bad) {
-        if constexpr (BF) {
-          l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0);
-          redo_row = (tid < rows_q) && !(l_run - l_before <= 0x1p32f);
-          if (__any_sync(0xffffffffu, redo_row) && lane == 0) st_shared_u32(flag, j + 1u);
-        } else {
-          const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
-          if (c == 0) {
-            m_run = mx;
-          } else if (__any_sync(0xffffffffu, mx > m_run + 8.f)) {
-            const float m_new = fmaxf(m_run, mx);
-            const float alpha = fast_exp2(m_run - m_new);
-            l_run *= alpha;
-            rescale_o(tO_row, alpha);
-            m_run = m_new;
-          }
-          l_run += chunk_weights<false>(tS_row, nk16, n_c, full, c2, m_run, false);
-        }
-        tmem_st_wait();
-      }
-      tc_fence_before();
-      if (consumer_sync_or(bad)) { bad = true; break; }
-      if (BF && ld_shared_u32(flag) == j + 1u) {
-        // Rare: recompute S, then every warp rewrites its P; flagged warps
-        // switch to the exact max (rescaling O for later chunks).
-        if (tid == 0) {
-          tc_fence_after();
-          const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
-#pragma unroll
-          for (int kk = 0; kk < HD / 16; ++kk)
-            umma_f16(tS, sdesc(sQ + kk * 32, 16, 1024), sdesc(sK(st) + kk * 32, 16, 1024), idesc_s,
-                     kk > 0 ? 1u : 0u);
-          umma_commit(bar_mma);
-        }
-        bad |= !mbar_wait_or_abort(bar_mma, ph_mma, abort_flag);
-        if (!bad) ph_mma ^= 1;
-        bad = __any_sync(0xffffffffu, bad);
-        tc_fence_after();
-        if (rows_here && !bad) {
-          l_run = l_before;
-          m_run = m_before;
-          if (__any_sync(0xffffffffu, redo_row)) {
-            const float mx = chunk_max(tS_row, nk16, n_c, full, c2);
-            const float m_new = (c == 0) ? mx : fmaxf(m_before, mx);
-            if (c > 0) {
-              const float alpha = fast_exp2(m_before - m_new);
-              l_run *= alpha;
-              rescale_o(tO_row, alpha);
-            }
-            m_run = m_new;
-            l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, false);
-          } else {
-            l_run += chunk_weights<true>(tS_row, nk16, n_c, full, c2, m_run, c == 0);
-          }
-          tmem_st_wait();
-        }
-        tc_fence_before();
-        if (consumer_sync_or(bad)) { bad = true; break; }
-      }
-
-      // O += P_hi V + P_lo V in TMEM columns [64, 128) (fresh on a unit's
-      // first chunk).  Its completion frees this K/V stage for the producer
-      // and, on the unit's last chunk, the Q buffer.
-      if (tid == 0) {
-        tc_fence_after();
-        const int ksteps = nk16 / 16;
-        for (int kk = 0; kk < ksteps; ++kk)
-          umma_f16_tmem_a(tO, tS + kk * 16, sdesc(sV(st) + kk * 2048, KV_BYTES, 1024), idesc_pv,
-                          (kk > 0 || c > 0) ? 1u : 0u);
-        for (int kk = 0; kk < ksteps; ++kk)
-          umma_f16_tmem_a(tO, tS + kk * 16 + 8, sdesc(sV(st) + kk * 2048, KV_BYTES, 1024), idesc_pv, 1u);
-        umma_commit(bar_empty(st));
-        if (last) umma_commit(bar_qempty);
-        umma_commit(bar_mma);
-      }
-      bad |= !mbar_wait_or_abort(bar_mma, ph_mma, abort_flag);
-      if (!bad) ph_mma ^= 1;
-      bad = __any_sync(0xffffffffu, bad);
-      tc_fence_after();
-
-      if (last && rows_here && !bad) {
-        // Epilogue: this thread's row, normalised, to the packed or padded output.
-        float o_acc[HD];
-#pragma unroll
-        for (int g = 0; g < HD / 16; ++g) tmem_ld16(tO_row + g * 16, o_acc + g * 16);
+      if (c == 0) {
+        // Where this thread's row goes (element offset of its output row), or -1.
+        const int h = static_cast<int>(ld_shared_u32(d + 4));
+        const int s0 = static_cast<int>(ld_shared_u32(d + 8));
+        const int q0 = static_cast<int>(ld_shared_u32(d + 16));
         const int i = q0 + tid;
+        long long dst_row = -1;
         if (i < n) {
-          long long dst_row = static_cast<long long>(s0) + i;
-          bool ok = true;
+          dst_row = static_cast<long long>(s0) + i;
           if constexpr (FUSED) {
-            dst_row = static_cast<long long>(b) * a.N + ld_shared_u16(pos_addr(pslot) + 2 * i);
+            const int ib = static_cast<int>(ld_shared_u32(d + 32));
+            const int pslot = static_cast<int>(ld_shared_u32(d + 36));
+            dst_row = static_cast<long long>(ib) * a.N + ld_shared_u16(pos_addr(pslot) + 2 * i);
           } else if constexpr (SCATTER) {
             dst_row = __ldg(a.src_idx + dst_row);
             if (dst_row < 0 || dst_row >= static_cast<long long>(a.B) * a.N) {
               record_error(a.err, RRA_DEVERR_INDEX_RANGE);
-              ok = false;
+              dst_row = -1;
             }
           }
-          if (ok) {
-            Tout* out = static_cast<Tout*>(a.o) + (static_cast<size_t>(dst_row) * a.H + h) * HD;
-            store_row<Tout>(out, o_acc, 1.f / l_run);
-          }
         }
+        out_elem = dst_row < 0 ? -1 : (dst_row * a.H + h) * HD;
       }
+      tc_fence_after();
+
+      if (rows_here) {
+        const uint32_t tS_row = tmem + b * BN + lane_off;
+        float t[32];
+        if (nk16 > 16) {
+          tmem_ld32(tS_row, t);
+        } else {
+          tmem_ld16(tS_row, t);
+#pragma unroll
+          for (int i = 16; i < 32; ++i) t[i] = 0.f;
+        }
+        const float mx = (c2 > 0.f ? chunk_extreme<false>(t, n_c, full) : chunk_extreme<true>(t, n_c, full)) * c2;
+        if (c == 0) {
+          m_run = mx;
+          l_run = 0.f;
+        } else if (__any_sync(0xffffffffu, tid < rows_q && mx > m_run + 8.f)) {
+          // Move the reference: O holds the products up to item j-1; wait
+          // for the last of them before rescaling it.  Only rows of the
+          // tile vote (lanes past it see whatever the Q buffer held before),
+          // so the result does not depend on stale shared memory.
+          bad |= !mbar_wait_or_abort(bar_sfree((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag);
+          bad = __any_sync(0xffffffffu, bad);
+          if (bad) break;
+          tc_fence_after();
+          const float m_new = fmaxf(m_run, mx);
+          const float alpha = fast_exp2(m_run - m_new);
+          l_run *= alpha;
+          rescale_o(tO_row, alpha);
+          m_run = m_new;
+        }
+        l_run += write_weights<BF>(tS_row, t, nk16, c2, m_run);
+        tmem_st_wait();
+      }
+      tc_fence_before();
+      mbar_arrive(bar_pready(b));
+
       if (last) {
-        m_run = 0.f;
-        l_run = 0.f;
+        // Epilogue: this thread's row, normalised, to the packed or padded output.
+        bad |= !mbar_wait_or_abort(bar_ofull, uidx & 1, abort_flag);
+        bad = __any_sync(0xffffffffu, bad);
+        if (bad) break;
+        tc_fence_after();
+        if (rows_here) {
+          const float inv = 1.f / l_run;
+          Tout* out = static_cast<Tout*>(a.o) + (out_elem < 0 ? 0 : out_elem);
+#pragma unroll
+          for (int g = 0; g < HD / 16; ++g) {
+            float o[16];
+            tmem_ld16(tO_row + g * 16, o);
+            if (g == HD / 16 - 1) {
+              tc_fence_before();
+              mbar_arrive(bar_oempty);   // O is in registers: the next unit may overwrite it
+            }
+            if (out_elem >= 0) store16<Tout>(out + g * 16, o, inv);
+          }
+        } else {
+          tc_fence_before();
+          mbar_arrive(bar_oempty);
+        }
+        ++uidx;
       }
-      // No barrier here: the next S product overwrites S/P only after thread
-      // 0 has seen this P.V product complete, and the next unit's first P.V
-      // (which overwrites O) waits behind the next P-ready barrier.
     }
-    if (bad && tid == 0) {
-      st_shared_u32(abort_flag, 1u);
-      record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
-    }
+  }
+  if (bad && lane == 0) {
+    st_shared_u32(abort_flag, 1u);
+    record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
   }
 
-  // Teardown.  After an abort, copies or MMAs still in flight get a bounded
-  // grace period (~1 ms) to land before the TMEM is released and the CTA exits.
-  if (ld_shared_volatile_u32(abort_flag) != 0u && tid == 0) {
-    const long long t0 = clock64();
-    while (clock64() - t0 < 2000000LL) {
-    }
-  }
+  // Teardown.  After an abort, copies or products still in flight get a
+  // bounded grace period (~1 ms) to land before the TMEM is released and the
+  // CTA exits.
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
+    if (lane == 0 && ld_shared_volatile_u32(abort_flag) != 0u) {
+      const long long t0 = clock64();
+      while (clock64() - t0 < 2000000LL) {
+      }
+    }
+    __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
@@ -937,20 +1089,44 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
   // Largest dynamic shared memory any launch of this instantiation asks for
   // (position lists for N <= 1024 in the fused mode).
   constexpr uint32_t kMaxSmem = SMEM_ALLOC + (MODE == MODE_FUSED ? POS_SLOTS * 2048u : 0u);
+  auto kernel = attend_tc_kernel<Tin, Tout, SCATTER, MODE>;
   static bool attr_set[kMaxDev] = {};
+  static uint32_t occ_smem[kMaxDev] = {};
+  static int occ_blocks[kMaxDev] = {};
   static std::mutex m;
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
+  const int pos_stride = (MODE == MODE_FUSED) ? ((2 * a.N + 15) & ~15) : 0;
+  const uint32_t smem = SMEM_ALLOC + static_cast<uint32_t>(POS_SLOTS * pos_stride);
+  int per_sm = 0;
   {
     std::lock_guard<std::mutex> lock(m);
     if (!attr_set[dev]) {
-      e = cudaFuncSetAttribute(attend_tc_kernel<Tin, Tout, SCATTER, MODE>,
-                               cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxSmem));
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kMaxSmem));
+      if (e != cudaSuccess) return e;
+      // All of the SM's unified L1/shared array as shared memory: four CTAs
+      // of ~52 KB must be resident together.
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               static_cast<int>(cudaSharedmemCarveoutMaxShared));
       if (e != cudaSuccess) return e;
       attr_set[dev] = true;
     }
+    if (occ_smem[dev] != smem) {
+      // Resident CTAs per SM at this shared-memory size (4 unless the
+      // position lists of a long N push it lower); sizes the persistent grid.
+      int per_sm_smem = 0, reserved = 0;
+      e = cudaDeviceGetAttribute(&per_sm_smem, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev);
+      if (e != cudaSuccess) return e;
+      e = cudaDeviceGetAttribute(&reserved, cudaDevAttrReservedSharedMemoryPerBlock, dev);
+      if (e != cudaSuccess) return e;
+      const int nb = per_sm_smem / (static_cast<int>(smem) + reserved);
+      if (nb < 1) return cudaErrorInvalidConfiguration;
+      occ_blocks[dev] = nb < CTAS_PER_SM ? nb : CTAS_PER_SM;
+      occ_smem[dev] = smem;
+    }
+    per_sm = occ_blocks[dev];
   }
   const bool bf16 = IsBf16<Tin>::value == 1;
   CUtensorMap mq, mk, mv;
@@ -965,14 +1141,11 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
     if ((e = make_map(&mk, a.kp, a.H, rows, bf16)) != cudaSuccess) return e;
     if ((e = make_map(&mv, a.vp, a.H, rows, bf16)) != cudaSuccess) return e;
   }
-  const int pos_stride = (MODE == MODE_FUSED) ? ((2 * a.N + 15) & ~15) : 0;
-  const uint32_t smem = SMEM_ALLOC + static_cast<uint32_t>(POS_SLOTS * pos_stride);
   const int qtiles = (a.max_seqlen + BM - 1) / BM;
   const long long units = static_cast<long long>(a.B) * a.H * qtiles;
-  const long long cap = static_cast<long long>(CTAS_PER_SM) * (num_sms > 0 ? num_sms : 152);
+  const long long cap = static_cast<long long>(per_sm) * (num_sms > 0 ? num_sms : 152);
   const int grid = static_cast<int>(units < cap ? units : cap);
-  attend_tc_kernel<Tin, Tout, SCATTER, MODE><<<grid, THREADS, smem, stream>>>(mq, mk, mv, a, qtiles,
-                                                                             static_cast<int>(units), pos_stride);
+  kernel<<<grid, THREADS, smem, stream>>>(mq, mk, mv, a, static_cast<int>(units), pos_stride);
   return cudaGetLastError();
 }
 
