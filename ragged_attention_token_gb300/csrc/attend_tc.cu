@@ -9,39 +9,39 @@
 // Work unit = (image b, head h, tile of 128 query rows).  Persistent CTAs of
 // 192 threads walk the units with a grid stride; a unit whose tile starts
 // past the image's length is skipped.  Per unit, keys stream in chunks of
-// 32; an item is one (unit, key chunk).  Warp roles:
+// 64; an item is one (unit, key chunk).  Warp roles:
 //
 //   warp 4     loads: per item, TMA copies of the chunk's K and V rows into a
-//              4-stage ring (and, on a unit's first item, of the Q tile),
+//              2-stage ring (and, on a unit's first item, of the Q tile),
 //              128-byte swizzle.  In the fused pipeline this warp also scans
 //              the image's keep row (kept positions -> a shared list) and
 //              writes +0 to the output rows of pruned positions;
 //   warp 5     tensor-core products, issued by one elected lane of the
-//              converged warp: S = Q K^T (M=128,
-//              N=chunk rounded up to 16, K=64) into one of two 32-column TMEM
-//              buffers, and O += P_hi V + P_lo V (M=128, N=64, K=chunk), P
-//              read from TMEM, O accumulating in TMEM columns 64..127;
+//              converged warp: S = Q K^T (M=128, N=chunk rounded up to 16,
+//              K=64) into TMEM columns 0..63, and O += P_hi V + P_lo V (M=128,
+//              N=64, K=chunk) with P read from TMEM and O accumulating in
+//              TMEM columns 64..127.  The next S product is issued the moment
+//              this P.V product has finished reading P;
 //   warps 0-3  softmax, thread r owning query row r (TMEM lane r): the row's
 //              max over the chunk, exponentials in base 2 against a per-row
 //              reference, P written over S as two bf16/fp16 parts; after a
 //              unit's last item, the epilogue (normalise, store the row).
 //
-// With two S buffers the product S(j+1) runs while chunk j's softmax runs,
-// and P(j)V runs during chunk j+1's softmax.  Every hand-off between the
-// roles is an mbarrier; no warp waits at a CTA-wide barrier inside the loop.
-//
-// The reference max of a row only moves (rescaling O in TMEM, once the
-// previous P.V product has finished) when a chunk's max exceeds it by more
-// than 8 in the log2 domain, so every weight is at most 2^8.  P is split
-// because one bf16 rounding of the weights alone leaves up to ~2e-3 of
-// output error at these lengths; hi + lo carries ~16 bits.  Keys past the
-// image's end are masked (p = 0), and the V rows the product reads past the
-// end are either a repeated finite row (gathered loads) or zeroed in shared
-// memory (packed loads), so whatever the buffer holds there (even NaN) never
-// reaches a kept output.  Every mbarrier wait is bounded by a clock-cycle
-// limit and gives up early once another warp has raised the CTA's abort
-// flag; then the CTA records RRA_DEVERR_WAIT_TIMEOUT, waits (bounded) for
-// its own copies and products to land, frees its TMEM and returns.
+// The reference of a row is its max over the unit's first chunk; it moves
+// (rescaling O in TMEM, which is stable then: the previous P.V product has
+// finished before this S product was issued) only when a later chunk's max
+// exceeds it by more than 8 in the log2 domain, so every weight is at most
+// 2^8.  A one-token image's single weight is exactly 1, so such a row
+// returns V bit for bit.  P is split because one bf16 rounding of the weights alone
+// leaves up to ~2e-3 of output error at these lengths; hi + lo carries ~16
+// bits.  Keys past the image's end are masked (p = 0), and the V rows the
+// product reads past the end are either a repeated finite row (gathered
+// loads) or zeroed in shared memory (packed loads), so whatever the buffer
+// holds there (even NaN) never reaches a kept output.  Every mbarrier wait
+// is bounded by a clock-cycle limit and gives up early once another warp
+// has raised the CTA's abort flag; then the CTA records
+// RRA_DEVERR_WAIT_TIMEOUT, waits (bounded) for its own copies and products
+// to land, frees its TMEM and returns.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -53,7 +53,7 @@ namespace rra {
 namespace {
 
 constexpr int BM = 128;        // query rows per unit (= TMEM lanes)
-constexpr int BN = 32;         // keys per chunk (= columns of one S buffer)
+constexpr int BN = 64;         // keys per chunk (= columns of the S buffer)
 constexpr int HD = 64;         // head dim
 constexpr int CONSUMERS = 128;             // warps 0-3: softmax and epilogue
 constexpr int PRODUCER_WARP = 4;           // TMA loads (+ mask scan, zero fill)
@@ -61,45 +61,45 @@ constexpr int MMA_WARP = 5;                // tcgen05.mma issue
 constexpr int THREADS = CONSUMERS + 64;
 constexpr int BOX = 32;        // rows per TMA box (packed inputs)
 constexpr int CTAS_PER_SM = 4;
-constexpr int STAGES = 4;      // K/V chunk ring
+constexpr int STAGES = 2;      // K/V chunk ring
 
 constexpr uint32_t Q_BYTES = BM * 128;                 // 128 rows x 128 B
-constexpr uint32_t KV_BYTES = BN * 128;                //  32 rows x 128 B
+constexpr uint32_t KV_BYTES = BN * 128;                //  64 rows x 128 B
 constexpr uint32_t OFF_Q = 0;                          // one Q tile
 constexpr uint32_t OFF_K = OFF_Q + Q_BYTES;            // K[STAGES]
 constexpr uint32_t OFF_V = OFF_K + STAGES * KV_BYTES;  // V[STAGES]
 constexpr uint32_t OFF_BAR = OFF_V + STAGES * KV_BYTES;
 // mbarriers (8 B each) and words, as offsets from OFF_BAR.
 constexpr uint32_t B_FULL = 0;        // [STAGES] item loaded (TMA bytes + producer arrive)
-constexpr uint32_t B_EMPTY = 32;      // [STAGES] item's K/V consumed (its P.V product done)
-constexpr uint32_t B_QEMPTY = 64;     // unit's last S product done: Q buffer free
-constexpr uint32_t B_SFULL = 72;      // [2] S product in buffer done (or end of work)
-constexpr uint32_t B_SFREE = 88;      // [2] P.V product reading buffer done
-constexpr uint32_t B_PREADY = 104;    // [2] P written to buffer (128 consumer arrivals)
-constexpr uint32_t B_OFULL = 120;     // unit's last P.V product done
-constexpr uint32_t B_OEMPTY = 128;    // unit's O read out (128 consumer arrivals)
-constexpr uint32_t B_DRAIN = 136;     // every product issued has completed
-constexpr uint32_t W_TMEM = 144;      // TMEM base written by tcgen05.alloc
-constexpr uint32_t W_ABORT = 148;     // abort flag
+constexpr uint32_t B_EMPTY = 16;      // [STAGES] item's K/V consumed (its P.V product done)
+constexpr uint32_t B_QEMPTY = 32;     // unit's last S product done: Q buffer free
+constexpr uint32_t B_SFULL = 40;      // S product done
+constexpr uint32_t B_SFREE = 48;      // P.V product done (S/P buffer free)
+constexpr uint32_t B_PREADY = 56;     // P written (128 consumer arrivals)
+constexpr uint32_t B_OFULL = 64;      // unit's last P.V product done
+constexpr uint32_t B_OEMPTY = 72;     // unit's O read out (128 consumer arrivals)
+constexpr uint32_t B_DRAIN = 80;      // every product issued has completed
+constexpr uint32_t W_TMEM = 88;       // TMEM base written by tcgen05.alloc
+constexpr uint32_t W_ABORT = 92;      // abort flag
 // Item descriptors, one per stage, then (fused pipeline) POS_SLOTS lists of
 // kept positions (int16, N each).
 constexpr uint32_t DESC_BYTES = 48;
-constexpr uint32_t OFF_DESC = OFF_BAR + 160;
+constexpr uint32_t OFF_DESC = OFF_BAR + 112;
 constexpr uint32_t OFF_POS = OFF_DESC + STAGES * DESC_BYTES;
-// Five lists: the producer scans unit u + 5 only after the P.V product of
-// unit u + 1 has started, i.e. after every consumer has finished unit u's
-// epilogue (the last reader of its list).
+// Five lists: the producer scans unit u + 5 only after the last S product
+// of unit u + 3, which follows the P.V products of unit u + 2; by then every
+// consumer has finished unit u's epilogue (the last reader of its list).
 constexpr int POS_SLOTS = 5;
 constexpr uint32_t SMEM_ALLOC = OFF_POS + 1024;        // + position lists; slack to align the base to 1024 B
 
 enum { MODE_PACKED = 0, MODE_GATHER = 1, MODE_FUSED = 2 };
-constexpr uint32_t TMEM_COLS = 128;                    // S: cols [0,32) and [32,64); O: cols [64,128)
-constexpr uint32_t TMEM_O = 2 * BN;
+constexpr uint32_t TMEM_COLS = 128;                    // S/P: cols [0,64); O: cols [64,128)
+constexpr uint32_t TMEM_O = BN;
 constexpr uint32_t WAIT_SUSPEND_NS = 20000;            // try_wait suspend hint
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
 
 static_assert(OFF_POS % 16 == 0, "position lists must start 16-byte aligned");
-static_assert(OFF_DESC + STAGES * DESC_BYTES <= OFF_POS, "descriptor ring overlaps");
+static_assert(OFF_DESC >= OFF_BAR + W_ABORT + 4, "descriptor ring overlaps the flags");
 
 template <typename T> struct IsBf16;
 template <> struct IsBf16<__nv_bfloat16> { static constexpr uint32_t value = 1; };
@@ -436,17 +436,6 @@ __device__ Unit next_unit_fused(int u, int step, int units, int BH, const Attend
   return x;
 }
 
-// bf16 hi/lo split of two weights: hi = p truncated to bf16 (upper 16 bits,
-// exact), lo = p - hi (exact in fp32) rounded to bf16; hi + lo carries p to
-// 2^-16 relative.  Packed low half = first element (K order).
-__device__ __forceinline__ void split2_bf16_trunc(float p0, float p1, uint32_t& hi, uint32_t& lo) {
-  const uint32_t b0 = __float_as_uint(p0), b1 = __float_as_uint(p1);
-  hi = __byte_perm(b0, b1, 0x7632);
-  const float r0 = p0 - __uint_as_float(b0 & 0xFFFF0000u);
-  const float r1 = p1 - __uint_as_float(b1 & 0xFFFF0000u);
-  __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
-  lo = *reinterpret_cast<uint32_t*>(&l);
-}
 
 
 // 32 consecutive fp32 columns of this thread's TMEM lane (wait tied to the
@@ -487,31 +476,6 @@ __device__ __forceinline__ float min3f(float x, float y, float z) {
   return d;
 }
 
-// Largest (LOW: smallest) raw score over the chunk's valid columns.  Columns
-// at or past n_c are first replaced by -inf (LOW: +inf), so that with the
-// scale's sign they also give a weight of exactly 0 below.
-template <bool LOW>
-__device__ __forceinline__ float chunk_extreme(float (&t)[32], int n_c, bool full) {
-  const float pad = LOW ? INFINITY : -INFINITY;
-  if (!full) {
-#pragma unroll
-    for (int i = 0; i < 32; ++i) t[i] = (i < n_c) ? t[i] : pad;
-  }
-  float e[4];
-#pragma unroll
-  for (int k = 0; k < 4; ++k) {
-    const float* s = t + 8 * k;
-    if constexpr (LOW) {
-      e[k] = min3f(min3f(min3f(s[0], s[1], s[2]), s[3], s[4]), s[5], s[6]);
-      e[k] = fminf(e[k], s[7]);
-    } else {
-      e[k] = max3f(max3f(max3f(s[0], s[1], s[2]), s[3], s[4]), s[5], s[6]);
-      e[k] = fmaxf(e[k], s[7]);
-    }
-  }
-  return LOW ? fminf(min3f(e[0], e[1], e[2]), e[3]) : fmaxf(max3f(e[0], e[1], e[2]), e[3]);
-}
-
 // Packed pairs of fp32 (sm_100 and later execute fma/add/sub on both halves
 // of a 64-bit register pair in one instruction).
 __device__ __forceinline__ uint64_t pack_f2(float a, float b) {
@@ -538,25 +502,31 @@ __device__ __forceinline__ uint64_t sub_f2(uint64_t a, uint64_t b) {
   return d;
 }
 
-// Weights p = 2^(c2*s - mref) of one chunk row, written back over S in TMEM
-// as hi/lo pairs (each 16-column piece of S becomes 8 hi + 8 lo columns in
-// place); returns their sum.  Masked columns hold -inf*sign(c2) and give 0.
+// Weights of one 32-column group of a chunk row, p = 2^(c2*s - mref) (0 at
+// columns >= nvalid when !full), written back over S in TMEM as hi/lo pairs
+// (each 16-column piece of S becomes 8 hi + 8 lo columns in place); returns
+// their sum.  Only the first 16 columns when cols == 16.
 // bf16: hi = p truncated to bf16 (exact), lo = p - hi (exact in fp32)
 // rounded to bf16; fp16: hi = p rounded to fp16, lo = p - hi rounded.
 template <bool BF16>
-__device__ __forceinline__ float write_weights(uint32_t tS_row, const float (&t)[32], int nk16, float c2,
-                                              float mref) {
+__device__ __forceinline__ float weights32(uint32_t tS, const float (&t)[32], int cols, int nvalid, bool full,
+                                          float c2, float mref) {
   const uint64_t c2x2 = pack_f2(c2, c2), nm2 = pack_f2(-mref, -mref);
   uint64_t acc[2] = {0ull, 0ull};   // packed partial sums (+0.0f pairs)
 #pragma unroll
-  for (int g = 0; g < BN / 16; ++g) {
-    if (g == 0 || nk16 > 16) {
+  for (int g = 0; g < 2; ++g) {
+    if (g == 0 || cols > 16) {
       uint32_t hi[8], lo[8];
 #pragma unroll
       for (int i = 0; i < 8; ++i) {
+        const int col = 16 * g + 2 * i;
         float x0, x1;
-        unpack_f2(fma_f2(pack_f2(t[16 * g + 2 * i], t[16 * g + 2 * i + 1]), c2x2, nm2), x0, x1);
-        const float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+        unpack_f2(fma_f2(pack_f2(t[col], t[col + 1]), c2x2, nm2), x0, x1);
+        float p0 = fast_exp2(x0), p1 = fast_exp2(x1);
+        if (!full) {
+          p0 = (col < nvalid) ? p0 : 0.f;
+          p1 = (col + 1 < nvalid) ? p1 : 0.f;
+        }
         const uint64_t pp = pack_f2(p0, p1);
         acc[i & 1] = add_f2(acc[i & 1], pp);
         float r0, r1;
@@ -575,14 +545,44 @@ __device__ __forceinline__ float write_weights(uint32_t tS_row, const float (&t)
           lo[i] = *reinterpret_cast<const uint32_t*>(&l);
         }
       }
-      tmem_st8(tS_row + g * 16, hi);
-      tmem_st8(tS_row + g * 16 + 8, lo);
+      tmem_st8(tS + g * 16, hi);
+      tmem_st8(tS + g * 16 + 8, lo);
     }
   }
   float s0, s1, s2, s3;
   unpack_f2(acc[0], s0, s1);
   unpack_f2(acc[1], s2, s3);
   return (s0 + s1) + (s2 + s3);
+}
+
+// Largest (LOW: smallest) raw score over the first nvalid columns of a
+// 32-column group; the others are first replaced by -inf (LOW: +inf).
+template <bool LOW>
+__device__ __forceinline__ float group_extreme(float (&t)[32], int nvalid) {
+  const float pad = LOW ? INFINITY : -INFINITY;
+  if (nvalid < 32) {
+#pragma unroll
+    for (int i = 0; i < 32; ++i) t[i] = (i < nvalid) ? t[i] : pad;
+  }
+  float e[4];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    const float* s = t + 8 * k;
+    if constexpr (LOW) e[k] = fminf(min3f(min3f(min3f(s[0], s[1], s[2]), s[3], s[4]), s[5], s[6]), s[7]);
+    else e[k] = fmaxf(max3f(max3f(max3f(s[0], s[1], s[2]), s[3], s[4]), s[5], s[6]), s[7]);
+  }
+  return LOW ? fminf(min3f(e[0], e[1], e[2]), e[3]) : fmaxf(max3f(e[0], e[1], e[2]), e[3]);
+}
+
+// 32 (or 16, the rest set to 0) columns of this thread's S row.
+__device__ __forceinline__ void load_group(uint32_t taddr, int cols, float (&t)[32]) {
+  if (cols > 16) {
+    tmem_ld32(taddr, t);
+  } else {
+    tmem_ld16(taddr, t);
+#pragma unroll
+    for (int i = 16; i < 32; ++i) t[i] = 0.f;
+  }
 }
 
 // O row (TMEM) *= alpha.
@@ -631,6 +631,7 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
   asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
 }
 
+
 template <typename Tin, typename Tout, bool SCATTER, int MODE>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -648,10 +649,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   const uint32_t bars = base + OFF_BAR;
   auto bar_full = [&](int i) { return bars + B_FULL + 8 * i; };
   auto bar_empty = [&](int i) { return bars + B_EMPTY + 8 * i; };
-  auto bar_sfull = [&](int i) { return bars + B_SFULL + 8 * i; };
-  auto bar_sfree = [&](int i) { return bars + B_SFREE + 8 * i; };
-  auto bar_pready = [&](int i) { return bars + B_PREADY + 8 * i; };
-  const uint32_t bar_qempty = bars + B_QEMPTY, bar_ofull = bars + B_OFULL, bar_oempty = bars + B_OEMPTY;
+  const uint32_t bar_qempty = bars + B_QEMPTY, bar_sfull = bars + B_SFULL, bar_sfree = bars + B_SFREE;
+  const uint32_t bar_pready = bars + B_PREADY, bar_ofull = bars + B_OFULL, bar_oempty = bars + B_OEMPTY;
   const uint32_t bar_drain = bars + B_DRAIN, abort_flag = bars + W_ABORT;
   auto desc_addr = [&](int i) { return base + OFF_DESC + i * DESC_BYTES; };
   auto pos_addr = [&](int s) { return base + OFF_POS + s * pos_stride; };
@@ -668,11 +667,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       mbar_init(bar_empty(i), 1);
     }
     mbar_init(bar_qempty, 1);
-    for (int i = 0; i < 2; ++i) {
-      mbar_init(bar_sfull(i), 1);
-      mbar_init(bar_sfree(i), 1);
-      mbar_init(bar_pready(i), CONSUMERS);
-    }
+    mbar_init(bar_sfull, 1);
+    mbar_init(bar_sfree, 1);
+    mbar_init(bar_pready, CONSUMERS);
     mbar_init(bar_ofull, 1);
     mbar_init(bar_oempty, CONSUMERS);
     mbar_init(bar_drain, 1);
@@ -737,7 +734,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           st_shared_u32(d + 36, static_cast<uint32_t>(uidx % POS_SLOTS));
         }
         if constexpr (GATHER) {
-          // K and V: lanes 0-7 and 16-23, one 4-row gather each; Q: up to 32 lanes.
+          // K: lanes 0-15, V: lanes 16-31, one 4-row gather each; Q: up to 32 lanes.
           const int kgroups = ((n_c + 15) & ~15) / 4;
           const int qgroups = (c == 0) ? (U.rows_q + 3) / 4 : 0;
           if (lane == 0) mbar_expect_tx(bar_full(st), static_cast<uint32_t>((2 * kgroups + qgroups) * 512));
@@ -766,13 +763,16 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
             else tma_gather4(sV(st) + g * 512, &tmap_v, rows, bar_full(st));
           }
         } else if (lane == 0) {
-          // One 32-row box each for K and V; Q in up to four boxes.
+          // 32-row boxes: up to two each for K and V, four for Q.
+          const int kboxes = (n_c + BOX - 1) / BOX;
           const int qboxes = (c == 0) ? (U.rows_q + BOX - 1) / BOX : 0;
-          mbar_expect_tx(bar_full(st), static_cast<uint32_t>((2 + qboxes) * BOX * 128));
+          mbar_expect_tx(bar_full(st), static_cast<uint32_t>((2 * kboxes + qboxes) * BOX * 128));
           for (int jj = 0; jj < qboxes; ++jj)
             tma_load_3d(sQ + jj * BOX * 128, &tmap_q, 0, U.h, U.s0 + U.q0 + jj * BOX, bar_full(st));
-          tma_load_3d(sK(st), &tmap_k, 0, U.h, U.s0 + k0, bar_full(st));
-          tma_load_3d(sV(st), &tmap_v, 0, U.h, U.s0 + k0, bar_full(st));
+          for (int jj = 0; jj < kboxes; ++jj) {
+            tma_load_3d(sK(st) + jj * BOX * 128, &tmap_k, 0, U.h, U.s0 + k0 + jj * BOX, bar_full(st));
+            tma_load_3d(sV(st) + jj * BOX * 128, &tmap_v, 0, U.h, U.s0 + k0 + jj * BOX, bar_full(st));
+          }
         }
         __syncwarp();
         if constexpr (FUSED) {
@@ -799,37 +799,41 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     }
   } else if (warp == MMA_WARP) {
     // ------------------------------------------------------------ products
-    // Order: S(0); then for each item jp: S(jp+1) (needs its loads and the
-    // P.V product of item jp-1, which read the same S buffer), then, once the
-    // consumers have written P(jp), O += P(jp) V (a unit's first one waits
-    // until the consumers have read out the previous unit's O).
+    // Per item j: S(j) (once its loads have landed; P.V(j-1) has finished
+    // with the S/P columns, see the end of the loop); then, once the
+    // consumers have written P(j), O += P(j) V (a unit's first one also
+    // waits until the consumers have read out the previous unit's O); then
+    // the wait for that product before S(j+1).  A unit's last S product
+    // frees the Q buffer for the next unit's loads.
+    const uint32_t tS = tmem, tO = tmem + TMEM_O;
     const uint32_t idesc_pv = idesc_f16(BF ? 1u : 0u, 1, BM, HD);
-    uint32_t k = 0, jp = 0, ustarted = 0;
-    int info0 = 0, info1 = 0;   // per S buffer: nk16 | first << 8 | last << 9
-    bool end = false;
-    auto issue_s = [&]() {
-      const int st = static_cast<int>(k % STAGES);
-      bad |= !mbar_wait_or_abort(bar_full(st), (k / STAGES) & 1, abort_flag);
+    uint32_t j = 0, ph_pready = 0, ph_sfree = 0, ustarted = 0;
+    int nk16 = 0, c = 0, nch = 0;
+    auto issue_s = [&](int st) {
+      tc_fence_after();
+      const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
+      const bool leader = elect_one();
+#pragma unroll
+      for (int kk = 0; kk < HD / 16; ++kk) {
+        const uint64_t da = sdesc(sQ + kk * 32, 16, 1024), db = sdesc(sK(st) + kk * 32, 16, 1024);
+        if (leader) umma_f16(tS, da, db, idesc_s, kk > 0 ? 1u : 0u);
+      }
+      if (leader) umma_commit(bar_sfull);
+    };
+    for (;; ++j) {
+      // S(j): loads, descriptor, then the product.
+      const int st = static_cast<int>(j % STAGES);
+      bad |= !mbar_wait_or_abort(bar_full(st), (j / STAGES) & 1, abort_flag);
       bad = __any_sync(0xffffffffu, bad);
-      if (bad) return;
+      if (bad) break;
       const uint32_t d = desc_addr(st);
-      if (static_cast<int>(ld_shared_u32(d + 0)) >= units) {
-        // End of work: the consumers learn it from this buffer's S barrier.
-        end = true;
-        if (elect_one()) umma_commit(bar_sfull(k & 1));
-        return;
-      }
+      if (static_cast<int>(ld_shared_u32(d + 0)) >= units) break;   // sentinel
       const int n = static_cast<int>(ld_shared_u32(d + 12));
-      const int nch = static_cast<int>(ld_shared_u32(d + 24));
-      const int c = static_cast<int>(ld_shared_u32(d + 28));
+      nch = static_cast<int>(ld_shared_u32(d + 24));
+      c = static_cast<int>(ld_shared_u32(d + 28));
       const int n_c = min(BN, n - c * BN);
-      const int nk16 = (n_c + 15) & ~15;
-      const bool last = c == nch - 1;
-      if (k >= 2) {
-        bad |= !mbar_wait_or_abort(bar_sfree(k & 1), ((k - 2) >> 1) & 1, abort_flag);
-        bad = __any_sync(0xffffffffu, bad);
-        if (bad) return;
-      }
+      nk16 = (n_c + 15) & ~15;
+      const bool first = c == 0, last = c == nch - 1;
       if constexpr (!GATHER) {
         // Packed boxes: V rows [n_c, nk16) enter the P.V product with p = 0;
         // make them finite zeros (the gathered path repeats a valid row).
@@ -839,43 +843,22 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         fence_proxy_async();
         __syncwarp();
       }
-      tc_fence_after();
-      {
-        const uint32_t idesc_s = idesc_f16(BF ? 1u : 0u, 0, BM, nk16);
-        const uint32_t tS = tmem + (k & 1) * BN;
-        const bool leader = elect_one();
-#pragma unroll
-        for (int kk = 0; kk < HD / 16; ++kk) {
-          const uint64_t da = sdesc(sQ + kk * 32, 16, 1024), db = sdesc(sK(st) + kk * 32, 16, 1024);
-          if (leader) umma_f16(tS, da, db, idesc_s, kk > 0 ? 1u : 0u);
-        }
-        if (leader) umma_commit(bar_sfull(k & 1));
-        if (leader && last) umma_commit(bar_qempty);
-      }
-      const int inf = nk16 | (c == 0 ? 256 : 0) | (last ? 512 : 0);
-      if (k & 1) info1 = inf;
-      else info0 = inf;
-      ++k;
-    };
-    issue_s();
-    while (!bad && jp < k) {
-      if (!end) {
-        issue_s();
-        if (bad) break;
-      }
-      const int b = static_cast<int>(jp & 1);
-      const int inf = b ? info1 : info0;
-      const bool first = (inf & 256) != 0, last = (inf & 512) != 0;
-      const int nk16 = inf & 255;
-      bad |= !mbar_wait_or_abort(bar_pready(b), (jp >> 1) & 1, abort_flag);
-      if (first && ustarted >= 1) bad |= !mbar_wait_or_abort(bar_oempty, (ustarted - 1) & 1, abort_flag);
+      issue_s(st);
+      if (last && elect_one()) umma_commit(bar_qempty);
+
+      // P(j) written, then the P.V product.
+      bad |= !mbar_wait_or_abort(bar_pready, ph_pready, abort_flag);
+      ph_pready ^= 1;
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
+      if (first && ustarted >= 1) {
+        bad |= !mbar_wait_or_abort(bar_oempty, (ustarted - 1) & 1, abort_flag);
+        bad = __any_sync(0xffffffffu, bad);
+        if (bad) break;
+      }
       if (first) ++ustarted;
       tc_fence_after();
       {
-        const int st = static_cast<int>(jp % STAGES);
-        const uint32_t tS = tmem + b * BN, tO = tmem + TMEM_O;
         const bool leader = elect_one();
 #pragma unroll
         for (int kk = 0; kk < BN / 16; ++kk) {
@@ -892,10 +875,13 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           }
         }
         if (leader) umma_commit(bar_empty(st));
-        if (leader) umma_commit(bar_sfree(b));
         if (leader && last) umma_commit(bar_ofull);
+        if (leader) umma_commit(bar_sfree);
       }
-      ++jp;
+      bad |= !mbar_wait_or_abort(bar_sfree, ph_sfree, abort_flag);
+      ph_sfree ^= 1;
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad) break;
     }
     if (!bad) {
       // Every product issued has completed (and with it the arrivals above).
@@ -906,16 +892,13 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   } else {
     // ------------------------------------------------------------ softmax
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t tO_row = tmem + TMEM_O + lane_off;
-    // A zero scale would make the masked -inf columns NaN; 1e-30 gives the
-    // same weights (all exactly 1) with the masking intact.
-    const float c2 = (a.scale_log2 == 0.f) ? 1e-30f : a.scale_log2;
-    uint32_t uidx = 0;
-    float m_run = 0.f, l_run = 0.f;   // this row's reference max (log2 units) and weight sum
+    const uint32_t tS_row = tmem + lane_off, tO_row = tmem + TMEM_O + lane_off;
+    const float c2 = a.scale_log2;
+    uint32_t uidx = 0, ph_sfull = 0;
+    float m_run = 0.f, l_run = 0.f;   // this row's reference (log2 units) and weight sum
     long long out_elem = -1;          // this row's output offset in the current unit
     for (uint32_t j = 0;; ++j) {
-      const int b = static_cast<int>(j & 1), st = static_cast<int>(j % STAGES);
-      bad |= !mbar_wait_or_abort(bar_sfull(b), (j >> 1) & 1, abort_flag);
+      const int st = static_cast<int>(j % STAGES);
       bad |= !mbar_wait_or_abort(bar_full(st), (j / STAGES) & 1, abort_flag);
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
@@ -927,7 +910,6 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       const int c = static_cast<int>(ld_shared_u32(d + 28));
       const int n_c = min(BN, n - c * BN);
       const int nk16 = (n_c + 15) & ~15;
-      const bool full = (n_c == BN);
       const bool rows_here = warp * 32 < rows_q;   // warp-uniform
       const bool last = (c == nchunks - 1);
       if (c == 0) {
@@ -953,42 +935,51 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         }
         out_elem = dst_row < 0 ? -1 : (dst_row * a.H + h) * HD;
       }
+      bad |= !mbar_wait_or_abort(bar_sfull, ph_sfull, abort_flag);
+      ph_sfull ^= 1;
+      bad = __any_sync(0xffffffffu, bad);
+      if (bad) break;
       tc_fence_after();
 
+      // Exact row max over the chunk (two passes over S: max, then the
+      // weights; the second half stays in registers).  The reference moves
+      // only when the max exceeds it by more than 8, rescaling O, which
+      // holds the finished products up to item j-1.
       if (rows_here) {
-        const uint32_t tS_row = tmem + b * BN + lane_off;
+        const int cols_a = min(32, nk16), cols_b = nk16 - 32;
+        const int va = min(32, n_c), vb = n_c - 32;
         float t[32];
-        if (nk16 > 16) {
-          tmem_ld32(tS_row, t);
-        } else {
-          tmem_ld16(tS_row, t);
-#pragma unroll
-          for (int i = 16; i < 32; ++i) t[i] = 0.f;
+        load_group(tS_row, cols_a, t);
+        float e = c2 >= 0.f ? group_extreme<false>(t, va) : group_extreme<true>(t, va);
+        if (cols_b > 0) {
+          load_group(tS_row + 32, cols_b, t);
+          const float eb = c2 >= 0.f ? group_extreme<false>(t, vb) : group_extreme<true>(t, vb);
+          e = c2 >= 0.f ? fmaxf(e, eb) : fminf(e, eb);
         }
-        const float mx = (c2 > 0.f ? chunk_extreme<false>(t, n_c, full) : chunk_extreme<true>(t, n_c, full)) * c2;
+        const float mx = e * c2;
         if (c == 0) {
           m_run = mx;
           l_run = 0.f;
-        } else if (__any_sync(0xffffffffu, tid < rows_q && mx > m_run + 8.f)) {
-          // Move the reference: O holds the products up to item j-1; wait
-          // for the last of them before rescaling it.  Only rows of the
-          // tile vote (lanes past it see whatever the Q buffer held before),
-          // so the result does not depend on stale shared memory.
-          bad |= !mbar_wait_or_abort(bar_sfree((j - 1) & 1), ((j - 1) >> 1) & 1, abort_flag);
-          bad = __any_sync(0xffffffffu, bad);
-          if (bad) break;
-          tc_fence_after();
+        }
+        // Only rows of the tile vote (lanes past it see whatever the Q
+        // buffer held before), so the result does not depend on stale data.
+        if (c > 0 && __any_sync(0xffffffffu, tid < rows_q && mx > m_run + 8.f)) {
           const float m_new = fmaxf(m_run, mx);
           const float alpha = fast_exp2(m_run - m_new);
           l_run *= alpha;
           rescale_o(tO_row, alpha);
           m_run = m_new;
+          load_group(tS_row + (cols_b > 0 ? 32 : 0), cols_b > 0 ? cols_b : cols_a, t);   // not kept across the rescale
         }
-        l_run += write_weights<BF>(tS_row, t, nk16, c2, m_run);
+        if (cols_b > 0) {
+          l_run += weights32<BF>(tS_row + 32, t, cols_b, vb, vb >= 32, c2, m_run);
+          load_group(tS_row, cols_a, t);
+        }
+        l_run += weights32<BF>(tS_row, t, cols_a, va, va >= 32, c2, m_run);
         tmem_st_wait();
       }
       tc_fence_before();
-      mbar_arrive(bar_pready(b));
+      mbar_arrive(bar_pready);
 
       if (last) {
         // Epilogue: this thread's row, normalised, to the packed or padded output.
