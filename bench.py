@@ -24,6 +24,7 @@ the work partitions with no collective); rank 0 prints the aggregate.
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -242,6 +243,24 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
     finally:
         rra.set_attend_kernel(prev)
     return res
+
+
+# DRAM bytes (read + write) per launch of the fused attend_tc_kernel, each from one ncu
+# capture of the same launches (dram__bytes_read.sum + dram__bytes_write.sum).  They
+# describe the kernel source whose SHA-256 starts with TRAFFIC_SRC_SHA; once that file
+# changes the traffic is reported as null until it is captured again.
+TRAFFIC_SRC_SHA = "fa438a5c637c92cc"
+TRAFFIC_BYTES = {"serving_B4": 430592, "batched_b64_p80": 11922176}
+
+
+def measured_traffic(key):
+    src = os.path.join(ROOT, "ragged_attention_token_gb300", "csrc", "attend_tc.cu")
+    try:
+        with open(src, "rb") as f:
+            ok = hashlib.sha256(f.read()).hexdigest().startswith(TRAFFIC_SRC_SHA)
+    except OSError:
+        ok = False
+    return TRAFFIC_BYTES.get(key) if ok else None
 
 
 def roofline_obj(bytes_alg, flops, us, peaks):
@@ -488,6 +507,7 @@ def run_rra(args, world, rank, local):
     if fused:
         kern = {"fused_us": round(kt["fused_us"], 3)}
         roof = roofline_obj(by["fused_min"], by["flops"], kt["fused_us"], peaks)
+        roof["traffic"] = measured_traffic(case.name)
         roof["kernel"] = "attend_tc_kernel (fused pipeline: mask scan, gather, attention, zero fill)"
     else:
         kern = {"pack_copy_us": round(kt["pack_copy_us"], 3), "attend_packed_us": round(kt["attend_packed_us"], 3),
@@ -508,7 +528,8 @@ def run_rra(args, world, rank, local):
         bk = kernel_times(big, big_sets, rra, stream)
         bb = case_bytes(big)
         extra["batched_b64_p80"] = {"workload": big_desc, "fused_us": round(bk["fused_us"], 3),
-                                    "roofline": roofline_obj(bb["fused_min"], bb["flops"], bk["fused_us"], peaks),
+                                    "roofline": {**roofline_obj(bb["fused_min"], bb["flops"], bk["fused_us"], peaks),
+                                                 "traffic": measured_traffic("batched_b64_p80")},
                                     "pipeline_tokens_per_s": round(big.kept_tokens / (bk["fused_us"] * 1e-6), 1)}
         del big_sets
 
@@ -530,7 +551,7 @@ def run_rra(args, world, rank, local):
                              f"({sets.R * sets.per_set / 2**20:.0f} MiB > L2)",
                        "parallelism": f"replicas x{world}"},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "path": "rra_pipeline_host (pinned H2D, pack, attend, D2H)"},
+                    "path": "rra_pipeline_host (pinned H2D, the pipeline kernel, D2H)"},
             "roofline": roof,
             "kernels": kern,
             "attend_kernel": args.attend_kernel,
@@ -540,7 +561,8 @@ def run_rra(args, world, rank, local):
             "launches_per_step": launches_per_step,
             "per_call_dispatch": {"value": round(per_call_value, 1), "unit": UNIT,
                                   "ms_per_step": round(per_call_ms / args.steps, 5),
-                                  "path": "one rra_plan_launch (graph of 2 kernels) per step from Python"},
+                                  "path": f"one rra_plan_launch (a graph of {launches_per_step} kernel launch"
+                                          f"{'es' if launches_per_step != 1 else ''}) per step from Python"},
         }
         line.update(extra)
         print(json.dumps(line), flush=True)
