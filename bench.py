@@ -249,8 +249,8 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
 # capture of the same launches (dram__bytes_read.sum + dram__bytes_write.sum).  They
 # describe the kernel source whose SHA-256 starts with TRAFFIC_SRC_SHA; once that file
 # changes the traffic is reported as null until it is captured again.
-TRAFFIC_SRC_SHA = "fa438a5c637c92cc"
-TRAFFIC_BYTES = {"serving_B4": 430592, "batched_b64_p80": 11922176}
+TRAFFIC_SRC_SHA = "975bf4075eaee147"
+TRAFFIC_BYTES = {"serving_B4": 430879, "batched_b64_p80": 11918336}
 
 
 def measured_traffic(key):
