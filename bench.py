@@ -12,7 +12,8 @@ and every step reads cold inputs.
 
 Printed (rank 0, one JSON line): kept tokens/s of the path (value), the
 host-timed latency of one rra_attend call at BS=1/2/4, end-to-end tokens/s
-from pinned host buffers through rra_pipeline_host, the dominant kernel's
+from pinned host buffers (through rra_pipeline_mapped, which reads the kept
+rows over the CPU-GPU link, and through rra_pipeline_host's copies), the dominant kernel's
 roofline fraction, the CPU oracle's throughput on a bounded sample, SM clocks
 sampled during the run and the number of kernel launches.
 
@@ -478,26 +479,43 @@ def run_rra(args, world, rank, local):
     per_call_ms = max_over_ranks(e4.elapsed_time(e5), world, device)
     per_call_value = T * args.steps * world / (per_call_ms * 1e-3)
 
-    # e2e: pinned host inputs -> device -> path -> host output, every step
-    keep_h, q_h, k_h, v_h = (x.pin_memory() for x in (case.keep, case.q, case.k, case.v))
+    # e2e: pinned host inputs -> GPU -> path -> pinned host output, every step.
+    # Headline: rra_pipeline_mapped, whose kernels read the mask and the kept
+    # rows over the CPU-GPU link and write the output into host memory.
+    # Beside it: rra_pipeline_host (copy engines move the whole padded
+    # tensors in, the output back).
+    keep_h, q_h, k_h, v_h = (x.contiguous().pin_memory() for x in (case.keep, case.q, case.k, case.v))
     out_h = torch.empty((B, N, H, d), dtype=case.dtype).pin_memory()
     keep_d, q_d, k_d, v_d, out_d, ws_d = sets.sets[0]
-    h2d = sum(x.numel() * x.element_size() for x in (keep_h, q_h, k_h, v_h))
+    elem = case.q.element_size()
     d2h = out_h.numel() * out_h.element_size()
-    with torch.cuda.stream(stream):
-        for _ in range(max(3, args.warmup)):
-            rra.pipeline_host(keep_h, q_h, k_h, v_h, out_h, keep_d, q_d, k_d, v_d, out_d, ws_d, SCALE, stream)
-        stream.synchronize()
-        barrier(world)
-        e2 = torch.cuda.Event(enable_timing=True)
-        e3 = torch.cuda.Event(enable_timing=True)
-        e2.record(stream)
-        for _ in range(args.steps):
-            rra.pipeline_host(keep_h, q_h, k_h, v_h, out_h, keep_d, q_d, k_d, v_d, out_d, ws_d, SCALE, stream)
-        e3.record(stream)
-        e3.synchronize()
-    e2e_ms = max_over_ranks(e2.elapsed_time(e3), world, device)
+
+    def e2e_time(step):
+        with torch.cuda.stream(stream):
+            for _ in range(max(3, args.warmup)):
+                step()
+            stream.synchronize()
+            barrier(world)
+            ea = torch.cuda.Event(enable_timing=True)
+            eb = torch.cuda.Event(enable_timing=True)
+            ea.record(stream)
+            for _ in range(args.steps):
+                step()
+            eb.record(stream)
+            eb.synchronize()
+        return max_over_ranks(ea.elapsed_time(eb), world, device)
+
+    e2e_ms = e2e_time(lambda: rra.pipeline_mapped(keep_h, q_h, k_h, v_h, out_h, ws_d, SCALE, stream))
     e2e_value = T * args.steps * world / (e2e_ms * 1e-3)
+    h2d = keep_h.numel() + 3 * T * H * d * elem            # the mask and the kept rows cross the link
+    copy_ms = e2e_time(lambda: rra.pipeline_host(keep_h, q_h, k_h, v_h, out_h, keep_d, q_d, k_d, v_d, out_d, ws_d,
+                                                 SCALE, stream))
+    e2e_copy = {"value": round(T * args.steps * world / (copy_ms * 1e-3), 1), "unit": UNIT,
+                "ms_per_step": round(copy_ms / args.steps, 5),
+                "h2d_bytes_per_step": sum(x.numel() * x.element_size() for x in (keep_h, q_h, k_h, v_h)),
+                "d2h_bytes_per_step": d2h,
+                "path": "rra_pipeline_host (cudaMemcpyAsync of the padded keep/q/k/v in, the fused kernel, the "
+                        "output out)"}
 
     # per-kernel device time (graph of back-to-back launches on cold inputs)
     n_sms = torch.cuda.get_device_properties(device).multi_processor_count
@@ -551,7 +569,10 @@ def run_rra(args, world, rank, local):
                              f"({sets.R * sets.per_set / 2**20:.0f} MiB > L2)",
                        "parallelism": f"replicas x{world}"},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
-                    "path": "rra_pipeline_host (pinned H2D, the pipeline kernel, D2H)"},
+                    "ms_per_step": round(e2e_ms / args.steps, 5),
+                    "path": "rra_pipeline_mapped (inputs and output in pinned host memory; pack + attend read the "
+                            "mask and the kept rows over the CPU-GPU link and write the output into host memory)"},
+            "e2e_copy": e2e_copy,
             "roofline": roof,
             "kernels": kern,
             "attend_kernel": args.attend_kernel,

@@ -168,6 +168,26 @@ RRA_API rra_status rra_pipeline_host(const uint8_t* keep_h, const void* q_h, con
                                      uint8_t* keep_d, void* q_d, void* k_d, void* v_d, void* out_d,
                                      void* workspace, size_t workspace_bytes, void* stream);
 
+/* The pipeline with inputs and output left in page-locked HOST memory and
+ * no copies: the kernels read keep_h and the KEPT rows of q_h/k_h/v_h
+ * straight from host memory over the CPU-GPU link, and write every row of
+ * out_h (attention at kept positions, +0 at pruned ones) straight into host
+ * memory.  Pruned input rows never cross the link, so the link carries
+ * B*N + 3*T*H*d*size(in) bytes in and B*N*H*d*size(out) bytes out, T the
+ * number of kept tokens.  Runs as rra_pack (with the row copy) then
+ * rra_attend on the packed buffers in `workspace`, two launches, whatever
+ * kernel rra_set_attend_kernel selected (the packed kernels touch host memory
+ * with plain loads and stores only).  Host buffers: allocated by
+ * cudaHostAlloc / cudaMallocHost or registered with cudaHostRegister, and
+ * device-accessible (else RRA_ERR_INVALID_ARG, nothing enqueued); pageable
+ * memory is refused.  `workspace`: DEVICE memory of rra_workspace_bytes()
+ * bytes (else RRA_ERR_INVALID_ARG).  Asynchronous on `stream`: out_h is
+ * complete once the stream has been synchronised. */
+RRA_API rra_status rra_pipeline_mapped(const uint8_t* keep_h, const void* q_h, const void* k_h,
+                                       const void* v_h, int B, int N, int H, int d, float scale,
+                                       rra_dtype in_dtype, void* out_h, rra_dtype out_dtype,
+                                       void* workspace, size_t workspace_bytes, void* stream);
+
 /* Size of the scratch array rra_pipeline_static uses on each GPU (64 MiB). */
 #define RRA_STATIC_SCRATCH_BYTES (64u * 1024u * 1024u)
 

@@ -212,13 +212,25 @@ bool pipeline_fused() { return g_attend_kernel.load() != RRA_ATTEND_MMA_SYNC; }
 // Kernel launches one rra_pipeline call makes: 1 fused, 2 packed.
 int pipeline_launches(const DeviceState&, const PipelineArgs&) { return pipeline_fused() ? 1 : 2; }
 
-rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaStream_t s) {
+// The two-launch form: rra_pack (with the row copy, and the zero fill of the
+// pruned output rows) into the workspace, then rra_attend on the packed
+// buffers scattering to the padded output.
+rra_status enqueue_packed_pipeline(const DeviceState& st, const PipelineArgs& p, cudaStream_t s) {
   size_t off[6], total = 0;
   workspace_layout(p.B, p.N, p.H, p.d, p.in, off, &total);
   uint8_t* ws = static_cast<uint8_t*>(p.ws);
   int32_t* cu = reinterpret_cast<int32_t*>(ws + off[0]);
   int32_t* dst = reinterpret_cast<int32_t*>(ws + off[1]);
   int32_t* src = reinterpret_cast<int32_t*>(ws + off[2]);
+  void* qp = ws + off[3];
+  void* kp = ws + off[4];
+  void* vp = ws + off[5];
+  RRA_TRY(enqueue_pack(st, p.keep, p.B, p.N, p.H, p.d, p.in, p.q, p.k, p.v, cu, dst, src, qp, kp, vp,
+                       p.out, p.out_dt, s));
+  return enqueue_attend(st, qp, kp, vp, cu, p.B, p.N, p.H, p.scale, p.in, p.out, p.out_dt, src, p.N, s);
+}
+
+rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaStream_t s) {
   if (pipeline_fused()) {
     // One launch: the attention kernel scans the keep mask per image,
     // gathers the kept rows straight from q/k/v and writes every output row.
@@ -240,12 +252,28 @@ rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaSt
     if (e != cudaSuccess) return cuda_fail(e, "fused pipeline launch");
     return RRA_OK;
   }
-  void* qp = ws + off[3];
-  void* kp = ws + off[4];
-  void* vp = ws + off[5];
-  RRA_TRY(enqueue_pack(st, p.keep, p.B, p.N, p.H, p.d, p.in, p.q, p.k, p.v, cu, dst, src, qp, kp, vp,
-                       p.out, p.out_dt, s));
-  return enqueue_attend(st, qp, kp, vp, cu, p.B, p.N, p.H, p.scale, p.in, p.out, p.out_dt, src, p.N, s);
+  return enqueue_packed_pipeline(st, p, s);
+}
+
+// The address through which the current device reaches page-locked host
+// memory at p (cudaHostAlloc / cudaMallocHost / cudaHostRegister), or null
+// for anything else (pageable, device or managed memory).
+void* mapped_host_ptr(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return nullptr;
+  }
+  return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+
+bool is_device_memory(const void* p) {
+  cudaPointerAttributes at{};
+  if (cudaPointerGetAttributes(&at, p) != cudaSuccess) {
+    (void)cudaGetLastError();
+    return false;
+  }
+  return at.type == cudaMemoryTypeDevice;
 }
 
 }  // namespace
@@ -450,6 +478,29 @@ rra_status rra_pipeline_host(const uint8_t* keep_h, const void* q_h, const void*
   g_launches += pipeline_launches(*st, p);
   if ((e = cudaMemcpyAsync(out_h, out_d, out_bytes, cudaMemcpyDeviceToHost, s)) != cudaSuccess)
     return cuda_fail(e, "out D2H");
+  return RRA_OK;
+}
+
+rra_status rra_pipeline_mapped(const uint8_t* keep_h, const void* q_h, const void* k_h, const void* v_h,
+                               int B, int N, int H, int d, float scale, rra_dtype in_dtype, void* out_h,
+                               rra_dtype out_dtype, void* workspace, size_t workspace_bytes, void* stream) {
+  const void* host[5] = {keep_h, q_h, k_h, v_h, out_h};
+  const char* names[5] = {"keep_h", "q_h", "k_h", "v_h", "out_h"};
+  void* mapped[5] = {};
+  for (int i = 0; i < 5; ++i) {
+    if (host[i] == nullptr) return fail(RRA_ERR_INVALID_ARG, "%s is null", names[i]);
+    mapped[i] = mapped_host_ptr(host[i]);
+    if (mapped[i] == nullptr)
+      return fail(RRA_ERR_INVALID_ARG, "%s is not page-locked host memory the device can reach", names[i]);
+  }
+  PipelineArgs p{static_cast<const uint8_t*>(mapped[0]), mapped[1], mapped[2], mapped[3], B, N, H, d, scale,
+                 in_dtype, out_dtype, mapped[4], workspace, workspace_bytes};
+  RRA_TRY(check_pipeline(p));
+  if (!is_device_memory(workspace)) return fail(RRA_ERR_INVALID_ARG, "workspace is not device memory");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  RRA_TRY(enqueue_packed_pipeline(*st, p, static_cast<cudaStream_t>(stream)));
+  g_launches += 2;
   return RRA_OK;
 }
 

@@ -41,6 +41,7 @@ _SIGNATURES = {
     "rra_pipeline_static": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "rra_pipeline_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i,
                                _vp, _vp, _vp, _vp, _vp, _vp, _sz, _vp]),
+    "rra_pipeline_mapped": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
     "rra_plan_create": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz,
                              ctypes.POINTER(_vp)]),
     "rra_plan_launch": (_i, [_vp, _vp]),
@@ -196,6 +197,18 @@ def pipeline_host(keep_h, q_h, k_h, v_h, out_h, keep_d, q_d, k_d, v_d, out_d, wo
                                    B, N, H, d, float(scale), _DTYPE[q_h.dtype], out_h.data_ptr(),
                                    _DTYPE[out_h.dtype], _ptr(keep_d), _ptr(q_d), _ptr(k_d), _ptr(v_d),
                                    _ptr(out_d), _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def pipeline_mapped(keep_h, q_h, k_h, v_h, out_h, workspace, scale: float = 0.125, stream=None):
+    """rra_pipeline_mapped: the kernels read the kept rows from, and write the output into, pinned host memory."""
+    for t in (keep_h, q_h, k_h, v_h, out_h):
+        if t.is_cuda or not t.is_contiguous():
+            raise ValueError("host buffers must be contiguous CPU tensors in pinned memory")
+    B, N, H, d = q_h.shape
+    _check(lib().rra_pipeline_mapped(keep_h.data_ptr(), q_h.data_ptr(), k_h.data_ptr(), v_h.data_ptr(),
+                                     B, N, H, d, float(scale), _DTYPE[q_h.dtype], out_h.data_ptr(),
+                                     _DTYPE[out_h.dtype], _ptr(workspace), _nbytes(workspace),
+                                     _stream(stream)))
 
 
 class Plan:
