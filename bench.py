@@ -278,14 +278,19 @@ def roofline_obj(bytes_alg, flops, us, peaks):
 
 
 def host_latency(rra, B, stream, reps=1000, warmup=100):
-    """Median host-timed µs of one rra_attend (+ stream sync) at serving batch B."""
+    """Median host-timed µs of one rra_attend at serving batch B: + stream sync, and as rra_attend_wait."""
     case = W.make_serving(B)
     keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
-    out, ws = rra.run_pipeline(keep, q, k, v, scale=SCALE)
+    out = torch.empty_like(q)
+    ws = rra.alloc_workspace(B, case.N, case.H, case.d, case.dtype)
     cu, dst, src, qp, kp, vp = rra.workspace_views(ws, B, case.N, case.H, case.d, case.dtype)
+    rra.pack(keep, q, k, v, cu, dst, src, qp, kp, vp, out_zero_fill=out)      # the packed inputs rra_attend reads
     torch.cuda.synchronize()
+    rra.get_device_error(clear=True)
     c_samples = rra.time_attend_host(qp, kp, vp, cu, B, case.N, out, warmup=warmup, reps=reps, src_idx=src,
                                      N=case.N, stream=stream)
+    w_samples = rra.time_attend_wait_host(qp, kp, vp, cu, B, case.N, out, warmup=warmup, reps=reps, src_idx=src,
+                                          N=case.N, stream=stream)
     py = []
     for i in range(warmup + reps):
         t0 = time.perf_counter()
@@ -298,7 +303,11 @@ def host_latency(rra, B, stream, reps=1000, warmup=100):
     g_samples = plan.time_host(warmup, reps, stream=stream)
     plan.close()
     null = rra.time_null_host(warmup, reps, stream=stream)
+    torch.cuda.synchronize()
+    if rra.get_device_error() != 0:
+        raise RuntimeError("host_latency: a kernel recorded a device-side error")
     return {"attend_c": round(statistics.median(c_samples), 2),
+            "attend_wait_c": round(statistics.median(w_samples), 2),
             "attend_python": round(statistics.median(py), 2),
             "pipeline_graph_c": round(statistics.median(g_samples), 2),
             "null_kernel_c": round(statistics.median(null), 2)}

@@ -17,8 +17,9 @@
  *     dispatch as the bottleneck, which the graph plan below addresses.
  *
  * Conventions for every entry point:
- *   - Tensors are device pointers, contiguous, 16-byte aligned (else
- *     RRA_ERR_MISALIGNED).  Padded tensors are [B, N, H, d] row-major; packed
+ *   - Tensors are device pointers (host pointers where an entry point says
+ *     so: rra_pipeline_host, rra_pipeline_mapped), contiguous, 16-byte
+ *     aligned (else RRA_ERR_MISALIGNED).  Padded tensors are [B, N, H, d] row-major; packed
  *     tensors are [cap, H, d] with cap = B*N rows, of which the first T (the
  *     number of kept tokens, known only on the device) are written.
  *   - d must be 64 (else RRA_ERR_UNSUPPORTED); 1 <= N <= 1024; H >= 1;
@@ -33,7 +34,8 @@
  *   - Asynchrony: every call only enqueues work on `stream` (a cudaStream_t;
  *     NULL is the legacy default stream).  Nothing synchronises and nothing
  *     is copied device->host, so the pack / attend / unpack / pipeline calls
- *     can be captured in a CUDA graph.
+ *     can be captured in a CUDA graph.  The exceptions block on purpose:
+ *     rra_attend_wait, rra_get_device_error and the rra_time_* helpers.
  *   - Errors: argument checks run on the host before anything is launched
  *     and return a status with nothing enqueued.  A failed launch returns
  *     RRA_ERR_CUDA.  Inconsistent device-side data (e.g. a cu_seqlens entry
@@ -123,6 +125,22 @@ RRA_API rra_status rra_attend(const void* qp, const void* kp, const void* vp,
                               const int32_t* cu_seqlens, int B, int max_seqlen, int H, int d,
                               float scale, rra_dtype in_dtype, void* o, rra_dtype out_dtype,
                               const int32_t* src_idx, int N, void* stream);
+
+/* rra_attend, blocking until its output is complete, without a stream
+ * synchronisation: the kernel's last CTA to finish publishes a ticket to a
+ * page-locked host word (system-scope release after every CTA's stores),
+ * and the calling thread polls that word.  Same arguments, layouts and
+ * results as rra_attend.  Returns RRA_OK once o holds every row.  After
+ * ~2 ms of polling the call falls back to cudaStreamSynchronize (long calls,
+ * or a kernel that failed), so an asynchronous error still comes back as
+ * RRA_ERR_CUDA.  Calls on one device are serialised by a lock (they share
+ * the word and a device-side count).  Made for host-side latency at serving
+ * sizes (the abstract's dispatch-floor comparison): polling a coherent host
+ * word returns sooner than a stream synchronisation does. */
+RRA_API rra_status rra_attend_wait(const void* qp, const void* kp, const void* vp,
+                                   const int32_t* cu_seqlens, int B, int max_seqlen, int H, int d,
+                                   float scale, rra_dtype in_dtype, void* o, rra_dtype out_dtype,
+                                   const int32_t* src_idx, int N, void* stream);
 
 /* The same attention without a packed copy of the inputs: row t of image
  * b's sequence is read straight from the padded q/k/v [B, N, H, d] at flat
@@ -257,6 +275,14 @@ RRA_API rra_status rra_time_attend_host(const void* qp, const void* kp, const vo
                                         int d, float scale, rra_dtype in_dtype, void* o,
                                         rra_dtype out_dtype, const int32_t* src_idx, int N,
                                         void* stream, int warmup, int reps, double* samples_us);
+
+/* Same helper for rra_attend_wait: {t0; rra_attend_wait(...); t1} (the call
+ * returns once the output is complete, so no stream sync is added). */
+RRA_API rra_status rra_time_attend_wait_host(const void* qp, const void* kp, const void* vp,
+                                             const int32_t* cu_seqlens, int B, int max_seqlen, int H,
+                                             int d, float scale, rra_dtype in_dtype, void* o,
+                                             rra_dtype out_dtype, const int32_t* src_idx, int N,
+                                             void* stream, int warmup, int reps, double* samples_us);
 
 /* Same helper for a graph plan: {t0; rra_plan_launch; sync; t1}. */
 RRA_API rra_status rra_time_plan_host(rra_plan* plan, void* stream, int warmup, int reps,

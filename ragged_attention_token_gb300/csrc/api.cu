@@ -5,6 +5,7 @@
 #include <chrono>
 #include <cstdarg>
 #include <cstdio>
+#include <cstdlib>
 #include <cstring>
 #include <mutex>
 
@@ -35,10 +36,23 @@ rra_status cuda_fail(cudaError_t e, const char* what) {
   return fail(RRA_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
 }
 
+// rra_attend_wait's count of finished CTAs (one per device, 0 between launches).
+__device__ uint32_t g_done_count = 0;
+
 struct DeviceState {
   bool ready = false;
   int num_sms = 0;
   int32_t* err = nullptr;
+  // rra_attend_wait: the page-locked host word the last CTA publishes to,
+  // made on first use, and the ticket of the latest call.  wait_mutex
+  // serialises the calls on this device (they share the count and the word).
+  std::mutex wait_mutex;
+  bool host_count = false;     // the CTA count is the host word itself (native host atomics)
+  uint32_t* done_count = nullptr;
+  uint32_t* host_word = nullptr;
+  uint32_t* host_word_dev = nullptr;
+  uint32_t ticket = 0;
+  uint32_t ctas_counted = 0;   // CTAs launched with a signal so far (mod 2^32)
 };
 
 constexpr int kMaxDevices = 64;
@@ -145,11 +159,75 @@ rra_status enqueue_pack(const DeviceState& st, const uint8_t* keep, int B, int N
   return RRA_OK;
 }
 
+rra_status check_attend(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens, int B,
+                        int max_seqlen, int H, int d, float scale, rra_dtype in_dtype, const void* o,
+                        rra_dtype out_dtype, const int32_t* src_idx, int N) {
+  RRA_TRY(check_shape(B, max_seqlen, H, d));
+  if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
+  if (!valid_out(out_dtype)) return fail(RRA_ERR_INVALID_ARG, "output dtype invalid");
+  if (!finite(scale)) return fail(RRA_ERR_INVALID_ARG, "scale is not finite");
+  RRA_CHECK_PTR(qp);
+  RRA_CHECK_PTR(kp);
+  RRA_CHECK_PTR(vp);
+  RRA_CHECK_PTR(o);
+  if (cu_seqlens == nullptr) return fail(RRA_ERR_INVALID_ARG, "cu_seqlens is null");
+  if (src_idx != nullptr) RRA_TRY(check_shape(B, N, H, d));
+  return RRA_OK;
+}
+
+// The page-locked host word and device count of rra_attend_wait, made on
+// first use (caller holds st.wait_mutex).
+rra_status done_signal_state(DeviceState& st) {
+  if (st.host_word != nullptr) return RRA_OK;
+  void* h = nullptr;
+  cudaError_t e = cudaHostAlloc(&h, 64, cudaHostAllocMapped | cudaHostAllocPortable);
+  if (e != cudaSuccess) return cuda_fail(e, "cudaHostAlloc(completion word)");
+  void* dp = nullptr;
+  e = cudaHostGetDevicePointer(&dp, h, 0);
+  void* cnt = nullptr;
+  if (e == cudaSuccess) e = cudaGetSymbolAddress(&cnt, g_done_count);
+  if (e != cudaSuccess) {
+    cudaFreeHost(h);
+    return cuda_fail(e, "completion word mapping");
+  }
+  int dev = 0, native = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&native, cudaDevAttrHostNativeAtomicSupported, dev) != cudaSuccess) {
+    (void)cudaGetLastError();
+    native = 0;
+  }
+  __atomic_store_n(static_cast<uint32_t*>(h), 0u, __ATOMIC_RELEASE);
+  st.host_word = static_cast<uint32_t*>(h);
+  st.host_word_dev = static_cast<uint32_t*>(dp);
+  // RRA_WAIT_DEVICE_COUNT=1 selects the device-word form even where host
+  // atomics are native (so both forms can be exercised on one machine).
+  const char* force = getenv("RRA_WAIT_DEVICE_COUNT");
+  st.host_count = native != 0 && !(force != nullptr && force[0] == '1');
+  // With native host atomics the CTAs count straight into the host word;
+  // otherwise into a device word, and the last CTA publishes a ticket.
+  st.done_count = st.host_count ? st.host_word_dev : static_cast<uint32_t*>(cnt);
+  st.ctas_counted = 0;
+  return RRA_OK;
+}
+
+struct DoneSignal {
+  uint32_t* count;
+  uint32_t count_base;   // *count before this launch
+  uint32_t* word;
+  uint32_t ticket;
+};
+
 rra_status enqueue_attend(const DeviceState& st, const void* qp, const void* kp, const void* vp,
                           const int32_t* cu, int B, int max_seqlen, int H, float scale,
                           rra_dtype in, void* o, rra_dtype out_dt, const int32_t* src_idx, int N,
-                          cudaStream_t s) {
+                          cudaStream_t s, const DoneSignal* done = nullptr, uint32_t* ctas = nullptr) {
   AttendArgs a{};
+  if (done != nullptr) {
+    a.done_count = done->count;
+    a.done_target = done->count_base;
+    a.done_word = done->word;
+    a.done_ticket = done->ticket;
+  }
   a.qp = qp;
   a.kp = kp;
   a.vp = vp;
@@ -166,9 +244,9 @@ rra_status enqueue_attend(const DeviceState& st, const void* qp, const void* kp,
   if (use_tcgen05(st, B, H)) {
     if (!attend_tc_available())
       return fail(RRA_ERR_CUDA, "attend: the driver's tensor-map encoder is unavailable");
-    e = launch_attend_tc(a, in, out_dt, st.num_sms, s);
+    e = launch_attend_tc(a, in, out_dt, st.num_sms, s, ctas);
   } else {
-    e = launch_attend(a, in, out_dt, s);
+    e = launch_attend(a, in, out_dt, s, ctas);
   }
   if (e != cudaSuccess) return cuda_fail(e, "attend launch");
   return RRA_OK;
@@ -363,21 +441,57 @@ rra_status rra_pack(const uint8_t* keep, int B, int N, int H, int d, rra_dtype i
 rra_status rra_attend(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens,
                       int B, int max_seqlen, int H, int d, float scale, rra_dtype in_dtype, void* o,
                       rra_dtype out_dtype, const int32_t* src_idx, int N, void* stream) {
-  RRA_TRY(check_shape(B, max_seqlen, H, d));
-  if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
-  if (!valid_out(out_dtype)) return fail(RRA_ERR_INVALID_ARG, "output dtype invalid");
-  if (!finite(scale)) return fail(RRA_ERR_INVALID_ARG, "scale is not finite");
-  RRA_CHECK_PTR(qp);
-  RRA_CHECK_PTR(kp);
-  RRA_CHECK_PTR(vp);
-  RRA_CHECK_PTR(o);
-  if (cu_seqlens == nullptr) return fail(RRA_ERR_INVALID_ARG, "cu_seqlens is null");
-  if (src_idx != nullptr) RRA_TRY(check_shape(B, N, H, d));
+  RRA_TRY(check_attend(qp, kp, vp, cu_seqlens, B, max_seqlen, H, d, scale, in_dtype, o, out_dtype, src_idx, N));
   DeviceState* st = nullptr;
   RRA_TRY(device_state(&st));
   RRA_TRY(enqueue_attend(*st, qp, kp, vp, cu_seqlens, B, max_seqlen, H, scale, in_dtype, o, out_dtype,
                          src_idx, src_idx ? N : 0, static_cast<cudaStream_t>(stream)));
   g_launches += 1;
+  return RRA_OK;
+}
+
+rra_status rra_attend_wait(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens, int B,
+                           int max_seqlen, int H, int d, float scale, rra_dtype in_dtype, void* o,
+                           rra_dtype out_dtype, const int32_t* src_idx, int N, void* stream) {
+  RRA_TRY(check_attend(qp, kp, vp, cu_seqlens, B, max_seqlen, H, d, scale, in_dtype, o, out_dtype, src_idx, N));
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  cudaStreamCaptureStatus cap = cudaStreamCaptureStatusNone;
+  cudaError_t ce = cudaStreamIsCapturing(s, &cap);
+  if (ce != cudaSuccess) return cuda_fail(ce, "attend_wait: cudaStreamIsCapturing");
+  if (cap != cudaStreamCaptureStatusNone)
+    return fail(RRA_ERR_INVALID_ARG, "attend_wait blocks on its result and cannot be captured in a graph");
+  std::lock_guard<std::mutex> lock(st->wait_mutex);
+  RRA_TRY(done_signal_state(*st));
+  if (++st->ticket == 0) st->ticket = 1;   // 0 is the word's initial value
+  const uint32_t ticket = st->ticket;
+  const DoneSignal sig{st->done_count, st->ctas_counted, st->host_count ? nullptr : st->host_word_dev, ticket};
+  uint32_t ctas = 0;
+  RRA_TRY(enqueue_attend(*st, qp, kp, vp, cu_seqlens, B, max_seqlen, H, scale, in_dtype, o, out_dtype, src_idx,
+                         src_idx ? N : 0, s, &sig, &ctas));
+  st->ctas_counted += ctas;   // every CTA of the launch will add one to the count
+  g_launches += 1;
+  const uint32_t want = st->host_count ? st->ctas_counted : ticket;
+  // Poll the word for up to ~2 ms (a serving-size call lands in a few us);
+  // a longer call is handed to a stream synchronisation, which also
+  // surfaces an asynchronous error.
+  const auto t0 = std::chrono::steady_clock::now();
+  for (uint32_t spin = 1;; ++spin) {
+    if (__atomic_load_n(st->host_word, __ATOMIC_ACQUIRE) == want) return RRA_OK;
+    if ((spin & 1023u) == 0u && std::chrono::steady_clock::now() - t0 > std::chrono::milliseconds(2)) break;
+  }
+  cudaError_t e = cudaStreamSynchronize(s);
+  if (e != cudaSuccess) return cuda_fail(e, "attend_wait: stream sync");
+  if (__atomic_load_n(st->host_word, __ATOMIC_ACQUIRE) != want) {
+    // Re-read the count so that later calls aim at the right total.
+    uint32_t count = 0;
+    if (st->host_count)
+      st->ctas_counted = __atomic_load_n(st->host_word, __ATOMIC_ACQUIRE);
+    else if (cudaMemcpy(&count, st->done_count, sizeof(count), cudaMemcpyDeviceToHost) == cudaSuccess)
+      st->ctas_counted = count;
+    return fail(RRA_ERR_CUDA, "attend_wait: the kernel finished without publishing its completion word");
+  }
   return RRA_OK;
 }
 
@@ -598,6 +712,23 @@ rra_status rra_time_attend_host(const void* qp, const void* kp, const void* vp, 
     cudaError_t e = cudaStreamSynchronize(s);
     const auto t1 = std::chrono::steady_clock::now();
     if (e != cudaSuccess) return cuda_fail(e, "sync");
+    if (i >= warmup) samples_us[i - warmup] = std::chrono::duration<double, std::micro>(t1 - t0).count();
+  }
+  return RRA_OK;
+}
+
+rra_status rra_time_attend_wait_host(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens,
+                                     int B, int max_seqlen, int H, int d, float scale, rra_dtype in_dtype,
+                                     void* o, rra_dtype out_dtype, const int32_t* src_idx, int N, void* stream,
+                                     int warmup, int reps, double* samples_us) {
+  if (reps < 1 || warmup < 0 || samples_us == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "bad timing arguments");
+  for (int i = 0; i < warmup + reps; ++i) {
+    const auto t0 = std::chrono::steady_clock::now();
+    rra_status rs = rra_attend_wait(qp, kp, vp, cu_seqlens, B, max_seqlen, H, d, scale, in_dtype, o, out_dtype,
+                                    src_idx, N, stream);
+    const auto t1 = std::chrono::steady_clock::now();
+    if (rs != RRA_OK) return rs;
     if (i >= warmup) samples_us[i - warmup] = std::chrono::duration<double, std::micro>(t1 - t0).count();
   }
   return RRA_OK;

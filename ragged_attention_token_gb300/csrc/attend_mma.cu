@@ -139,7 +139,7 @@ __device__ __forceinline__ void store_pair<__half>(__half* p, float x, float y) 
 }
 
 template <typename Tin, typename Tout, bool SCATTER>
-__global__ void __launch_bounds__(THREADS) attend_mma_kernel(const AttendArgs a) {
+__device__ __forceinline__ void attend_mma_tile(const AttendArgs& a) {
   constexpr bool BF16 = IsBf16<Tin>::value;
   // Q tile, then two stages of (K block, V block); all 64 x 64 x 2 B, 1024-B aligned.
   __shared__ __align__(1024) uint8_t smem[BM * 128 + 2 * 2 * BN * 128];
@@ -173,6 +173,30 @@ __global__ void __launch_bounds__(THREADS) attend_mma_kernel(const AttendArgs a)
   load_tile(sK(0), kp, seq_start, 0, n, H, h);
   load_tile(sV(0), vp, seq_start, 0, n, H, h);
   cp_async_commit();
+
+  // Output row of each 16-byte vector this thread stores in the epilogue
+  // (-1: past the image), looked up now so the epilogue does not wait on
+  // the scatter indices.
+  constexpr int VPR = HD / OutVec<Tout>::per16;   // 16-byte vectors per row
+  constexpr int VECS = BM * VPR / THREADS;        // per thread
+  static_assert(BM * VPR % THREADS == 0, "epilogue vectors must divide evenly over the threads");
+  long long dst_rows[VECS];
+#pragma unroll
+  for (int k = 0; k < VECS; ++k) {
+    const int i = m0 + (static_cast<int>(threadIdx.x) + k * THREADS) / VPR;
+    long long r = -1;
+    if (i < n) {
+      r = static_cast<long long>(seq_start) + i;   // packed row
+      if constexpr (SCATTER) {
+        r = __ldg(a.src_idx + r);
+        if (r < 0 || r >= static_cast<long long>(a.B) * a.N) {
+          record_error(a.err, RRA_DEVERR_INDEX_RANGE);
+          r = -1;
+        }
+      }
+    }
+    dst_rows[k] = r;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint32_t qf[4][4];
@@ -319,47 +343,51 @@ __global__ void __launch_bounds__(THREADS) attend_mma_kernel(const AttendArgs a)
     }
   }
   __syncthreads();
-  constexpr int VPR = HD / OutVec<Tout>::per16;   // 16-byte vectors per row
   Tout* out = static_cast<Tout*>(a.o);
-  for (int id = threadIdx.x; id < BM * VPR; id += THREADS) {
+#pragma unroll
+  for (int k = 0; k < VECS; ++k) {
+    if (dst_rows[k] < 0) continue;
+    const int id = static_cast<int>(threadIdx.x) + k * THREADS;
     const int row = id / VPR, c = id - row * VPR;
-    const int i = m0 + row;
-    if (i >= n) continue;
-    long long dst_row = static_cast<long long>(seq_start) + i;   // packed row
-    if constexpr (SCATTER) {
-      dst_row = __ldg(a.src_idx + dst_row);
-      if (dst_row < 0 || dst_row >= static_cast<long long>(a.B) * a.N) {
-        record_error(a.err, RRA_DEVERR_INDEX_RANGE);
-        continue;
-      }
-    }
     const uint4 val = *reinterpret_cast<const uint4*>(so + row * OSTRIDE + c * OutVec<Tout>::per16);
-    uint4* gp = reinterpret_cast<uint4*>(out + (static_cast<size_t>(dst_row) * H + h) * HD) + c;
+    uint4* gp = reinterpret_cast<uint4*>(out + (static_cast<size_t>(dst_rows[k]) * H + h) * HD) + c;
     *gp = val;
   }
 }
 
+// One CTA per (query tile, head, image); CTAs whose tile lies past the
+// image's length (or whose image has a bad length) return at once.
+template <typename Tin, typename Tout, bool SCATTER>
+__global__ void __launch_bounds__(THREADS) attend_mma_kernel(const AttendArgs a) {
+  attend_mma_tile<Tin, Tout, SCATTER>(a);
+  if (a.done_count != nullptr) signal_done(a);
+}
+
 template <typename Tin, typename Tout>
-cudaError_t launch_typed(const AttendArgs& a, cudaStream_t stream) {
+cudaError_t launch_typed(const AttendArgs& a, cudaStream_t stream, uint32_t* ctas) {
   dim3 grid((a.max_seqlen + BM - 1) / BM, a.H, a.B);
-  if (a.src_idx != nullptr)
-    attend_mma_kernel<Tin, Tout, true><<<grid, THREADS, 0, stream>>>(a);
+  const uint32_t n = grid.x * grid.y * grid.z;
+  AttendArgs b = a;
+  if (b.done_count != nullptr) b.done_target += n;
+  if (ctas != nullptr) *ctas = n;
+  if (b.src_idx != nullptr)
+    attend_mma_kernel<Tin, Tout, true><<<grid, THREADS, 0, stream>>>(b);
   else
-    attend_mma_kernel<Tin, Tout, false><<<grid, THREADS, 0, stream>>>(a);
+    attend_mma_kernel<Tin, Tout, false><<<grid, THREADS, 0, stream>>>(b);
   return cudaGetLastError();
 }
 
 }  // namespace
 
-cudaError_t launch_attend(const AttendArgs& a, rra_dtype in, rra_dtype out, cudaStream_t stream) {
+cudaError_t launch_attend(const AttendArgs& a, rra_dtype in, rra_dtype out, cudaStream_t stream, uint32_t* ctas) {
   if (in == RRA_BF16) {
-    if (out == RRA_BF16) return launch_typed<__nv_bfloat16, __nv_bfloat16>(a, stream);
-    if (out == RRA_F16) return launch_typed<__nv_bfloat16, __half>(a, stream);
-    return launch_typed<__nv_bfloat16, float>(a, stream);
+    if (out == RRA_BF16) return launch_typed<__nv_bfloat16, __nv_bfloat16>(a, stream, ctas);
+    if (out == RRA_F16) return launch_typed<__nv_bfloat16, __half>(a, stream, ctas);
+    return launch_typed<__nv_bfloat16, float>(a, stream, ctas);
   }
-  if (out == RRA_BF16) return launch_typed<__half, __nv_bfloat16>(a, stream);
-  if (out == RRA_F16) return launch_typed<__half, __half>(a, stream);
-  return launch_typed<__half, float>(a, stream);
+  if (out == RRA_BF16) return launch_typed<__half, __nv_bfloat16>(a, stream, ctas);
+  if (out == RRA_F16) return launch_typed<__half, __half>(a, stream, ctas);
+  return launch_typed<__half, float>(a, stream, ctas);
 }
 
 }  // namespace rra

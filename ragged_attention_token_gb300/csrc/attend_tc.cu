@@ -1146,6 +1146,11 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
   }
+  // Host completion word (rra_attend_wait): the packed and gather modes
+  // write their output with plain stores only, all issued by now.
+  if constexpr (!FUSED) {
+    if (a.done_count != nullptr) signal_done(a);
+  }
 }
 
 // ---------------------------------------------------------------- host side
@@ -1194,7 +1199,7 @@ cudaError_t make_gather_map(CUtensorMap* map, const void* ptr, long long rows, b
 }
 
 template <typename Tin, typename Tout, bool SCATTER, int MODE>
-cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t stream) {
+cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t stream, uint32_t* ctas) {
   // Largest dynamic shared memory any launch of this instantiation asks for
   // (position lists for N <= 1024 in the fused mode).
   constexpr bool kFused = MODE == MODE_FUSED || MODE == MODE_FUSED_ROWS;
@@ -1255,42 +1260,47 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
   const long long units = static_cast<long long>(a.B) * a.H * qtiles;
   const long long cap = static_cast<long long>(per_sm) * (num_sms > 0 ? num_sms : 152);
   const int grid = static_cast<int>(units < cap ? units : cap);
-  kernel<<<grid, THREADS, smem, stream>>>(mq, mk, mv, a, static_cast<int>(units), pos_stride);
+  AttendArgs b = a;
+  if (b.done_count != nullptr) b.done_target += static_cast<uint32_t>(grid);
+  if (ctas != nullptr) *ctas = static_cast<uint32_t>(grid);
+  kernel<<<grid, THREADS, smem, stream>>>(mq, mk, mv, b, static_cast<int>(units), pos_stride);
   return cudaGetLastError();
 }
 
 template <typename Tin, typename Tout>
-cudaError_t launch_tc_out(const AttendArgs& a, int mode, int num_sms, cudaStream_t stream) {
+cudaError_t launch_tc_out(const AttendArgs& a, int mode, int num_sms, cudaStream_t stream, uint32_t* ctas) {
   if (mode == MODE_FUSED) {
     // Zero fill by bulk copies unless the grid has at most one unit per SM
     // (there the kernel is one latency chain per CTA and plain stores finish
     // sooner: measured 6.0 against 6.6 us on the serving workload).
     const long long units = static_cast<long long>(a.B) * a.H * ((a.max_seqlen + BM - 1) / BM);
     if (units <= (num_sms > 0 ? num_sms : 152))
-      return launch_tc_typed<Tin, Tout, true, MODE_FUSED_ROWS>(a, num_sms, stream);
-    return launch_tc_typed<Tin, Tout, true, MODE_FUSED>(a, num_sms, stream);
+      return launch_tc_typed<Tin, Tout, true, MODE_FUSED_ROWS>(a, num_sms, stream, ctas);
+    return launch_tc_typed<Tin, Tout, true, MODE_FUSED>(a, num_sms, stream, ctas);
   }
-  if (mode == MODE_GATHER) return launch_tc_typed<Tin, Tout, true, MODE_GATHER>(a, num_sms, stream);
-  if (a.src_idx != nullptr) return launch_tc_typed<Tin, Tout, true, MODE_PACKED>(a, num_sms, stream);
-  return launch_tc_typed<Tin, Tout, false, MODE_PACKED>(a, num_sms, stream);
+  if (mode == MODE_GATHER) return launch_tc_typed<Tin, Tout, true, MODE_GATHER>(a, num_sms, stream, ctas);
+  if (a.src_idx != nullptr) return launch_tc_typed<Tin, Tout, true, MODE_PACKED>(a, num_sms, stream, ctas);
+  return launch_tc_typed<Tin, Tout, false, MODE_PACKED>(a, num_sms, stream, ctas);
 }
 
 template <typename Tin>
-cudaError_t launch_tc_in(const AttendArgs& a, rra_dtype out, int mode, int num_sms, cudaStream_t stream) {
-  if (out == RRA_BF16) return launch_tc_out<Tin, __nv_bfloat16>(a, mode, num_sms, stream);
-  if (out == RRA_F16) return launch_tc_out<Tin, __half>(a, mode, num_sms, stream);
-  return launch_tc_out<Tin, float>(a, mode, num_sms, stream);
+cudaError_t launch_tc_in(const AttendArgs& a, rra_dtype out, int mode, int num_sms, cudaStream_t stream,
+                         uint32_t* ctas = nullptr) {
+  if (out == RRA_BF16) return launch_tc_out<Tin, __nv_bfloat16>(a, mode, num_sms, stream, ctas);
+  if (out == RRA_F16) return launch_tc_out<Tin, __half>(a, mode, num_sms, stream, ctas);
+  return launch_tc_out<Tin, float>(a, mode, num_sms, stream, ctas);
 }
 
 }  // namespace
 
 bool attend_tc_available() { return encode_fn(); }
 
-cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream) {
+cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream,
+                             uint32_t* ctas) {
   if (!encode_fn()) return cudaErrorNotSupported;
   if (static_cast<long long>(a.B) * a.max_seqlen >= (1LL << 31)) return cudaErrorInvalidValue;
-  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, MODE_PACKED, num_sms, stream);
-  return launch_tc_in<__half>(a, out, MODE_PACKED, num_sms, stream);
+  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, MODE_PACKED, num_sms, stream, ctas);
+  return launch_tc_in<__half>(a, out, MODE_PACKED, num_sms, stream, ctas);
 }
 
 cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,

@@ -47,7 +47,40 @@ struct AttendArgs {
   int B, H, N, max_seqlen;
   float scale_log2;         // softmax scale times log2(e)
   int32_t* err;
+  // Completion signal for a host that polls instead of synchronising the
+  // stream (rra_attend_wait); done_count == nullptr: off.
+  uint32_t* done_count;     // count of finished CTAs, never reset: a device word,
+                            // or (done_word == nullptr) a page-locked host word
+  uint32_t done_target;     // its value before this launch (the launcher adds the grid size)
+  uint32_t* done_word;      // device address of a page-locked host word, or nullptr
+  uint32_t done_ticket;     // value published to *done_word
 };
+
+// Each CTA adds one to *done_count once all its threads' output stores are
+// issued, with release semantics, so by cumulativity every CTA's stores are
+// visible before the count moves.  The count is never reset and no CTA waits
+// on another.  Two forms:
+//   done_word == nullptr: the count is itself a page-locked host word (the
+//     device has native atomics on host memory); each CTA adds with a
+//     system-scope release reduction, no round trip, and the host polls the
+//     count until it reaches done_target.
+//   otherwise: the count is a device word; the CTA whose add brings it to
+//     done_target publishes done_ticket to the host word with a
+//     system-scope release store.
+// Called by all threads of the CTA (it holds a CTA barrier).
+__device__ __forceinline__ void signal_done(const AttendArgs& a) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    if (a.done_word == nullptr) {
+      asm volatile("red.release.sys.global.add.u32 [%0], 1;" ::"l"(a.done_count) : "memory");
+    } else {
+      uint32_t prev;
+      asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(a.done_count) : "memory");
+      if (prev + 1u == a.done_target)
+        asm volatile("st.release.sys.global.u32 [%0], %1;" ::"l"(a.done_word), "r"(a.done_ticket) : "memory");
+    }
+  }
+}
 
 struct UnpackArgs {
   const uint4* op;
@@ -63,11 +96,15 @@ void set_last_error_message(const char* msg);
 
 // Launchers (each enqueues exactly one kernel on `stream`).
 cudaError_t launch_pack(const PackArgs& a, int num_sms, cudaStream_t stream);
-cudaError_t launch_attend(const AttendArgs& a, rra_dtype in, rra_dtype out, cudaStream_t stream);
+// The attention launchers add their grid size to a.done_target when a
+// completion signal is on and report it through *ctas (when not null).
+cudaError_t launch_attend(const AttendArgs& a, rra_dtype in, rra_dtype out, cudaStream_t stream,
+                          uint32_t* ctas = nullptr);
 cudaError_t launch_unpack(const UnpackArgs& a, cudaStream_t stream);
 // tcgen05 + TMA attention; needs the driver's tensor-map encoder.
 bool attend_tc_available();
-cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream);
+cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream,
+                             uint32_t* ctas = nullptr);
 // Same kernel reading Q/K/V rows straight from the padded [B, N, H, 64]
 // tensors (a.qp/kp/vp) at rows src_idx[t], scattering to the padded output.
 cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,

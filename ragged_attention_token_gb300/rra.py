@@ -49,6 +49,9 @@ _SIGNATURES = {
     "rra_get_device_error": (_i, [ctypes.POINTER(ctypes.c_int32), _i]),
     "rra_time_attend_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp,
                                   _i, _i, _dp]),
+    "rra_time_attend_wait_host": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp,
+                                       _i, _i, _dp]),
+    "rra_attend_wait": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp]),
     "rra_time_plan_host": (_i, [_vp, _vp, _i, _i, _dp]),
     "rra_time_null_host": (_i, [_vp, _i, _i, _dp]),
     "rra_set_attend_kernel": (_i, [_i]),
@@ -159,6 +162,15 @@ def attend(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, scale: float = 0.
                             _stream(stream)))
 
 
+def attend_wait(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, scale: float = 0.125,
+                src_idx=None, N: int = 0, stream=None):
+    """rra_attend_wait: rra_attend, returning once `o` is complete (polls a host completion word)."""
+    H, d = qp.shape[-2], qp.shape[-1]
+    _check(lib().rra_attend_wait(_ptr(qp), _ptr(kp), _ptr(vp), _ptr(cu_seqlens), B, max_seqlen, H, d,
+                                 float(scale), _DTYPE[qp.dtype], _ptr(o), _DTYPE[o.dtype], _ptr(src_idx), N,
+                                 _stream(stream)))
+
+
 def attend_gather(q, k, v, cu_seqlens, src_idx, out, scale: float = 0.125, stream=None):
     """rra_attend_gather: attention reading rows src_idx of padded q/k/v, writing padded out."""
     B, N, H, d = q.shape
@@ -258,6 +270,17 @@ def time_attend_host(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, warmup:
     _check(lib().rra_time_attend_host(_ptr(qp), _ptr(kp), _ptr(vp), _ptr(cu_seqlens), B, max_seqlen, H, d,
                                       float(scale), _DTYPE[qp.dtype], _ptr(o), _DTYPE[o.dtype],
                                       _ptr(src_idx), N, _stream(stream), warmup, reps, buf))
+    return list(buf)
+
+
+def time_attend_wait_host(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, warmup: int, reps: int,
+                          scale: float = 0.125, src_idx=None, N: int = 0, stream=None) -> list[float]:
+    """Host-timed µs of rra_attend_wait calls (each returns with its output complete)."""
+    H, d = qp.shape[-2], qp.shape[-1]
+    buf = (ctypes.c_double * reps)()
+    _check(lib().rra_time_attend_wait_host(_ptr(qp), _ptr(kp), _ptr(vp), _ptr(cu_seqlens), B, max_seqlen, H, d,
+                                           float(scale), _DTYPE[qp.dtype], _ptr(o), _DTYPE[o.dtype],
+                                           _ptr(src_idx), N, _stream(stream), warmup, reps, buf))
     return list(buf)
 
 

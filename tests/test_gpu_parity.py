@@ -294,6 +294,60 @@ def test_host_timed_helpers():
     assert len(z) == 20 and all(x > 0 for x in z)
 
 
+@pytest.mark.parametrize("make", [lambda: W.make_serving(4), lambda: W.make_batched(0.8)], ids=["serving_B4",
+                                                                                             "batched_p80"])
+def test_attend_wait_returns_complete_output(make, kernel):
+    # rra_attend_wait returns only once the output is complete: read it right
+    # away (a copy on another stream, no sync in between) and compare with
+    # rra_attend + sync, bit for bit, over repeated calls (fresh tickets).
+    case = make()
+    ref, qp, kp, vp, cu = _packed_inputs(case)
+    B, N, H, d = case.B, case.N, case.H, case.d
+    T = len(ref["src"])
+    src = torch.from_numpy(ref["src"]).to("cuda")
+    want_packed = torch.empty((B * N, H, d), dtype=torch.float32, device="cuda")
+    rra.attend(qp, kp, vp, cu, B, N, want_packed, scale=SCALE)
+    want_pad = torch.zeros((B, N, H, d), dtype=case.dtype, device="cuda")
+    rra.attend(qp, kp, vp, cu, B, N, want_pad, scale=SCALE, src_idx=src, N=N)
+    torch.cuda.synchronize()
+    err = np.abs(want_packed[:T].cpu().double().numpy() - ref["o"]).max()
+    assert err <= ATOL
+    side = torch.cuda.Stream()
+    n0 = rra.launch_count()
+    for _ in range(3):
+        o = torch.full((B * N, H, d), float("nan"), dtype=torch.float32, device="cuda")
+        o_pad = torch.zeros((B, N, H, d), dtype=case.dtype, device="cuda")
+        torch.cuda.synchronize()
+        rra.attend_wait(qp, kp, vp, cu, B, N, o, scale=SCALE)
+        with torch.cuda.stream(side):
+            got = o[:T].clone()
+        side.synchronize()
+        assert torch.equal(got.view(torch.int32), want_packed[:T].view(torch.int32))
+        rra.attend_wait(qp, kp, vp, cu, B, N, o_pad, scale=SCALE, src_idx=src, N=N)
+        with torch.cuda.stream(side):
+            got_pad = o_pad.clone()
+        side.synchronize()
+        assert torch.equal(got_pad.view(torch.int16), want_pad.view(torch.int16))
+    assert rra.launch_count() - n0 == 6
+    s = rra.time_attend_wait_host(qp, kp, vp, cu, B, N, o, warmup=3, reps=10)
+    assert len(s) == 10 and all(x > 0 for x in s)
+
+
+def test_attend_wait_device_count_form():
+    # The same test in a fresh process with the device-word form of the
+    # completion signal forced (the host-word form is the default where the
+    # device has native atomics on host memory).
+    import os
+    import subprocess
+    import sys
+    env = dict(os.environ, RRA_WAIT_DEVICE_COUNT="1")
+    here = os.path.dirname(os.path.abspath(__file__))
+    r = subprocess.run([sys.executable, "-m", "pytest", "-x", "-q", "-m", "gpu", "-p", "no:cacheprovider",
+                        os.path.join(here, "test_gpu_parity.py"), "-k", "attend_wait_returns_complete_output"],
+                       env=env, capture_output=True, text=True, timeout=600)
+    assert r.returncode == 0, r.stdout[-2000:] + r.stderr[-2000:]
+
+
 def test_launch_count_counts_kernels(kernel):
     case = W.make_tiny()
     keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
