@@ -192,10 +192,16 @@ RRA_API rra_status rra_pipeline_host(const uint8_t* keep_h, const void* q_h, con
  * out_h (attention at kept positions, +0 at pruned ones) straight into host
  * memory.  Pruned input rows never cross the link, so the link carries
  * B*N + 3*T*H*d*size(in) bytes in and B*N*H*d*size(out) bytes out, T the
- * number of kept tokens.  Runs as rra_pack (with the row copy) then
- * rra_attend on the packed buffers in `workspace`, two launches, whatever
- * kernel rra_set_attend_kernel selected (the packed kernels touch host memory
- * with plain loads and stores only).  Host buffers: allocated by
+ * number of kept tokens.  With the tcgen05 kernel (RRA_ATTEND_TCGEN05 or
+ * AUTO) and at most one (image, head, 128-query tile) unit per SM
+ * (B*H*ceil(N/128) <= SM count, serving sizes): ONE launch of the fused
+ * kernel, which copies the kept rows in with 16-byte cp.async copies (no
+ * tensor maps over host memory) and writes every output row with plain
+ * stores; the workspace is not touched.  Otherwise (larger batches, or the
+ * mma.sync kernel selected): rra_pack (with the row copy) then the mma.sync
+ * attention on the packed buffers in `workspace` (its epilogue writes whole
+ * 128-byte lines, the efficient unit over the link), two launches.  Host
+ * buffers: allocated by
  * cudaHostAlloc / cudaMallocHost or registered with cudaHostRegister, and
  * device-accessible (else RRA_ERR_INVALID_ARG, nothing enqueued); pageable
  * memory is refused.  `workspace`: DEVICE memory of rra_workspace_bytes()

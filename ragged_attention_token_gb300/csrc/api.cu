@@ -220,7 +220,8 @@ struct DoneSignal {
 rra_status enqueue_attend(const DeviceState& st, const void* qp, const void* kp, const void* vp,
                           const int32_t* cu, int B, int max_seqlen, int H, float scale,
                           rra_dtype in, void* o, rra_dtype out_dt, const int32_t* src_idx, int N,
-                          cudaStream_t s, const DoneSignal* done = nullptr, uint32_t* ctas = nullptr) {
+                          cudaStream_t s, const DoneSignal* done = nullptr, uint32_t* ctas = nullptr,
+                          bool coalesced_out = false) {
   AttendArgs a{};
   if (done != nullptr) {
     a.done_count = done->count;
@@ -241,7 +242,7 @@ rra_status enqueue_attend(const DeviceState& st, const void* qp, const void* kp,
   a.scale_log2 = scale * 1.4426950408889634f;
   a.err = st.err;
   cudaError_t e;
-  if (use_tcgen05(st, B, H)) {
+  if (!coalesced_out && use_tcgen05(st, B, H)) {
     if (!attend_tc_available())
       return fail(RRA_ERR_CUDA, "attend: the driver's tensor-map encoder is unavailable");
     e = launch_attend_tc(a, in, out_dt, st.num_sms, s, ctas);
@@ -292,8 +293,13 @@ int pipeline_launches(const DeviceState&, const PipelineArgs&) { return pipeline
 
 // The two-launch form: rra_pack (with the row copy, and the zero fill of the
 // pruned output rows) into the workspace, then rra_attend on the packed
-// buffers scattering to the padded output.
-rra_status enqueue_packed_pipeline(const DeviceState& st, const PipelineArgs& p, cudaStream_t s) {
+// buffers scattering to the padded output.  coalesced_out: the output is in
+// host memory; take the mma.sync attention, whose epilogue writes whole
+// 128-byte lines per store instruction (the tcgen05 epilogue writes one row
+// per thread, which crosses the link as partial lines: 213 against 142 us on
+// B=64 at 80% pruning).
+rra_status enqueue_packed_pipeline(const DeviceState& st, const PipelineArgs& p, cudaStream_t s,
+                                   bool coalesced_out = false) {
   size_t off[6], total = 0;
   workspace_layout(p.B, p.N, p.H, p.d, p.in, off, &total);
   uint8_t* ws = static_cast<uint8_t*>(p.ws);
@@ -305,7 +311,8 @@ rra_status enqueue_packed_pipeline(const DeviceState& st, const PipelineArgs& p,
   void* vp = ws + off[5];
   RRA_TRY(enqueue_pack(st, p.keep, p.B, p.N, p.H, p.d, p.in, p.q, p.k, p.v, cu, dst, src, qp, kp, vp,
                        p.out, p.out_dt, s));
-  return enqueue_attend(st, qp, kp, vp, cu, p.B, p.N, p.H, p.scale, p.in, p.out, p.out_dt, src, p.N, s);
+  return enqueue_attend(st, qp, kp, vp, cu, p.B, p.N, p.H, p.scale, p.in, p.out, p.out_dt, src, p.N, s, nullptr,
+                        nullptr, coalesced_out);
 }
 
 rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaStream_t s) {
@@ -613,7 +620,34 @@ rra_status rra_pipeline_mapped(const uint8_t* keep_h, const void* q_h, const voi
   if (!is_device_memory(workspace)) return fail(RRA_ERR_INVALID_ARG, "workspace is not device memory");
   DeviceState* st = nullptr;
   RRA_TRY(device_state(&st));
-  RRA_TRY(enqueue_packed_pipeline(*st, p, static_cast<cudaStream_t>(stream)));
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const long long units = static_cast<long long>(B) * H * ((N + 127) / 128);
+  if (pipeline_fused() && units <= st->num_sms) {
+    // One launch: the tcgen05 kernel scans the mask, copies the kept rows
+    // in with cp.async and writes every output row with plain stores.  Only
+    // while each CTA has at most one (image, head, query tile) unit: larger
+    // batches move more bytes than latency, and there pack's coalesced
+    // 256-thread row copies use the link better than one loading warp per
+    // CTA (measured on B=64: 142 against 190 us at 80% pruning, 399 against
+    // 740 us dense).
+    AttendArgs a{};
+    a.keep = p.keep;
+    a.qp = p.q;
+    a.kp = p.k;
+    a.vp = p.v;
+    a.o = p.out;
+    a.B = p.B;
+    a.H = p.H;
+    a.N = p.N;
+    a.max_seqlen = p.N;
+    a.scale_log2 = p.scale * 1.4426950408889634f;
+    a.err = st->err;
+    cudaError_t e = launch_attend_tc_fused_host(a, p.in, p.out_dt, st->num_sms, s);
+    if (e != cudaSuccess) return cuda_fail(e, "mapped pipeline launch");
+    g_launches += 1;
+    return RRA_OK;
+  }
+  RRA_TRY(enqueue_packed_pipeline(*st, p, s, /*coalesced_out=*/true));
   g_launches += 2;
   return RRA_OK;
 }

@@ -97,8 +97,11 @@ constexpr uint32_t SMEM_ALLOC = OFF_POS + 1024;        // + position lists; slac
 
 // MODE_FUSED: the pruned rows are written by bulk copies (zero_pruned_tokens);
 // MODE_FUSED_ROWS: by plain stores (zero_pruned_rows), for grids of at most
-// one unit per SM, where the kernel is one latency chain per CTA.
-enum { MODE_PACKED = 0, MODE_GATHER = 1, MODE_FUSED = 2, MODE_FUSED_ROWS = 3 };
+// one unit per SM, where the kernel is one latency chain per CTA;
+// MODE_FUSED_HOST: MODE_FUSED_ROWS for keep/q/k/v/out in page-locked host
+// memory: rows come in by 16-byte cp.async copies (completion counted on the
+// stage's mbarrier) instead of TMA, and every output row leaves by plain stores.
+enum { MODE_PACKED = 0, MODE_GATHER = 1, MODE_FUSED = 2, MODE_FUSED_ROWS = 3, MODE_FUSED_HOST = 4 };
 constexpr uint32_t TMEM_COLS = 128;                    // S/P: cols [0,64); O: cols [64,128)
 constexpr uint32_t TMEM_O = BN;
 constexpr uint32_t WAIT_SUSPEND_NS = 20000;            // try_wait suspend hint
@@ -164,6 +167,20 @@ __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.comm
 __device__ __forceinline__ void bulk_wait_read() { asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory"); }
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+// 16-byte copy global -> shared through L2 (the source may be page-locked
+// host memory), and an arrival on `bar` once every cp.async this thread has
+// issued so far has landed (the barrier's expected count includes it).
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_arrive_noinc(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+// Byte offset of 16-byte chunk `ch` of row `row` in a 128-byte-swizzled tile
+// (the layout the TMA copies produce; the tile starts 1024-byte aligned).
+__device__ __forceinline__ uint32_t swz128(int row, int ch) {
+  return static_cast<uint32_t>(row * 128 + ((ch ^ (row & 7)) << 4));
 }
 
 // ------------------------------------------------------------------ tcgen05
@@ -419,11 +436,37 @@ __device__ __forceinline__ void zero_pruned_tokens(const AttendArgs& a, int b, i
   bulk_commit();
 }
 
-// The (b, h) unit's part of the pruned-output zero fill, by either scheme.
-template <typename Tout, bool BULK>
+// Whole output rows (all heads) of image b's pruned tokens -> +0 with plain
+// stores, the share of the (b, h) unit: pruned tokens h, h + H, ... of the
+// list at the back of `pos` (entries N-1, N-2, ...).  The warp writes each
+// token's H*64 contiguous outputs with consecutive lanes on consecutive 16-byte
+// vectors, so every store instruction covers whole 128-byte lines.  Used
+// for an output in host memory: the positions come from the scan (the keep
+// row is not read over the link again) and the writes cross the link as
+// full lines.
+template <typename Tout>
+__device__ __forceinline__ void zero_listed_tokens(const AttendArgs& a, int b, int h, int npruned, uint32_t pos,
+                                                   int lane) {
+  const int vecs = a.H * HD * static_cast<int>(sizeof(Tout)) / 16;   // per token row
+  uint4* img = reinterpret_cast<uint4*>(static_cast<Tout*>(a.o) + static_cast<size_t>(b) * a.N * a.H * HD);
+  for (int r = h; r < npruned; r += a.H) {
+    const size_t j = static_cast<size_t>(ld_shared_u16(pos + 2u * static_cast<uint32_t>(a.N - 1 - r)));
+    uint4* row = img + j * vecs;
+    for (int v = lane; v < vecs; v += 32) row[v] = make_uint4(0u, 0u, 0u, 0u);
+  }
+}
+
+// Zero-fill schemes: per-head rows found by re-reading the keep row (plain
+// stores), whole-token rows by bulk copies, whole-token rows from the scan's
+// list of pruned positions (plain stores).
+enum { ZF_MASK_ROWS = 0, ZF_BULK_TOKENS = 1, ZF_LIST_TOKENS = 2 };
+
+// The (b, h) unit's part of the pruned-output zero fill, by scheme ZF.
+template <typename Tout, int ZF>
 __device__ __forceinline__ void zero_fill_share(const AttendArgs& a, int b, int h, int npruned, uint32_t pos,
                                                 uint32_t zero, int lane) {
-  if constexpr (BULK) zero_pruned_tokens<Tout>(a, b, h, npruned, pos, zero, lane);
+  if constexpr (ZF == ZF_BULK_TOKENS) zero_pruned_tokens<Tout>(a, b, h, npruned, pos, zero, lane);
+  else if constexpr (ZF == ZF_LIST_TOKENS) zero_listed_tokens<Tout>(a, b, h, npruned, pos, lane);
   else zero_pruned_rows<Tout>(a, b, h, lane);
 }
 
@@ -438,7 +481,7 @@ __device__ __forceinline__ void zero_fill_share(const AttendArgs& a, int b, int 
 // the item that follows are in flight, so every output row is written
 // exactly once (images with no kept token too) and the zero fill stays off
 // the path that feeds the tensor cores.
-template <typename Tout, bool BULK>
+template <typename Tout, int ZF>
 __device__ Unit next_unit_fused(int u, int step, int units, int BH, const AttendArgs& a, int lane, uint32_t pos,
                                 uint32_t zero) {
   Unit x;
@@ -464,7 +507,7 @@ __device__ Unit next_unit_fused(int u, int step, int units, int BH, const Attend
         const int kept_before = cnt + __popc(m & lt);
         if (flag[r]) {
           st_shared_u16(pos + 2u * static_cast<uint32_t>(kept_before), static_cast<uint32_t>(j));
-        } else if (BULK && j < a.N) {
+        } else if (ZF != ZF_MASK_ROWS && j < a.N) {
           st_shared_u16(pos + 2u * static_cast<uint32_t>(a.N - 1 - (j - kept_before)), static_cast<uint32_t>(j));
         }
         cnt += __popc(m);
@@ -474,7 +517,7 @@ __device__ Unit next_unit_fused(int u, int step, int units, int BH, const Attend
     if (q0 >= cnt) {
       if (qt == 0) {
         __syncwarp();
-        zero_fill_share<Tout, BULK>(a, b, h, a.N - cnt, pos, zero, lane);
+        zero_fill_share<Tout, ZF>(a, b, h, a.N - cnt, pos, zero, lane);
       }
       continue;
     }
@@ -731,8 +774,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
                      const __grid_constant__ CUtensorMap tmap_v, const AttendArgs a, int units, int pos_stride) {
   constexpr bool BF = IsBf16<Tin>::value == 1;
   constexpr bool GATHER = MODE != MODE_PACKED;
-  constexpr bool FUSED = MODE == MODE_FUSED || MODE == MODE_FUSED_ROWS;
+  constexpr bool FUSED = MODE == MODE_FUSED || MODE == MODE_FUSED_ROWS || MODE == MODE_FUSED_HOST;
   constexpr bool ZF_BULK = MODE == MODE_FUSED;
+  constexpr int ZF = ZF_BULK ? ZF_BULK_TOKENS : (MODE == MODE_FUSED_HOST ? ZF_LIST_TOKENS : ZF_MASK_ROWS);
+  constexpr bool HOSTLD = MODE == MODE_FUSED_HOST;   // cp.async loads (no tensor maps)
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -757,7 +802,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   }
   if (tid == 32) {
     for (int i = 0; i < STAGES; ++i) {
-      mbar_init(bar_full(i), 1);
+      // TMA: the producer's arrive + the copies' bytes; cp.async: one
+      // arrival per producer lane when its copies land + lane 0's arrive.
+      mbar_init(bar_full(i), HOSTLD ? 33 : 1);
       mbar_init(bar_empty(i), 1);
     }
     mbar_init(bar_qempty, 1);
@@ -775,7 +822,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     st_shared_v4(zero_buf + 16 * lane, 0u, 0u, 0u, 0u);   // 32 lanes x 16 B = ZERO_BYTES
     fence_proxy_async();
   }
-  if (warp == PRODUCER_WARP && lane == 0) {
+  if (!HOSTLD && warp == PRODUCER_WARP && lane == 0) {
     prefetch_tensormap(&tmap_q);
     prefetch_tensormap(&tmap_k);
     prefetch_tensormap(&tmap_v);
@@ -798,7 +845,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     int zlast_b = -1, zlast_h = 0, zlast_n = 0;   // fused: the last unit's zero-fill share, if pending
     uint32_t zlast_pos = 0;
     Unit U;
-    if constexpr (FUSED) U = next_unit_fused<Tout, ZF_BULK>(blockIdx.x, step, units, BH, a, lane, pos_addr(0), zero_buf);
+    if constexpr (FUSED) U = next_unit_fused<Tout, ZF>(blockIdx.x, step, units, BH, a, lane, pos_addr(0), zero_buf);
     else U = next_unit(blockIdx.x, step, units, BH, a, lane == 0);
     bool done = false;
     while (!done && !bad) {
@@ -816,10 +863,11 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
             st_shared_u32(d + 0, static_cast<uint32_t>(units));
             mbar_arrive(bar_full(st));
           }
+          if constexpr (HOSTLD) cp_async_arrive_noinc(bar_full(st));
           // The last unit's zero-fill share, after the end of work is
           // published: the other warps need not wait for it.
           if constexpr (FUSED) {
-            if (zlast_b >= 0) zero_fill_share<Tout, ZF_BULK>(a, zlast_b, zlast_h, zlast_n, zlast_pos, zero_buf, lane);
+            if (zlast_b >= 0) zero_fill_share<Tout, ZF>(a, zlast_b, zlast_h, zlast_n, zlast_pos, zero_buf, lane);
           }
           done = true;
           break;
@@ -838,7 +886,34 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           st_shared_u32(d + 32, static_cast<uint32_t>(U.b));
           st_shared_u32(d + 36, static_cast<uint32_t>(uidx % POS_SLOTS));
         }
-        if constexpr (GATHER) {
+        if constexpr (HOSTLD) {
+          // 16-byte pieces, piece p = row p/8, chunk p%8, lanes striding
+          // over them; rows past the tile's end repeat its last row (finite
+          // V rows for the keys the products read past the image's end).
+          const uint32_t pslot = pos_addr(static_cast<int>(uidx % POS_SLOTS));
+          const size_t img = static_cast<size_t>(U.b) * a.N;
+          const uint8_t* qg = static_cast<const uint8_t*>(a.qp);
+          const uint8_t* kg = static_cast<const uint8_t*>(a.kp);
+          const uint8_t* vg = static_cast<const uint8_t*>(a.vp);
+          auto row_off = [&](int t) {
+            return ((img + static_cast<size_t>(ld_shared_u16(pslot + 2 * t))) * a.H + U.h) * (HD * 2);
+          };
+          if (c == 0) {
+            for (int p = lane; p < U.rows_q * 8; p += 32) {
+              const int r = p >> 3, ch = p & 7;
+              cp_async16(sQ + swz128(r, ch), qg + row_off(U.q0 + r) + ch * 16);
+            }
+          }
+          const int nk = (n_c + 15) & ~15;
+          for (int p = lane; p < nk * 8; p += 32) {
+            const int r = p >> 3, ch = p & 7;
+            const size_t off = row_off(k0 + min(r, n_c - 1)) + ch * 16;
+            cp_async16(sK(st) + swz128(r, ch), kg + off);
+            cp_async16(sV(st) + swz128(r, ch), vg + off);
+          }
+          cp_async_arrive_noinc(bar_full(st));
+          if (lane == 0) mbar_arrive(bar_full(st));   // after the descriptor stores
+        } else if constexpr (GATHER) {
           // K: lanes 0-15, V: lanes 16-31, one 4-row gather each; Q: up to 32 lanes.
           const int kgroups = ((n_c + 15) & ~15) / 4;
           const int qgroups = (c == 0) ? (U.rows_q + 3) / 4 : 0;
@@ -879,6 +954,14 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
             tma_load_3d(sV(st) + jj * BOX * 128, &tmap_v, 0, U.h, U.s0 + k0 + jj * BOX, bar_full(st));
           }
         }
+        if constexpr (HOSTLD) {
+          // Output in host memory: the first query tile's share of the
+          // pruned rows goes out right behind the unit's first loads, so
+          // the link carries the writes while the unit computes.
+          if (c == 0 && U.q0 == 0)
+            zero_fill_share<Tout, ZF>(a, U.b, U.h, a.N - U.n, pos_addr(static_cast<int>(uidx % POS_SLOTS)), zero_buf,
+                                      lane);
+        }
         __syncwarp();
         ++j;
       }
@@ -887,15 +970,15 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       const uint32_t zpos = pos_addr(static_cast<int>(uidx % POS_SLOTS));
       ++uidx;
       if constexpr (FUSED)
-        U = next_unit_fused<Tout, ZF_BULK>(U.u + step, step, units, BH, a, lane, pos_addr(uidx % POS_SLOTS), zero_buf);
+        U = next_unit_fused<Tout, ZF>(U.u + step, step, units, BH, a, lane, pos_addr(uidx % POS_SLOTS), zero_buf);
       else U = next_unit(U.u + step, step, units, BH, a, lane == 0);
       if constexpr (FUSED) {
         // With the next unit scanned (and this unit's loads in flight), the
         // first query tile's share of the image's pruned output rows; after
         // the last unit it waits until the end of work is published.
-        if (zq == 0) {
+        if (!HOSTLD && zq == 0) {
           if (U.u < units) {
-            zero_fill_share<Tout, ZF_BULK>(a, zb, zh, zn, zpos, zero_buf, lane);
+            zero_fill_share<Tout, ZF>(a, zb, zh, zn, zpos, zero_buf, lane);
           } else {
             zlast_b = zb;
             zlast_h = zh;
@@ -943,6 +1026,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       const int n_c = min(BN, n - c * BN);
       nk16 = (n_c + 15) & ~15;
       const bool first = c == 0, last = c == nch - 1;
+      if constexpr (HOSTLD) fence_proxy_async();   // cp.async wrote the tiles through the generic proxy
       if constexpr (!GATHER) {
         // Packed boxes: V rows [n_c, nk16) enter the P.V product with p = 0;
         // make them finite zeros (the gathered path repeats a valid row).
@@ -1202,7 +1286,7 @@ template <typename Tin, typename Tout, bool SCATTER, int MODE>
 cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t stream, uint32_t* ctas) {
   // Largest dynamic shared memory any launch of this instantiation asks for
   // (position lists for N <= 1024 in the fused mode).
-  constexpr bool kFused = MODE == MODE_FUSED || MODE == MODE_FUSED_ROWS;
+  constexpr bool kFused = MODE == MODE_FUSED || MODE == MODE_FUSED_ROWS || MODE == MODE_FUSED_HOST;
   constexpr uint32_t kMaxSmem = SMEM_ALLOC + (kFused ? POS_SLOTS * 2048u : 0u);
   auto kernel = attend_tc_kernel<Tin, Tout, SCATTER, MODE>;
   static bool attr_set[kMaxDev] = {};
@@ -1244,8 +1328,10 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
     per_sm = occ_blocks[dev];
   }
   const bool bf16 = IsBf16<Tin>::value == 1;
-  CUtensorMap mq, mk, mv;
-  if constexpr (MODE != MODE_PACKED) {
+  CUtensorMap mq{}, mk{}, mv{};
+  if constexpr (MODE == MODE_FUSED_HOST) {
+    // cp.async loads: the kernel takes no tensor map (the zeroed ones are unused).
+  } else if constexpr (MODE != MODE_PACKED) {
     const long long rows = static_cast<long long>(a.B) * a.N * a.H;
     if ((e = make_gather_map(&mq, a.qp, rows, bf16)) != cudaSuccess) return e;
     if ((e = make_gather_map(&mk, a.kp, rows, bf16)) != cudaSuccess) return e;
@@ -1278,6 +1364,7 @@ cudaError_t launch_tc_out(const AttendArgs& a, int mode, int num_sms, cudaStream
       return launch_tc_typed<Tin, Tout, true, MODE_FUSED_ROWS>(a, num_sms, stream, ctas);
     return launch_tc_typed<Tin, Tout, true, MODE_FUSED>(a, num_sms, stream, ctas);
   }
+  if (mode == MODE_FUSED_HOST) return launch_tc_typed<Tin, Tout, true, MODE_FUSED_HOST>(a, num_sms, stream, ctas);
   if (mode == MODE_GATHER) return launch_tc_typed<Tin, Tout, true, MODE_GATHER>(a, num_sms, stream, ctas);
   if (a.src_idx != nullptr) return launch_tc_typed<Tin, Tout, true, MODE_PACKED>(a, num_sms, stream, ctas);
   return launch_tc_typed<Tin, Tout, false, MODE_PACKED>(a, num_sms, stream, ctas);
@@ -1317,6 +1404,13 @@ cudaError_t launch_attend_tc_fused(const AttendArgs& a, rra_dtype in, rra_dtype 
   if (a.keep == nullptr || a.N > 1024) return cudaErrorInvalidValue;
   if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, MODE_FUSED, num_sms, stream);
   return launch_tc_in<__half>(a, out, MODE_FUSED, num_sms, stream);
+}
+
+cudaError_t launch_attend_tc_fused_host(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
+                                        cudaStream_t stream) {
+  if (a.keep == nullptr || a.N > 1024) return cudaErrorInvalidValue;
+  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, MODE_FUSED_HOST, num_sms, stream);
+  return launch_tc_in<__half>(a, out, MODE_FUSED_HOST, num_sms, stream);
 }
 
 }  // namespace rra

@@ -115,5 +115,10 @@ cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype
 // (padded), a.o, a.B, a.N, a.H, a.scale_log2, a.err are used.
 cudaError_t launch_attend_tc_fused(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
                                    cudaStream_t stream);
+// The same pipeline for keep/q/k/v/o in page-locked host memory (device
+// addresses of the mapping): the rows come in by cp.async copies instead of
+// TMA, every output row leaves by plain stores.
+cudaError_t launch_attend_tc_fused_host(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
+                                        cudaStream_t stream);
 
 }  // namespace rra
