@@ -350,6 +350,44 @@ __device__ __forceinline__ void store16<__half>(__half* dst, const float* o, flo
   store16_half<__half2>(dst, o, inv);
 }
 
+// Loads of one item for an image whose every token is kept (position t is
+// token t): 32-row groups inside the image as one 3-D box each, the partial
+// last group by gather4, repeating its last row.  Kept out of line so that
+// the gather path's code is laid out as without it.
+__device__ __noinline__ void issue_whole_loads(int lane, int qgroups, int kgroups, int row0, int h, int H, int q0,
+                                                int rows_q, int k0, int n_c, uint32_t sq, uint32_t sk, uint32_t sv,
+                                                uint32_t bar, const CUtensorMap* mq, const CUtensorMap* mk,
+                                                const CUtensorMap* mv, const CUtensorMap* mq3,
+                                                const CUtensorMap* mk3, const CUtensorMap* mv3) {
+  if (lane < qgroups) {
+    const int G = lane >> 3;
+    if (32 * G + 32 <= rows_q) {
+      if ((lane & 7) == 0) tma_load_3d(sq + G * 4096, mq3, 0, h, row0 + q0 + 32 * G, bar);
+    } else {
+      int rows[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rows[i] = (row0 + min(q0 + 4 * lane + i, q0 + rows_q - 1)) * H + h;
+      tma_gather4(sq + lane * 512, mq, rows, bar);
+    }
+  }
+  const int g = lane & 15;
+  if (g < kgroups) {
+    const int G = g >> 3;
+    if (32 * G + 32 <= n_c) {
+      if ((g & 7) == 0) {
+        if (lane < 16) tma_load_3d(sk + G * 4096, mk3, 0, h, row0 + k0 + 32 * G, bar);
+        else tma_load_3d(sv + G * 4096, mv3, 0, h, row0 + k0 + 32 * G, bar);
+      }
+    } else {
+      int rows[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) rows[i] = (row0 + min(k0 + 4 * g + i, k0 + n_c - 1)) * H + h;
+      if (lane < 16) tma_gather4(sk + g * 512, mk, rows, bar);
+      else tma_gather4(sv + g * 512, mv, rows, bar);
+    }
+  }
+}
+
 // One unit of work as every thread of the CTA sees it (all fields uniform).
 struct Unit {
   int u, b, h, s0, n, q0, rows_q, nchunks;
@@ -785,7 +823,9 @@ __device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
 template <typename Tin, typename Tout, bool SCATTER, int MODE>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
-                     const __grid_constant__ CUtensorMap tmap_v, const AttendArgs a, int units, int pos_stride) {
+                     const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_q3,
+                     const __grid_constant__ CUtensorMap tmap_k3, const __grid_constant__ CUtensorMap tmap_v3,
+                     const AttendArgs a, int units, int pos_stride) {
   constexpr bool BF = IsBf16<Tin>::value == 1;
   constexpr bool GATHER = MODE != MODE_PACKED;
   constexpr bool FUSED = MODE == MODE_FUSED || MODE == MODE_FUSED_ROWS || MODE == MODE_FUSED_HOST;
@@ -946,27 +986,34 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           if (lane == 0) mbar_expect_tx(bar_full(st), static_cast<uint32_t>((2 * kgroups + qgroups) * 512));
           __syncwarp();
           const uint32_t pslot = pos_addr(static_cast<int>(uidx % POS_SLOTS));
-          if (lane < qgroups) {
-            int rows[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int t = min(U.q0 + 4 * lane + i, U.q0 + U.rows_q - 1);
-              if constexpr (FUSED) rows[i] = (U.b * a.N + ld_shared_u16(pslot + 2 * t)) * a.H + U.h;
-              else rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+          bool whole = false;   // every token of the image kept: position t is token t
+          if constexpr (FUSED) whole = U.n == a.N;
+          if (whole) {
+            issue_whole_loads(lane, qgroups, kgroups, U.b * a.N, U.h, a.H, U.q0, U.rows_q, k0, n_c, sQ, sK(st), sV(st),
+                              bar_full(st), &tmap_q, &tmap_k, &tmap_v, &tmap_q3, &tmap_k3, &tmap_v3);
+          } else {
+            if (lane < qgroups) {
+              int rows[4];
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int t = min(U.q0 + 4 * lane + i, U.q0 + U.rows_q - 1);
+                if constexpr (FUSED) rows[i] = (U.b * a.N + ld_shared_u16(pslot + 2 * t)) * a.H + U.h;
+                else rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+              }
+              tma_gather4(sQ + lane * 512, &tmap_q, rows, bar_full(st));
             }
-            tma_gather4(sQ + lane * 512, &tmap_q, rows, bar_full(st));
-          }
-          const int g = lane & 15;
-          if (g < kgroups) {
-            int rows[4];
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const int t = min(k0 + 4 * g + i, k0 + n_c - 1);
-              if constexpr (FUSED) rows[i] = (U.b * a.N + ld_shared_u16(pslot + 2 * t)) * a.H + U.h;
-              else rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+            const int g = lane & 15;
+            if (g < kgroups) {
+              int rows[4];
+  #pragma unroll
+              for (int i = 0; i < 4; ++i) {
+                const int t = min(k0 + 4 * g + i, k0 + n_c - 1);
+                if constexpr (FUSED) rows[i] = (U.b * a.N + ld_shared_u16(pslot + 2 * t)) * a.H + U.h;
+                else rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+              }
+              if (lane < 16) tma_gather4(sK(st) + g * 512, &tmap_k, rows, bar_full(st));
+              else tma_gather4(sV(st) + g * 512, &tmap_v, rows, bar_full(st));
             }
-            if (lane < 16) tma_gather4(sK(st) + g * 512, &tmap_k, rows, bar_full(st));
-            else tma_gather4(sV(st) + g * 512, &tmap_v, rows, bar_full(st));
           }
         } else if (lane == 0) {
           // 32-row boxes: up to two each for K and V, four for Q.
@@ -1356,7 +1403,7 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
     per_sm = occ_blocks[dev];
   }
   const bool bf16 = IsBf16<Tin>::value == 1;
-  CUtensorMap mq{}, mk{}, mv{};
+  CUtensorMap mq{}, mk{}, mv{}, mq3{}, mk3{}, mv3{};
   if constexpr (MODE == MODE_FUSED_HOST) {
     // cp.async loads: the kernel takes no tensor map (the zeroed ones are unused).
   } else if constexpr (MODE != MODE_PACKED) {
@@ -1364,6 +1411,13 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
     if ((e = make_gather_map(&mq, a.qp, rows, bf16)) != cudaSuccess) return e;
     if ((e = make_gather_map(&mk, a.kp, rows, bf16)) != cudaSuccess) return e;
     if ((e = make_gather_map(&mv, a.vp, rows, bf16)) != cudaSuccess) return e;
+    if constexpr (kFused) {
+      // 32-token boxes for images whose every token is kept
+      const long long tokens = static_cast<long long>(a.B) * a.N;
+      if ((e = make_map(&mq3, a.qp, a.H, tokens, bf16)) != cudaSuccess) return e;
+      if ((e = make_map(&mk3, a.kp, a.H, tokens, bf16)) != cudaSuccess) return e;
+      if ((e = make_map(&mv3, a.vp, a.H, tokens, bf16)) != cudaSuccess) return e;
+    }
   } else {
     const long long rows = static_cast<long long>(a.B) * a.max_seqlen;
     if ((e = make_map(&mq, a.qp, a.H, rows, bf16)) != cudaSuccess) return e;
@@ -1390,7 +1444,7 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, b, static_cast<int>(units), pos_stride);
+  return cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mq3, mk3, mv3, b, static_cast<int>(units), pos_stride);
 }
 
 template <typename Tin, typename Tout>
