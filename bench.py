@@ -250,8 +250,8 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
 # capture of the same launches (dram__bytes_read.sum + dram__bytes_write.sum).  They
 # describe the kernel source whose SHA-256 starts with TRAFFIC_SRC_SHA; once that file
 # changes the traffic is reported as null until it is captured again.
-TRAFFIC_SRC_SHA = "64efef59ca3ada58"
-TRAFFIC_BYTES = {"serving_B4": 430798, "batched_b64_p80": 11922603}
+TRAFFIC_SRC_SHA = "995dcc5285738e7e"
+TRAFFIC_BYTES = {"serving_B4": 430730, "batched_b64_p80": 11921664}
 
 
 def measured_traffic(key):

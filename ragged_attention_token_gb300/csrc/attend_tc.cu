@@ -13,9 +13,12 @@
 //
 //   warp 4     loads: per item, TMA copies of the chunk's K and V rows into a
 //              2-stage ring (and, on a unit's first item, of the Q tile),
-//              128-byte swizzle.  In the fused pipeline this warp also scans
-//              the image's keep row (kept positions -> a shared list) and
-//              writes +0 to the output rows of pruned positions;
+//              128-byte swizzle: 32-row boxes of packed tensors, gather4 of
+//              kept rows of padded tensors (3-D boxes where an image keeps
+//              every token), or, for tensors in host memory, 16-byte cp.async
+//              copies into the same layout.  In the fused pipeline this warp
+//              also scans the image's keep row (kept positions -> a shared
+//              list) and writes +0 to the output rows of pruned positions;
 //   warp 5     tensor-core products, issued by one elected lane of the
 //              converged warp: S = Q K^T (M=128, N=chunk rounded up to 16,
 //              K=64) into TMEM columns 0..63, and O += P_hi V + P_lo V (M=128,
