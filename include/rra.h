@@ -107,6 +107,28 @@ RRA_API rra_status rra_pack(const uint8_t* keep, int B, int N, int H, int d, rra
                             void* qp, void* kp, void* vp,
                             void* out_zero_fill, rra_dtype out_dtype, void* stream);
 
+/* Re-pack between the layers of progressive token pruning (EViT-like pruners
+ * drop tokens at a few layers; abstract, both revisions): the next layer's
+ * packed buffers are built from the previous layer's packed buffers instead
+ * of padded tensors, so no padded tensor exists between layers.
+ *   keep_new  uint8 [B, N]: the new layer's mask over the ORIGINAL positions,
+ *             a subset of the previous layer's mask;
+ *   dst_prev  int32 [B*N]: the previous layer's dst_idx (packed row of each
+ *             original position, -1 where it was pruned);
+ *   qp_prev/kp_prev/vp_prev: the previous layer's packed [cap, H, d] rows.
+ * Writes cu_seqlens, dst_idx and src_idx exactly as rra_pack(keep_new) does
+ * (src_idx keeps ORIGINAL flat positions b*N+j, so one rra_unpack or scatter
+ * after the last layer restores the padded layout), and copies row
+ * dst_prev[b*N+j] of each previous buffer to the new packed row of every
+ * position keep_new keeps.  A position keep_new keeps that dst_prev marks
+ * pruned records RRA_DEVERR_INDEX_RANGE and its rows are not copied.  The
+ * previous and new buffers must not overlap (RRA_ERR_INVALID_ARG).  One
+ * launch, asynchronous on `stream`. */
+RRA_API rra_status rra_repack(const uint8_t* keep_new, const int32_t* dst_prev, int B, int N, int H, int d,
+                              rra_dtype in_dtype, const void* qp_prev, const void* kp_prev,
+                              const void* vp_prev, int32_t* cu_seqlens, int32_t* dst_idx,
+                              int32_t* src_idx, void* qp, void* kp, void* vp, void* stream);
+
 /* Bidirectional ragged attention on packed buffers (method overview,
  * bullet 2; abstract).  For image b with rows s = cu[b] .. e = cu[b+1]-1 and
  * head h, for every row i in [s, e]:

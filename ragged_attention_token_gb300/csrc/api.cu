@@ -137,8 +137,11 @@ bool use_tcgen05(const DeviceState& st, int B, int H) {
 rra_status enqueue_pack(const DeviceState& st, const uint8_t* keep, int B, int N, int H, int d,
                         rra_dtype in, const void* q, const void* k, const void* v, int32_t* cu,
                         int32_t* dst, int32_t* src, void* qp, void* kp, void* vp, void* outz,
-                        rra_dtype out_dt, cudaStream_t s) {
+                        rra_dtype out_dt, cudaStream_t s, const int32_t* src_rows = nullptr) {
   PackArgs a{};
+  a.src_rows = src_rows;
+  a.src_cap = static_cast<long long>(B) * N;
+  a.err = st.err;
   a.keep = keep;
   a.B = B;
   a.N = N;
@@ -441,6 +444,37 @@ rra_status rra_pack(const uint8_t* keep, int B, int N, int H, int d, rra_dtype i
   RRA_TRY(device_state(&st));
   RRA_TRY(enqueue_pack(*st, keep, B, N, H, d, in_dtype, q, k, v, cu_seqlens, dst_idx, src_idx, qp, kp, vp,
                        out_zero_fill, out_dtype, static_cast<cudaStream_t>(stream)));
+  g_launches += 1;
+  return RRA_OK;
+}
+
+rra_status rra_repack(const uint8_t* keep_new, const int32_t* dst_prev, int B, int N, int H, int d,
+                      rra_dtype in_dtype, const void* qp_prev, const void* kp_prev, const void* vp_prev,
+                      int32_t* cu_seqlens, int32_t* dst_idx, int32_t* src_idx, void* qp, void* kp, void* vp,
+                      void* stream) {
+  RRA_TRY(check_shape(B, N, H, d));
+  if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
+  if (keep_new == nullptr || dst_prev == nullptr) return fail(RRA_ERR_INVALID_ARG, "keep_new or dst_prev is null");
+  RRA_CHECK_PTR(qp_prev);
+  RRA_CHECK_PTR(kp_prev);
+  RRA_CHECK_PTR(vp_prev);
+  RRA_CHECK_PTR(qp);
+  RRA_CHECK_PTR(kp);
+  RRA_CHECK_PTR(vp);
+  if (cu_seqlens == nullptr || dst_idx == nullptr || src_idx == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "index buffer is null");
+  const size_t bytes = static_cast<size_t>(B) * N * H * d * dtype_bytes(in_dtype);
+  const void* prev[3] = {qp_prev, kp_prev, vp_prev};
+  const void* next[3] = {qp, kp, vp};
+  for (const void* x : prev)
+    for (const void* y : next) {
+      const uintptr_t a0 = reinterpret_cast<uintptr_t>(x), b0 = reinterpret_cast<uintptr_t>(y);
+      if (a0 < b0 + bytes && b0 < a0 + bytes) return fail(RRA_ERR_INVALID_ARG, "previous and new packed buffers overlap");
+    }
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  RRA_TRY(enqueue_pack(*st, keep_new, B, N, H, d, in_dtype, qp_prev, kp_prev, vp_prev, cu_seqlens, dst_idx, src_idx,
+                       qp, kp, vp, nullptr, RRA_F32, static_cast<cudaStream_t>(stream), dst_prev));
   g_launches += 1;
   return RRA_OK;
 }

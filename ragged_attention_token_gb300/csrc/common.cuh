@@ -34,6 +34,11 @@ struct PackArgs {
   int32_t* cu_seqlens;
   int32_t* dst_idx;
   int32_t* src_idx;
+  // Re-pack: the row copied for kept position g is row src_rows[g] of q/k/v
+  // (a previous layer's packed buffers, src_cap rows) instead of row g.
+  const int32_t* src_rows;
+  long long src_cap;
+  int32_t* err;
 };
 
 struct AttendArgs {

@@ -70,7 +70,7 @@ __global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const PackArgs a) {
   __shared__ int s_red[PACK_WARPS];
   __shared__ int s_kept_cnt[PACK_WARPS];
   __shared__ int s_pruned_cnt[PACK_WARPS];
-  __shared__ int s_kept_g[PACK_THREADS];
+  __shared__ long long s_kept_src[PACK_THREADS];   // source row of the copy, -1: none
   __shared__ int s_kept_dst[PACK_THREADS];
   __shared__ int s_pruned_g[PACK_THREADS];
 
@@ -109,7 +109,15 @@ __global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const PackArgs a) {
       a.dst_idx[g] = kept ? excl : -1;
       if (kept) {
         a.src_idx[excl] = static_cast<int32_t>(g);
-        s_kept_g[local_rank] = static_cast<int>(g - g0);
+        long long srow = g;
+        if (a.src_rows != nullptr) {
+          srow = __ldg(a.src_rows + g);
+          if (srow < 0 || srow >= a.src_cap) {   // kept now, pruned before: nothing to copy
+            record_error(a.err, RRA_DEVERR_INDEX_RANGE);
+            srow = -1;
+          }
+        }
+        s_kept_src[local_rank] = srow;
         s_kept_dst[local_rank] = excl;
       } else {
         s_pruned_g[pruned_off + __popc(pb & lt_mask)] = static_cast<int>(g - g0);
@@ -123,22 +131,26 @@ __global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const PackArgs a) {
     const int rv = a.row_vecs;
     const int items = kept_total * rv;
     int it = threadIdx.x;
-    for (; it + PACK_THREADS < items; it += 2 * PACK_THREADS) {
-      const int t0 = it / rv, c0 = it - t0 * rv;
-      const int i1 = it + PACK_THREADS;
-      const int t1 = i1 / rv, c1 = i1 - t1 * rv;
-      const size_t s0 = static_cast<size_t>(g0 + s_kept_g[t0]) * rv + c0;
-      const size_t d0 = static_cast<size_t>(s_kept_dst[t0]) * rv + c0;
-      const size_t s1 = static_cast<size_t>(g0 + s_kept_g[t1]) * rv + c1;
-      const size_t d1 = static_cast<size_t>(s_kept_dst[t1]) * rv + c1;
-      const uint4 q0 = __ldg(a.q + s0), k0 = __ldg(a.k + s0), v0 = __ldg(a.v + s0);
-      const uint4 q1 = __ldg(a.q + s1), k1 = __ldg(a.k + s1), v1 = __ldg(a.v + s1);
-      a.qp[d0] = q0; a.kp[d0] = k0; a.vp[d0] = v0;
-      a.qp[d1] = q1; a.kp[d1] = k1; a.vp[d1] = v1;
+    if (a.src_rows == nullptr) {
+      for (; it + PACK_THREADS < items; it += 2 * PACK_THREADS) {
+        const int t0 = it / rv, c0 = it - t0 * rv;
+        const int i1 = it + PACK_THREADS;
+        const int t1 = i1 / rv, c1 = i1 - t1 * rv;
+        const size_t s0 = static_cast<size_t>(s_kept_src[t0]) * rv + c0;
+        const size_t d0 = static_cast<size_t>(s_kept_dst[t0]) * rv + c0;
+        const size_t s1 = static_cast<size_t>(s_kept_src[t1]) * rv + c1;
+        const size_t d1 = static_cast<size_t>(s_kept_dst[t1]) * rv + c1;
+        const uint4 q0 = __ldg(a.q + s0), k0 = __ldg(a.k + s0), v0 = __ldg(a.v + s0);
+        const uint4 q1 = __ldg(a.q + s1), k1 = __ldg(a.k + s1), v1 = __ldg(a.v + s1);
+        a.qp[d0] = q0; a.kp[d0] = k0; a.vp[d0] = v0;
+        a.qp[d1] = q1; a.kp[d1] = k1; a.vp[d1] = v1;
+      }
     }
     for (; it < items; it += PACK_THREADS) {
       const int t0 = it / rv, c0 = it - t0 * rv;
-      const size_t s0 = static_cast<size_t>(g0 + s_kept_g[t0]) * rv + c0;
+      const long long sr = s_kept_src[t0];
+      if (sr < 0) continue;
+      const size_t s0 = static_cast<size_t>(sr) * rv + c0;
       const size_t d0 = static_cast<size_t>(s_kept_dst[t0]) * rv + c0;
       const uint4 q0 = __ldg(a.q + s0), k0 = __ldg(a.k + s0), v0 = __ldg(a.v + s0);
       a.qp[d0] = q0; a.kp[d0] = k0; a.vp[d0] = v0;

@@ -35,6 +35,7 @@ _SIGNATURES = {
     "rra_workspace_offsets": (_i, [_i, _i, _i, _i, _i, ctypes.POINTER(_sz)]),
     "rra_pack": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp]),
     "rra_attend": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp]),
+    "rra_repack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "rra_attend_gather": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "rra_unpack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "rra_pipeline": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
@@ -152,6 +153,15 @@ def pack(keep, q, k, v, cu_seqlens, dst_idx, src_idx, qp=None, kp=None, vp=None,
     _check(lib().rra_pack(_ptr(keep), B, N, H, d, _DTYPE[q.dtype], _ptr(q), _ptr(k), _ptr(v),
                           _ptr(cu_seqlens), _ptr(dst_idx), _ptr(src_idx), _ptr(qp), _ptr(kp), _ptr(vp),
                           _ptr(out_zero_fill), out_dt, _stream(stream)))
+
+
+def repack(keep_new, dst_prev, qp_prev, kp_prev, vp_prev, cu_seqlens, dst_idx, src_idx, qp, kp, vp, stream=None):
+    """rra_repack: the next layer's packed rows from the previous layer's packed rows."""
+    B, N = keep_new.shape
+    H, d = qp_prev.shape[-2], qp_prev.shape[-1]
+    _check(lib().rra_repack(_ptr(keep_new), _ptr(dst_prev), B, N, H, d, _DTYPE[qp_prev.dtype], _ptr(qp_prev),
+                            _ptr(kp_prev), _ptr(vp_prev), _ptr(cu_seqlens), _ptr(dst_idx), _ptr(src_idx),
+                            _ptr(qp), _ptr(kp), _ptr(vp), _stream(stream)))
 
 
 def attend(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, scale: float = 0.125,

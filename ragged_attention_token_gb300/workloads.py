@@ -35,6 +35,7 @@ HEAD_DIM = 64
 
 WORKLOADS = ("tiny", "serving", "batched", "hires", "progressive")
 _WORKLOAD_INDEX = {name: i + 1 for i, name in enumerate(WORKLOADS)}
+_CHAIN_SEED_BASE = 1_000_000   # seeds of the progressive chain: base + 100*B (+ layer)
 
 SERVING_BATCHES = (1, 2, 4)
 BATCHED_RATES = (0.0, 0.5, 0.8, 0.9)
@@ -208,6 +209,23 @@ def make_progressive_layer(layer: int, masks: list[torch.Tensor] | None = None,
     q, k, v = _values(g, B, N, H, HEAD_DIM, torch.bfloat16)
     return Case(f"progressive_L{layer}", B, N, H, HEAD_DIM, torch.bfloat16,
                 masks[layer - 1].clone(), q, k, v, seed, {"layer": layer})
+
+
+def make_progressive_chain(B: int = 256, N: int = 197, H: int = 6,
+                           seed: int | None = None) -> tuple[list[torch.Tensor], list[Case]]:
+    """The 12-layer progressive workload at batch B as one chain: the masks of
+    ``progressive_masks(B, N)`` and, per layer, fresh seeded Q/K/V.  The chained
+    path packs layer 1 from its padded tensors and re-packs every later layer's
+    inputs from the previous layer's packed layout."""
+    base = _CHAIN_SEED_BASE + 100 * B if seed is None else seed
+    masks = progressive_masks(B, N, base)
+    cases = []
+    for layer in range(1, PROGRESSIVE_LAYERS + 1):
+        g = _gen(base + layer)
+        q, k, v = _values(g, B, N, H, HEAD_DIM, torch.bfloat16)
+        cases.append(Case(f"progressive_chain_L{layer}", B, N, H, HEAD_DIM, torch.bfloat16,
+                          masks[layer - 1].clone(), q, k, v, base + layer, {"layer": layer}))
+    return masks, cases
 
 
 def make_custom(B: int, N: int, H: int, lengths: list[int] | None = None,
