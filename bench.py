@@ -601,6 +601,80 @@ def run_rra(args, world, rank, local):
     return 0
 
 
+def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
+    """The 12-layer progressive workload at batch B, one CUDA graph per pass, two ways.
+
+    chain: layer 1 packs its padded Q/K/V; every later layer receives its Q/K/V
+    in the previous layer's packed layout (as projections of packed features
+    would) and re-packs them at a pruning layer (rra_repack); attention runs on
+    packed buffers; one unpack after the last layer.  per_layer: rra_pipeline
+    (padded in, padded out) for every layer."""
+    dev = torch.device("cuda", 0)
+    masks, cases = W.make_progressive_chain(B)
+    N, H, d = cases[0].N, cases[0].H, cases[0].d
+    L = len(cases)
+    keeps = [m.to(dev) for m in masks]
+    padded = [tuple(x.to(dev) for x in (c.q, c.k, c.v)) for c in cases]
+
+    def index_bufs():
+        return (torch.empty(B + 1, dtype=torch.int32, device=dev), torch.empty(B * N, dtype=torch.int32, device=dev),
+                torch.empty(B * N, dtype=torch.int32, device=dev))
+
+    def packed_bufs():
+        return [torch.empty((B * N, H, d), dtype=torch.bfloat16, device=dev) for _ in range(3)]
+
+    inputs = [padded[0]]
+    for l in range(1, L):
+        pb = packed_bufs()
+        rra.pack(keeps[l - 1], *padded[l], *index_bufs(), *pb, stream=stream)
+        inputs.append(tuple(pb))
+    stream.synchronize()
+    event = [l > 0 and not torch.equal(masks[l], masks[l - 1]) for l in range(L)]
+    idx = []
+    for l in range(L):
+        idx.append(index_bufs() if (l == 0 or event[l]) else idx[l - 1])
+    packed = [packed_bufs() if (l == 0 or event[l]) else None for l in range(L)]
+    outs = [torch.empty((B * N, H, d), dtype=torch.bfloat16, device=dev) for _ in range(L)]
+    final = torch.empty((B, N, H, d), dtype=torch.bfloat16, device=dev)
+
+    def chain():
+        rra.pack(keeps[0], *inputs[0], *idx[0], *packed[0], stream=stream)
+        for l in range(L):
+            src = packed[0] if l == 0 else inputs[l]
+            if l > 0 and event[l]:
+                rra.repack(keeps[l], idx[l - 1][1], *inputs[l], *idx[l], *packed[l], stream=stream)
+                src = packed[l]
+            rra.attend(*src, idx[l][0], B, N, outs[l], scale=SCALE, stream=stream)
+        rra.unpack(outs[L - 1], idx[L - 1][1], B, N, final, stream=stream)
+
+    ws = rra.alloc_workspace(B, N, H, d, torch.bfloat16)
+    outs_pl = [torch.empty_like(padded[l][0]) for l in range(L)]
+
+    def per_layer():
+        for l in range(L):
+            rra.pipeline(keeps[l], *padded[l], outs_pl[l], ws, scale=SCALE, stream=stream)
+
+    t_chain = graph_time_per_launch([chain], stream, reps)
+    t_layer = graph_time_per_launch([per_layer], stream, reps)
+    kept = [int((m != 0).sum()) for m in masks]
+    row = H * d * 2
+    chain_bytes = B * N + 6 * kept[0] * row + B * N * row + kept[-1] * row
+    for l in range(L):
+        chain_bytes += 4 * kept[l] * row                       # attention: Q, K, V in, O out
+        if l > 0 and event[l]:
+            chain_bytes += B * N + 4 * B * N + 6 * kept[l] * row   # mask, previous dst, rows in and out
+    t_min = chain_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    line = {"case": f"progressive_chain_B{B}", "B": B, "N": N, "H": H, "layers": L, "kept_tokens_all_layers": sum(kept),
+            "chain_us": round(t_chain, 2), "per_layer_fused_us": round(t_layer, 2),
+            "chain_speedup": round(t_layer / t_chain, 3),
+            "chain_tokens_per_s": round(sum(kept) / (t_chain * 1e-6), 1),
+            "chain_min_us": round(t_min, 2), "chain_frac": round(t_min / t_chain, 4),
+            "launches_chain": 1 + L + sum(event) + 1, "launches_per_layer": L}
+    del padded, inputs, packed, outs, outs_pl, final, ws
+    torch.cuda.empty_cache()
+    return line
+
+
 def run_sweep(args):
     """Every workload: device µs per kernel, path tokens/s, roofline (one JSON line each)."""
     from ragged_attention_token_gb300 import build as _build
@@ -630,6 +704,7 @@ def run_sweep(args):
                 "fused_tokens_per_s": round(case.kept_tokens / (kt["fused_us"] * 1e-6), 1)}
         print(json.dumps(line), flush=True)
         del sets
+    print(json.dumps(progressive_chain_times(rra, stream, peaks)), flush=True)
     return 0
 
 
