@@ -30,7 +30,8 @@
  *   - Ownership: the caller allocates and frees every buffer.  The library
  *     allocates no device memory, except the CUDA graph owned by an rra_plan
  *     (and the fixed scratch array of rra_pipeline_static, which is part of
- *     the loaded module).
+ *     the loaded module); rra_attend_wait keeps one 64-byte page-locked host
+ *     word per device.
  *   - Asynchrony: every call only enqueues work on `stream` (a cudaStream_t;
  *     NULL is the legacy default stream).  Nothing synchronises and nothing
  *     is copied device->host, so the pack / attend / unpack / pipeline calls
@@ -156,7 +157,10 @@ RRA_API rra_status rra_attend(const void* qp, const void* kp, const void* vp,
  * ~2 ms of polling the call falls back to cudaStreamSynchronize (long calls,
  * or a kernel that failed), so an asynchronous error still comes back as
  * RRA_ERR_CUDA.  Calls on one device are serialised by a lock (they share
- * the word and a device-side count).  Made for host-side latency at serving
+ * the word and a device-side count).  The first call on a device allocates
+ * that 64-byte page-locked host word (cudaHostAlloc, kept until the process
+ * exits).  A call on a stream that is being captured returns
+ * RRA_ERR_INVALID_ARG with nothing enqueued.  Made for host-side latency at serving
  * sizes (the abstract's dispatch-floor comparison): polling a coherent host
  * word returns sooner than a stream synchronisation does. */
 RRA_API rra_status rra_attend_wait(const void* qp, const void* kp, const void* vp,
