@@ -92,3 +92,39 @@ def test_status_strings(L):
     for s, name in enumerate(["RRA_OK", "RRA_ERR_INVALID_ARG", "RRA_ERR_UNSUPPORTED", "RRA_ERR_MISALIGNED",
                               "RRA_ERR_CUDA", "RRA_ERR_DEVICE"]):
         assert L.rra_status_string(s).decode() == name
+
+
+def test_host_side_errors_of_the_later_entry_points(L):
+    # rra_repack: shape, null, alignment and overlap checks, all before any CUDA call.
+    def repack(**kw):
+        a = dict(keep=0x100, dst=0x200, B=2, N=197, H=6, d=64, dt=rra.RRA_BF16, qp=0x10000, kp=0x20000,
+                 vp=0x30000, cu=0x300, di=0x400, si=0x500, q2=0x1000000, k2=0x2000000, v2=0x3000000)
+        a.update(kw)
+        return L.rra_repack(a["keep"], a["dst"], a["B"], a["N"], a["H"], a["d"], a["dt"], a["qp"], a["kp"],
+                            a["vp"], a["cu"], a["di"], a["si"], a["q2"], a["k2"], a["v2"], None)
+    assert repack(d=32) == rra.RRA_ERR_UNSUPPORTED
+    assert repack(keep=None) == rra.RRA_ERR_INVALID_ARG
+    assert repack(dst=None) == rra.RRA_ERR_INVALID_ARG
+    assert repack(si=None) == rra.RRA_ERR_INVALID_ARG
+    assert repack(kp=0x20008) == rra.RRA_ERR_MISALIGNED
+    assert repack(dt=rra.RRA_F32) == rra.RRA_ERR_INVALID_ARG
+    assert repack(q2=0x10000 + 256) == rra.RRA_ERR_INVALID_ARG            # new rows overlap the previous ones
+    assert b"overlap" in L.rra_last_error_message()
+    # rra_attend_wait takes rra_attend's checks first.
+    def wait(**kw):
+        a = dict(qp=0x1000, kp=0x2000, vp=0x3000, cu=0x4000, B=2, S=197, H=6, d=64, scale=0.125,
+                 ind=rra.RRA_BF16, o=0x5000, outd=rra.RRA_BF16)
+        a.update(kw)
+        return L.rra_attend_wait(a["qp"], a["kp"], a["vp"], a["cu"], a["B"], a["S"], a["H"], a["d"], a["scale"],
+                                 a["ind"], a["o"], a["outd"], None, 0, None)
+    assert wait(d=32) == rra.RRA_ERR_UNSUPPORTED
+    assert wait(qp=None) == rra.RRA_ERR_INVALID_ARG
+    assert wait(o=0x5004) == rra.RRA_ERR_MISALIGNED
+    assert wait(scale=float("inf")) == rra.RRA_ERR_INVALID_ARG
+    buf = (ctypes.c_double * 1)()
+    assert L.rra_time_attend_wait_host(0x1000, 0x2000, 0x3000, 0x4000, 2, 197, 6, 64, 0.125, rra.RRA_BF16,
+                                       0x5000, rra.RRA_BF16, None, 0, None, 0, 0, buf) == rra.RRA_ERR_INVALID_ARG
+    # rra_pipeline_mapped: a null host buffer is refused by name.
+    st = L.rra_pipeline_mapped(None, 0x1000, 0x2000, 0x3000, 2, 197, 6, 64, 0.125, rra.RRA_BF16, 0x5000,
+                               rra.RRA_BF16, 0x6000, 1 << 30, None)
+    assert st == rra.RRA_ERR_INVALID_ARG and b"keep_h" in L.rra_last_error_message()
