@@ -2,8 +2,10 @@
 from .ragged_attention import (  # noqa: F401
     attend,
     attend_row,
+    cls_scores,
     pack_indices,
     pack_rows,
     pipeline,
+    topk_keep,
     unpack,
 )

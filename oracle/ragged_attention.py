@@ -36,6 +36,8 @@ tensor, closed forms, invariants, and an exact sympy evaluation).
 """
 from __future__ import annotations
 
+import math
+
 import numpy as np
 
 
@@ -140,3 +142,63 @@ def pipeline(keep, q, k, v, scale):
     vp = pack_rows(np.asarray(v, dtype=np.float64), src)
     op = attend(qp, kp, vp, cu, scale)
     return unpack(op, dst, B, N), cu, dst, src
+
+
+# ----------------------------------------------------------------------------
+# The step before the path: a token-pruning decision made on the device.
+#
+# The abstract (both revisions) names EViT among the pruners the pipeline
+# serves; the pages do not describe its rule.  The reading taken here is the
+# plainest one consistent with "keep the tokens the class token attends to":
+#   * an image's class token is its first kept token (position 0 in the
+#     configurations, which always keep it);
+#   * a kept token's score is the class token's softmax attention weight on
+#     it, averaged over the heads;
+#   * a pruning step keeps the class token and the top ceil(m * num / den)
+#     of the image's m other kept tokens by score, equal scores going to the
+#     lower position (NaN scores rank below every number).
+
+
+def cls_scores(qp, kp, cu_seqlens, src_idx, N, scale):
+    """[B, N] fp64: for image b, the attention weights of its first kept token
+    (packed row cu[b]) over the image's kept tokens, averaged over heads, at
+    the tokens' original positions; 0 at positions with no kept token."""
+    qp = np.asarray(qp, dtype=np.float64)
+    kp = np.asarray(kp, dtype=np.float64)
+    T, H, d = qp.shape
+    B = len(cu_seqlens) - 1
+    out = np.zeros((B, N), dtype=np.float64)
+    for b in range(B):
+        s0, s1 = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+        if s1 <= s0:
+            continue
+        acc = np.zeros(s1 - s0, dtype=np.float64)
+        for h in range(H):
+            s = scale * (kp[s0:s1, h, :] @ qp[s0, h, :])
+            p = np.exp(s - s.max())
+            acc += p / p.sum()
+        for t in range(s0, s1):
+            out[b, int(src_idx[t]) - b * N] = acc[t - s0] / H
+    return out
+
+
+def topk_keep(scores, keep_prev, num, den):
+    """[B, N] uint8: each image's first kept token plus the top
+    ceil(m * num / den) of its m other kept tokens by score (descending,
+    equal scores to the lower position, NaN below every number)."""
+    scores = np.asarray(scores, dtype=np.float64)
+    keep_prev = np.asarray(keep_prev)
+    B, N = keep_prev.shape
+    out = np.zeros((B, N), dtype=np.uint8)
+    for b in range(B):
+        kept = [j for j in range(N) if keep_prev[b, j] != 0]
+        if not kept:
+            continue
+        out[b, kept[0]] = 1
+        others = kept[1:]
+        m = len(others)
+        k = (m * num + den - 1) // den
+        key = lambda j: (-(scores[b, j]) if scores[b, j] == scores[b, j] else math.inf, j)
+        for j in sorted(others, key=key)[:k]:
+            out[b, j] = 1
+    return out
