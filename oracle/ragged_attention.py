@@ -156,7 +156,7 @@ def pipeline(keep, q, k, v, scale):
 #     it, averaged over the heads;
 #   * a pruning step keeps the class token and the top ceil(m * num / den)
 #     of the image's m other kept tokens by score, equal scores going to the
-#     lower position (NaN scores rank below every number).
+#     lower position (a NaN score counts as -inf).
 
 
 def cls_scores(qp, kp, cu_seqlens, src_idx, N, scale):
@@ -185,7 +185,7 @@ def cls_scores(qp, kp, cu_seqlens, src_idx, N, scale):
 def topk_keep(scores, keep_prev, num, den):
     """[B, N] uint8: each image's first kept token plus the top
     ceil(m * num / den) of its m other kept tokens by score (descending,
-    equal scores to the lower position, NaN below every number)."""
+    equal scores to the lower position, a NaN score counting as -inf)."""
     scores = np.asarray(scores, dtype=np.float64)
     keep_prev = np.asarray(keep_prev)
     B, N = keep_prev.shape
@@ -198,7 +198,7 @@ def topk_keep(scores, keep_prev, num, den):
         others = kept[1:]
         m = len(others)
         k = (m * num + den - 1) // den
-        key = lambda j: (-(scores[b, j]) if scores[b, j] == scores[b, j] else math.inf, j)
+        key = lambda j: (-(scores[b, j]) if scores[b, j] == scores[b, j] else math.inf, j)   # NaN -> -inf
         for j in sorted(others, key=key)[:k]:
             out[b, j] = 1
     return out

@@ -123,13 +123,15 @@ def test_topk_is_the_best_subset_by_brute_force():
         assert set(np.nonzero(out[0])[0]) == {0, *best}
 
 
-def test_topk_nan_ranks_last():
+def test_topk_nan_counts_as_minus_infinity():
     keep = np.ones((1, 6), dtype=np.uint8)
     scores = np.array([[0.0, np.nan, 0.2, np.nan, 0.1, 0.3]])
     out = oracle.topk_keep(scores, keep, 3, 5)        # m = 5, k = 3
     assert list(np.nonzero(out[0])[0]) == [0, 2, 4, 5]
     out = oracle.topk_keep(scores, keep, 4, 5)        # k = 4: the first NaN position
     assert list(np.nonzero(out[0])[0]) == [0, 1, 2, 4, 5]
+    tie = np.array([[0.0, np.nan, -np.inf, 5.0]])     # NaN and -inf tie; the lower position wins
+    assert list(np.nonzero(oracle.topk_keep(tie, np.ones((1, 4), np.uint8), 2, 3)[0])[0]) == [0, 1, 3]
 
 
 def test_topk_reproduces_the_workload_generators_rule():
