@@ -130,6 +130,27 @@ RRA_API rra_status rra_repack(const uint8_t* keep_new, const int32_t* dst_prev, 
                               const void* vp_prev, int32_t* cu_seqlens, int32_t* dst_idx,
                               int32_t* src_idx, void* qp, void* kp, void* vp, void* stream);
 
+/* The step before the path, on the device (an EViT-like pruner; the
+ * abstract names EViT among the pruners the pipeline serves but does not
+ * spell out its rule).  Reading: an image's class token is its first kept
+ * token; a kept token's score is the class token's softmax attention weight
+ * on it (scale * <q_cls, k_j> over the image's kept tokens), averaged over
+ * the heads.
+ *   rra_cls_scores: packed q/k [cap, H, d] with cu_seqlens and src_idx (as
+ *   rra_pack writes them) -> scores float [B, N] at the original positions,
+ *   0 where no token is kept.  fp32 arithmetic.  One launch.
+ *   rra_topk_keep: keep_new [B, N] = each image's first kept token of
+ *   keep_prev plus the top ceil(m * keep_num / keep_den) of its m other
+ *   kept tokens by score; equal scores go to the lower position, a NaN score
+ *   counts as -inf.  0 <= keep_num <= keep_den, keep_prev and keep_new must
+ *   not overlap (else RRA_ERR_INVALID_ARG).  One launch; O(N^2) comparisons
+ *   per image (N <= 1024). */
+RRA_API rra_status rra_cls_scores(const void* qp, const void* kp, const int32_t* cu_seqlens,
+                                  const int32_t* src_idx, int B, int N, int H, int d, float scale,
+                                  rra_dtype in_dtype, float* scores, void* stream);
+RRA_API rra_status rra_topk_keep(const float* scores, const uint8_t* keep_prev, int B, int N, int keep_num,
+                                 int keep_den, uint8_t* keep_new, void* stream);
+
 /* Bidirectional ragged attention on packed buffers (method overview,
  * bullet 2; abstract).  For image b with rows s = cu[b] .. e = cu[b+1]-1 and
  * head h, for every row i in [s, e]:

@@ -479,6 +479,44 @@ rra_status rra_repack(const uint8_t* keep_new, const int32_t* dst_prev, int B, i
   return RRA_OK;
 }
 
+rra_status rra_cls_scores(const void* qp, const void* kp, const int32_t* cu_seqlens, const int32_t* src_idx,
+                          int B, int N, int H, int d, float scale, rra_dtype in_dtype, float* scores,
+                          void* stream) {
+  RRA_TRY(check_shape(B, N, H, d));
+  if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
+  if (!finite(scale)) return fail(RRA_ERR_INVALID_ARG, "scale is not finite");
+  RRA_CHECK_PTR(qp);
+  RRA_CHECK_PTR(kp);
+  if (cu_seqlens == nullptr || src_idx == nullptr || scores == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "cu_seqlens, src_idx or scores is null");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  cudaError_t e = launch_cls_scores(qp, kp, cu_seqlens, src_idx, B, N, H, scale, in_dtype, scores, st->err,
+                                    static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "cls_scores launch");
+  g_launches += 1;
+  return RRA_OK;
+}
+
+rra_status rra_topk_keep(const float* scores, const uint8_t* keep_prev, int B, int N, int keep_num, int keep_den,
+                         uint8_t* keep_new, void* stream) {
+  RRA_TRY(check_shape(B, N, 1, 64));
+  if (scores == nullptr || keep_prev == nullptr || keep_new == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "scores, keep_prev or keep_new is null");
+  if (keep_den < 1 || keep_num < 0 || keep_num > keep_den)
+    return fail(RRA_ERR_INVALID_ARG, "keep fraction %d/%d outside [0, 1]", keep_num, keep_den);
+  const uintptr_t a0 = reinterpret_cast<uintptr_t>(keep_prev), b0 = reinterpret_cast<uintptr_t>(keep_new);
+  const size_t bytes = static_cast<size_t>(B) * N;
+  if (a0 < b0 + bytes && b0 < a0 + bytes) return fail(RRA_ERR_INVALID_ARG, "keep_prev and keep_new overlap");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  cudaError_t e = launch_topk_keep(scores, keep_prev, B, N, keep_num, keep_den, keep_new,
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "topk_keep launch");
+  g_launches += 1;
+  return RRA_OK;
+}
+
 rra_status rra_attend(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens,
                       int B, int max_seqlen, int H, int d, float scale, rra_dtype in_dtype, void* o,
                       rra_dtype out_dtype, const int32_t* src_idx, int N, void* stream) {

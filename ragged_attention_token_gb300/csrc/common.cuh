@@ -106,6 +106,12 @@ cudaError_t launch_pack(const PackArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_attend(const AttendArgs& a, rra_dtype in, rra_dtype out, cudaStream_t stream,
                           uint32_t* ctas = nullptr);
 cudaError_t launch_unpack(const UnpackArgs& a, cudaStream_t stream);
+// Device-side pruning step: class-token attention scores [B, N] and the
+// top-k keep decision (one CTA per image each).
+cudaError_t launch_cls_scores(const void* qp, const void* kp, const int32_t* cu, const int32_t* src, int B, int N,
+                              int H, float scale, rra_dtype in, float* scores, int32_t* err, cudaStream_t stream);
+cudaError_t launch_topk_keep(const float* scores, const uint8_t* keep_prev, int B, int N, int num, int den,
+                             uint8_t* keep_new, cudaStream_t stream);
 // tcgen05 + TMA attention; needs the driver's tensor-map encoder.
 bool attend_tc_available();
 cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream,

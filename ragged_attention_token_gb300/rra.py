@@ -36,6 +36,8 @@ _SIGNATURES = {
     "rra_pack": (_i, [_vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i, _vp]),
     "rra_attend": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp]),
     "rra_repack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
+    "rra_cls_scores": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "rra_topk_keep": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "rra_attend_gather": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "rra_unpack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "rra_pipeline": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
@@ -162,6 +164,22 @@ def repack(keep_new, dst_prev, qp_prev, kp_prev, vp_prev, cu_seqlens, dst_idx, s
     _check(lib().rra_repack(_ptr(keep_new), _ptr(dst_prev), B, N, H, d, _DTYPE[qp_prev.dtype], _ptr(qp_prev),
                             _ptr(kp_prev), _ptr(vp_prev), _ptr(cu_seqlens), _ptr(dst_idx), _ptr(src_idx),
                             _ptr(qp), _ptr(kp), _ptr(vp), _stream(stream)))
+
+
+def cls_scores(qp, kp, cu_seqlens, src_idx, B: int, N: int, scores, scale: float = 0.125, stream=None):
+    """rra_cls_scores: the class token's attention over each image's kept tokens, head mean, [B, N] fp32."""
+    H, d = qp.shape[-2], qp.shape[-1]
+    if scores.dtype != torch.float32:
+        raise ValueError("scores must be float32")
+    _check(lib().rra_cls_scores(_ptr(qp), _ptr(kp), _ptr(cu_seqlens), _ptr(src_idx), B, N, H, d, float(scale),
+                                _DTYPE[qp.dtype], _ptr(scores), _stream(stream)))
+
+
+def topk_keep(scores, keep_prev, keep_num: int, keep_den: int, keep_new, stream=None):
+    """rra_topk_keep: the class token plus the top ceil(m*num/den) other kept tokens by score."""
+    B, N = keep_prev.shape
+    _check(lib().rra_topk_keep(_ptr(scores), _ptr(keep_prev), B, N, int(keep_num), int(keep_den), _ptr(keep_new),
+                               _stream(stream)))
 
 
 def attend(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, scale: float = 0.125,
