@@ -675,6 +675,31 @@ def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
     return line
 
 
+def device_pruning_times(rra, stream, B=256, reps=10):
+    """One pruning step of the progressive workload on the device (layer 3 -> 4 at batch B):
+    class-token scores from layer 3's packed Q/K, then the 70% top-k keep decision."""
+    dev = torch.device("cuda", 0)
+    masks, cases = W.make_progressive_chain(B)
+    c = cases[2]
+    keep, q, k, v = (x.to(dev) for x in (c.keep, c.q, c.k, c.v))
+    N, H, d = c.N, c.H, c.d
+    cu = torch.empty(B + 1, dtype=torch.int32, device=dev)
+    dst = torch.empty(B * N, dtype=torch.int32, device=dev)
+    src = torch.empty(B * N, dtype=torch.int32, device=dev)
+    qp, kp, vp = (torch.empty((B * N, H, d), dtype=c.dtype, device=dev) for _ in range(3))
+    rra.pack(keep, q, k, v, cu, dst, src, qp, kp, vp, stream=stream)
+    scores = torch.empty((B, N), dtype=torch.float32, device=dev)
+    keep_new = torch.empty_like(keep)
+    # graphs of 20 back-to-back launches (the inputs stay in L2 between them)
+    t_scores = graph_time_per_launch([lambda: rra.cls_scores(qp, kp, cu, src, B, N, scores, scale=SCALE,
+                                                             stream=stream)] * 20, stream, reps)
+    t_topk = graph_time_per_launch([lambda: rra.topk_keep(scores, keep, 7, 10, keep_new, stream=stream)] * 20,
+                                   stream, reps)
+    return {"case": f"device_pruning_B{B}", "B": B, "N": N, "H": H, "kept_before": int((c.keep != 0).sum()),
+            "kept_after": int((keep_new != 0).sum()), "cls_scores_us": round(t_scores, 2),
+            "topk_keep_us": round(t_topk, 2)}
+
+
 def run_sweep(args):
     """Every workload: device µs per kernel, path tokens/s, roofline (one JSON line each)."""
     from ragged_attention_token_gb300 import build as _build
@@ -705,6 +730,7 @@ def run_sweep(args):
         print(json.dumps(line), flush=True)
         del sets
     print(json.dumps(progressive_chain_times(rra, stream, peaks)), flush=True)
+    print(json.dumps(device_pruning_times(rra, stream)), flush=True)
     return 0
 
 
