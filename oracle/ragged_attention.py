@@ -202,3 +202,20 @@ def topk_keep(scores, keep_prev, num, den):
         for j in sorted(others, key=key)[:k]:
             out[b, j] = 1
     return out
+
+
+# ----------------------------------------------------------------------------
+# The rest of a ViT block on the compact buffer: a linear layer over the
+# packed rows only (the article's problem section: padding wastes masked
+# multiplies; packing removes them from every layer, not only attention).
+
+
+def linear_packed(a, w, bias, T):
+    """fp64 [T, N]: rows t < T of the packed [cap, K] matrix a times w^T
+    ([N, K], the nn.Linear layout), plus bias [N] when given."""
+    a = np.asarray(a, dtype=np.float64)[: int(T)]
+    w = np.asarray(w, dtype=np.float64)
+    out = a @ w.T
+    if bias is not None:
+        out = out + np.asarray(bias, dtype=np.float64)[None, :]
+    return out
