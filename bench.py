@@ -250,8 +250,8 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
 # capture of the same launches (dram__bytes_read.sum + dram__bytes_write.sum).  They
 # describe the kernel source whose SHA-256 starts with TRAFFIC_SRC_SHA; once that file
 # changes the traffic is reported as null until it is captured again.
-TRAFFIC_SRC_SHA = "995dcc5285738e7e"
-TRAFFIC_BYTES = {"serving_B4": 430730, "batched_b64_p80": 11921664}
+TRAFFIC_SRC_SHA = "84f8ec8241cdb73e"
+TRAFFIC_BYTES = {"serving_B4": 430587, "batched_b64_p80": 11922603}
 
 
 def measured_traffic(key):
@@ -700,6 +700,47 @@ def device_pruning_times(rra, stream, B=256, reps=10):
             "topk_keep_us": round(t_topk, 2)}
 
 
+def linear_times(rra, stream, peaks, reps=10):
+    """Packed QKV projection of the batched DeiT-B workload (K=768 -> N=2304) with
+    rra_linear_packed: over the kept rows only (T from cu_seqlens on the device)
+    at 80% and 0% pruning, and over every padded row; torch's cuBLAS GEMM on the
+    same rows for context."""
+    dev = torch.device("cuda", 0)
+    K, Nout = 768, 2304
+    g = torch.Generator().manual_seed(2024)
+    w = (torch.randn((Nout, K), generator=g) / math.sqrt(K)).to(torch.bfloat16).to(dev)
+    bias = torch.randn((Nout,), generator=g).to(dev)
+    lines = []
+    for rate in (0.8, 0.0):
+        case = W.make_batched(rate)
+        cap = case.B * case.N
+        T = case.kept_tokens
+        a = torch.randn((cap, K), generator=g).to(torch.bfloat16).to(dev)
+        c = torch.empty((cap, Nout), dtype=torch.bfloat16, device=dev)
+        cu_kept = torch.tensor([0, T], dtype=torch.int32, device=dev)
+        cu_all = torch.tensor([0, cap], dtype=torch.int32, device=dev)
+        t_kept = graph_time_per_launch([lambda: rra.linear_packed(a, w, cu_kept, 1, c, bias=bias, stream=stream)] * 10,
+                                       stream, reps)
+        t_all = graph_time_per_launch([lambda: rra.linear_packed(a, w, cu_all, 1, c, bias=bias, stream=stream)] * 10,
+                                      stream, reps)
+        a_t = a[:T]
+        bias_lp = bias.to(torch.bfloat16)
+
+        def cublas():
+            with torch.cuda.stream(stream):
+                torch.nn.functional.linear(a_t, w, bias_lp)
+        t_cublas = graph_time_per_launch([cublas] * 10, stream, reps)
+        flops = 2.0 * T * K * Nout
+        peak = peaks.get("bf16_tflops")
+        lines.append({"case": f"linear_packed_qkv_b64_p{int(rate * 100)}", "T": T, "rows_padded": cap, "K": K,
+                      "N": Nout, "packed_us": round(t_kept, 2), "padded_rows_us": round(t_all, 2),
+                      "cublas_packed_us": round(t_cublas, 2),
+                      "tflops": round(flops / (t_kept * 1e-6) / 1e12, 1), "peak_tflops": peak,
+                      "frac": round(flops / (t_kept * 1e-6) / 1e12 / peak, 4) if peak else None})
+        del a, c
+    return lines
+
+
 def run_sweep(args):
     """Every workload: device µs per kernel, path tokens/s, roofline (one JSON line each)."""
     from ragged_attention_token_gb300 import build as _build
@@ -731,6 +772,8 @@ def run_sweep(args):
         del sets
     print(json.dumps(progressive_chain_times(rra, stream, peaks)), flush=True)
     print(json.dumps(device_pruning_times(rra, stream)), flush=True)
+    for line in linear_times(rra, stream, peaks):
+        print(json.dumps(line), flush=True)
     return 0
 
 

@@ -130,6 +130,22 @@ RRA_API rra_status rra_repack(const uint8_t* keep_new, const int32_t* dst_prev, 
                               const void* vp_prev, int32_t* cu_seqlens, int32_t* dst_idx,
                               int32_t* src_idx, void* qp, void* kp, void* vp, void* stream);
 
+/* Packed linear layer: the rest of a ViT block (QKV projection, output
+ * projection, MLP) on the compact buffer, so pruned tokens cost no multiplies
+ * there either (article, problem section: padding wastes bandwidth and
+ * masked work).  c[t, :] = a[t, :] W^T (+ bias) for t < T = cu_seqlens[B],
+ * T read on the device; rows t >= T of c are not written.
+ *   a    [cap, K] of in_dtype (F16 or BF16), the packed rows;
+ *   w    [N, K] of in_dtype (the nn.Linear weight layout);
+ *   bias float [N] or NULL (16-byte aligned);
+ *   c    [cap, N] of out_dtype (F16, BF16 or F32).
+ * K a multiple of 64, N a multiple of 128 (else RRA_ERR_UNSUPPORTED); fp32
+ * accumulation (tcgen05, TMEM).  One launch; a cu_seqlens[B] outside
+ * [0, cap] records RRA_DEVERR_INDEX_RANGE and writes nothing. */
+RRA_API rra_status rra_linear_packed(const void* a, const void* w, const float* bias, const int32_t* cu_seqlens,
+                                     int B, int cap, int K, int N, rra_dtype in_dtype, void* c,
+                                     rra_dtype out_dtype, void* stream);
+
 /* The step before the path, on the device (an EViT-like pruner; the
  * abstract names EViT among the pruners the pipeline serves but does not
  * spell out its rule).  Reading: an image's class token is its first kept

@@ -479,6 +479,30 @@ rra_status rra_repack(const uint8_t* keep_new, const int32_t* dst_prev, int B, i
   return RRA_OK;
 }
 
+rra_status rra_linear_packed(const void* a, const void* w, const float* bias, const int32_t* cu_seqlens, int B,
+                             int cap, int K, int N, rra_dtype in_dtype, void* c, rra_dtype out_dtype,
+                             void* stream) {
+  if (B < 1 || B > 65535) return fail(RRA_ERR_INVALID_ARG, "B=%d outside [1, 65535]", B);
+  if (cap < 1 || cap > 65535 * 128) return fail(RRA_ERR_INVALID_ARG, "cap=%d outside [1, 65535*128]", cap);
+  if (K < 64 || K % 64 != 0 || K > 16384) return fail(RRA_ERR_UNSUPPORTED, "K=%d: a multiple of 64 up to 16384", K);
+  if (N < 128 || N % 128 != 0 || N > 65535 * 128)
+    return fail(RRA_ERR_UNSUPPORTED, "N=%d: a multiple of 128", N);
+  if (!valid_in(in_dtype)) return fail(RRA_ERR_INVALID_ARG, "input dtype invalid");
+  if (!valid_out(out_dtype)) return fail(RRA_ERR_INVALID_ARG, "output dtype invalid");
+  RRA_CHECK_PTR(a);
+  RRA_CHECK_PTR(w);
+  RRA_CHECK_PTR(c);
+  if (cu_seqlens == nullptr) return fail(RRA_ERR_INVALID_ARG, "cu_seqlens is null");
+  if (bias != nullptr && !aligned16(bias)) return fail(RRA_ERR_MISALIGNED, "bias not 16-byte aligned");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  cudaError_t e = launch_linear_packed(a, w, bias, cu_seqlens, B, cap, K, N, in_dtype, c, out_dtype, st->err,
+                                       static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "linear_packed launch");
+  g_launches += 1;
+  return RRA_OK;
+}
+
 rra_status rra_cls_scores(const void* qp, const void* kp, const int32_t* cu_seqlens, const int32_t* src_idx,
                           int B, int N, int H, int d, float scale, rra_dtype in_dtype, float* scores,
                           void* stream) {

@@ -106,6 +106,11 @@ cudaError_t launch_pack(const PackArgs& a, int num_sms, cudaStream_t stream);
 cudaError_t launch_attend(const AttendArgs& a, rra_dtype in, rra_dtype out, cudaStream_t stream,
                           uint32_t* ctas = nullptr);
 cudaError_t launch_unpack(const UnpackArgs& a, cudaStream_t stream);
+// Packed linear layer on the tensor cores: c[t] = a[t] W^T (+ bias) for the
+// T = cu[B] kept rows (T read on the device).
+cudaError_t launch_linear_packed(const void* a, const void* w, const float* bias, const int32_t* cu, int B,
+                                 int cap, int K, int N, rra_dtype in, void* c, rra_dtype out, int32_t* err,
+                                 cudaStream_t stream);
 // Device-side pruning step: class-token attention scores [B, N] and the
 // top-k keep decision (one CTA per image each).
 cudaError_t launch_cls_scores(const void* qp, const void* kp, const int32_t* cu, const int32_t* src, int B, int N,

@@ -37,6 +37,7 @@ _SIGNATURES = {
     "rra_attend": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp]),
     "rra_repack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "rra_cls_scores": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _vp]),
+    "rra_linear_packed": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "rra_topk_keep": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "rra_attend_gather": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "rra_unpack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
@@ -164,6 +165,16 @@ def repack(keep_new, dst_prev, qp_prev, kp_prev, vp_prev, cu_seqlens, dst_idx, s
     _check(lib().rra_repack(_ptr(keep_new), _ptr(dst_prev), B, N, H, d, _DTYPE[qp_prev.dtype], _ptr(qp_prev),
                             _ptr(kp_prev), _ptr(vp_prev), _ptr(cu_seqlens), _ptr(dst_idx), _ptr(src_idx),
                             _ptr(qp), _ptr(kp), _ptr(vp), _stream(stream)))
+
+
+def linear_packed(a, w, cu_seqlens, B: int, c, bias=None, stream=None):
+    """rra_linear_packed: c[t] = a[t] @ w.T (+ bias) for the T = cu_seqlens[B] packed rows."""
+    cap, K = a.shape
+    N = w.shape[0]
+    if bias is not None and bias.dtype != torch.float32:
+        raise ValueError("bias must be float32")
+    _check(lib().rra_linear_packed(_ptr(a), _ptr(w), _ptr(bias), _ptr(cu_seqlens), B, cap, K, N, _DTYPE[a.dtype],
+                                   _ptr(c), _DTYPE[c.dtype], _stream(stream)))
 
 
 def cls_scores(qp, kp, cu_seqlens, src_idx, B: int, N: int, scores, scale: float = 0.125, stream=None):
