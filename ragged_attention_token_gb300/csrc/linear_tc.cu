@@ -12,8 +12,9 @@
 // K step reads both straight from 128-byte-swizzled shared memory.
 //
 // One CTA per 128 x 128 output tile; a tile whose first row is past T
-// returns at once.  Warp 0 streams 64-wide K chunks of the A and W tiles
-// through a 4-stage TMA ring; warp 1 (which also owns the 128 TMEM columns
+// returns at once; two CTAs share an SM, so one's epilogue overlaps the
+// other's products.  Warp 0 streams 64-wide K chunks of the A and W tiles
+// through a 3-stage TMA ring; warp 1 (which also owns the 128 TMEM columns
 // of the fp32 accumulator) issues the MMAs from converged code with
 // elect.sync and commits each stage back to the producer; warps 2-5 read the
 // accumulator (each its TMEM lane quadrant), add the bias and store their
@@ -31,7 +32,7 @@ namespace {
 constexpr int LM = 128;                                  // output rows per tile (TMEM lanes)
 constexpr int LN = 128;                                  // output columns per tile (TMEM columns)
 constexpr int LK = 64;                                   // K per stage (one 128-byte swizzled row)
-constexpr int L_STAGES = 4;
+constexpr int L_STAGES = 3;                              // 96 KB ring: two CTAs per SM
 constexpr int L_THREADS = 192;
 constexpr uint32_t L_A_BYTES = LM * 128;
 constexpr uint32_t L_W_BYTES = LN * 128;
@@ -101,7 +102,7 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
 }
 
 template <typename Tin, typename Tout>
-__global__ void __launch_bounds__(L_THREADS, 1)
+__global__ void __launch_bounds__(L_THREADS, 2)
     linear_tc_kernel(const __grid_constant__ CUtensorMap map_a, const __grid_constant__ CUtensorMap map_w,
                      const LinearArgs a) {
   extern __shared__ uint8_t smem_raw[];
