@@ -128,3 +128,32 @@ def test_host_side_errors_of_the_later_entry_points(L):
     st = L.rra_pipeline_mapped(None, 0x1000, 0x2000, 0x3000, 2, 197, 6, 64, 0.125, rra.RRA_BF16, 0x5000,
                                rra.RRA_BF16, 0x6000, 1 << 30, None)
     assert st == rra.RRA_ERR_INVALID_ARG and b"keep_h" in L.rra_last_error_message()
+
+
+def test_host_side_errors_of_the_next_step_entry_points(L):
+    # rra_cls_scores / rra_topk_keep
+    st = L.rra_cls_scores(0x1000, 0x2000, 0x300, 0x400, 2, 197, 6, 32, 0.125, rra.RRA_BF16, 0x5000, None)
+    assert st == rra.RRA_ERR_UNSUPPORTED
+    st = L.rra_cls_scores(0x1000, 0x2000, None, 0x400, 2, 197, 6, 64, 0.125, rra.RRA_BF16, 0x5000, None)
+    assert st == rra.RRA_ERR_INVALID_ARG
+    st = L.rra_cls_scores(0x1008, 0x2000, 0x300, 0x400, 2, 197, 6, 64, 0.125, rra.RRA_BF16, 0x5000, None)
+    assert st == rra.RRA_ERR_MISALIGNED
+    assert L.rra_topk_keep(0x1000, 0x2000, 2, 197, 8, 7, 0x9000, None) == rra.RRA_ERR_INVALID_ARG   # num > den
+    assert L.rra_topk_keep(0x1000, 0x2000, 2, 197, 1, 0, 0x9000, None) == rra.RRA_ERR_INVALID_ARG   # den = 0
+    assert L.rra_topk_keep(0x1000, 0x2000, 2, 197, 7, 10, 0x2010, None) == rra.RRA_ERR_INVALID_ARG  # overlap
+    assert b"overlap" in L.rra_last_error_message()
+    assert L.rra_topk_keep(None, 0x2000, 2, 197, 7, 10, 0x9000, None) == rra.RRA_ERR_INVALID_ARG
+    # rra_linear_packed: K a multiple of 64, N a multiple of 128, alignment, null counts.
+    def lin(**kw):
+        a = dict(a=0x10000, w=0x20000, bias=None, cu=0x300, B=1, cap=512, K=384, N=1152,
+                 ind=rra.RRA_BF16, c=0x40000, outd=rra.RRA_F32)
+        a.update(kw)
+        return L.rra_linear_packed(a["a"], a["w"], a["bias"], a["cu"], a["B"], a["cap"], a["K"], a["N"],
+                                   a["ind"], a["c"], a["outd"], None)
+    assert lin(K=96) == rra.RRA_ERR_UNSUPPORTED
+    assert lin(N=192) == rra.RRA_ERR_UNSUPPORTED
+    assert lin(cu=None) == rra.RRA_ERR_INVALID_ARG
+    assert lin(cap=0) == rra.RRA_ERR_INVALID_ARG
+    assert lin(a=0x10008) == rra.RRA_ERR_MISALIGNED
+    assert lin(bias=0x50004) == rra.RRA_ERR_MISALIGNED
+    assert lin(ind=rra.RRA_F32) == rra.RRA_ERR_INVALID_ARG
