@@ -387,7 +387,7 @@ def run_reference(args, world, rank):
     oracle.pipeline(keep, q, k, v, SCALE)
     t_one = time.perf_counter() - t0
     steps = max(1, min(args.steps, int(120.0 / max(t_one, 1e-6))))   # about two minutes at most
-    warm = max(0, min(args.warmup, steps))
+    warm = max(0, min(args.warmup, int(60.0 / max(t_one, 1e-6)) + 1))   # as asked, within about a minute
     for _ in range(warm):
         oracle.pipeline(keep, q, k, v, SCALE)
     t0 = time.perf_counter()
