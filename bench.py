@@ -264,6 +264,18 @@ def measured_traffic(key):
     return TRAFFIC_BYTES.get(key) if ok else None
 
 
+def packed_qkvo_frac(case, us, peaks):
+    """Fraction of the attention roofline as stated for this problem: the slower of
+    the packed Q/K/V/O bytes (4*T*H*d*s) at the HBM peak and 4*H*d*sum(n_b^2)
+    FLOPs at the bf16 peak, over the measured time.  Smaller than the pipeline's
+    own byte count (which also writes every padded output row), so a pipeline
+    kernel reads lower against it."""
+    s = case.q.element_size()
+    t_bytes = 4 * case.kept_tokens * case.H * case.d * s / (peaks["hbm_gbs"] * 1e9)
+    t_flops = 4 * case.H * case.d * sum(n * n for n in case.lengths) / (peaks["bf16_tflops"] * 1e12)
+    return round(max(t_bytes, t_flops) * 1e6 / us, 4)
+
+
 def roofline_obj(bytes_alg, flops, us, peaks):
     t = us * 1e-6
     bw = bytes_alg / t / 1e9
@@ -557,6 +569,7 @@ def run_rra(args, world, rank, local):
         extra["batched_b64_p80"] = {"workload": big_desc, "fused_us": round(bk["fused_us"], 3),
                                     "roofline": {**roofline_obj(bb["fused_min"], bb["flops"], bk["fused_us"], peaks),
                                                  "traffic": measured_traffic("batched_b64_p80")},
+                                    "packed_qkvo_frac": packed_qkvo_frac(big, bk["fused_us"], peaks),
                                     "pipeline_tokens_per_s": round(big.kept_tokens / (bk["fused_us"] * 1e-6), 1)}
         del big_sets
 
@@ -765,6 +778,8 @@ def run_sweep(args):
         line = {"case": case.name, "B": case.B, "N": case.N, "H": case.H, "T": case.kept_tokens,
                 **{k: round(v, 3) for k, v in kt.items()},
                 "fused_min_us": round(fused_min_t, 3), "fused_frac": round(fused_min_t / kt["fused_us"], 4),
+                "packed_qkvo_frac": {"fused": packed_qkvo_frac(case, kt["fused_us"], peaks),
+                                     "attend_packed_tc": packed_qkvo_frac(case, kt["attend_packed_tc_us"], peaks)},
                 "fused": roofline_obj(by["fused_min"], by["flops"], kt["fused_us"], peaks),
                 "two_launch_mma_us": round(two, 3),
                 "fused_tokens_per_s": round(case.kept_tokens / (kt["fused_us"] * 1e-6), 1)}
