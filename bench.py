@@ -79,7 +79,7 @@ def case_bytes(case, out_bytes_per_el=None):
         attend=3 * T * H * d * s + T * H * d * so,
         index=B * N + (B * N - T) * H * d * so + 4 * (B + 1) + 4 * B * N + 4 * T,
         pack=B * N + 2 * 3 * T * H * d * s + (B * N - T) * H * d * so + 4 * (B + 1) + 4 * B * N + 4 * T,
-        fused_min=B * N + 3 * T * H * d * s + B * N * H * d * so + 12 * B * N,
+        fused_min=B * N + 3 * T * H * d * s + B * N * H * d * so,   # the fused kernel writes no indices
         flops=4 * H * d * sum(n * n for n in case.lengths),
     )
 
