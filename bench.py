@@ -327,9 +327,13 @@ def host_latency(rra, B, stream, reps=1000, warmup=100):
 
 # ----------------------------------------------------------------- CPU side
 
-def oracle_tokens_per_s(case, budget_s=10.0):
-    """The CPU oracle (as it stands) on the workload: kept tokens/s on this host."""
+def oracle_legs(case, budget_s=10.0):
+    """The CPU oracle (as it stands) on the workload, on this host: kept tokens/s
+    on one thread (in this process, BLAS pinned to one thread above) and on every
+    core of the affinity mask (one worker process per core, each repeating full
+    steps of the same inputs; oracle/timing.py)."""
     import oracle
+    from oracle import timing as OT
     keep = case.keep.numpy()
     q, k, v = (x.double().numpy() for x in (case.q, case.k, case.v))
     T = case.kept_tokens
@@ -341,10 +345,21 @@ def oracle_tokens_per_s(case, budget_s=10.0):
         el = time.perf_counter() - t0
         if el >= budget_s:
             break
-    return T * steps / el, steps, el
+    one = {"value": round(T * steps / el, 1), "threads": 1, "steps": steps, "seconds": round(el, 2)}
+    cores = OT.host_cores()
+    allc = OT.time_pipeline(keep, q, k, v, SCALE, budget_s, cores)
+    every = {"value": round(allc["tokens_per_s"], 1), "threads": cores, "steps": allc["steps"],
+             "seconds": round(allc["window_s"], 2)}
+    return one, every, cores
 
 
-CPU_THREADS = 1   # single-threaded Python loops; BLAS pinned to one thread above
+def cpu_baseline_obj(case, budget_s=10.0):
+    one, every, cores = oracle_legs(case, budget_s)
+    return {"value": every["value"], "unit": UNIT, "cores": cores, "threads": every["threads"], "kind": "oracle",
+            "sample": (f"full steps of the same workload for ~{budget_s:.0f} s per leg: {every['steps']} steps on "
+                       f"{every['threads']} worker processes (one per core, fp64 numpy, BLAS 1 thread each) and "
+                       f"{one['steps']} steps on 1 thread"),
+            "legs": {"all_cores": every, "one_thread": one}}
 
 
 # -------------------------------------------------------------------- main
@@ -387,34 +402,49 @@ def max_over_ranks(x, world, device):
     return float(t.item())
 
 
+def workload_config(case, desc, world):
+    """The `config` object of both arms' JSON lines (identical for the same workload)."""
+    return {"workload": desc, "B": case.B, "N": case.N, "H": case.H, "d": case.d,
+            "kept_tokens_per_step": case.kept_tokens,
+            "path": "CUDA graphs of rra_pipeline steps on rotating input sets, replayed back to back",
+            "l2": "rotating input sets larger than 2x L2 in total: every step reads cold inputs",
+            "parallelism": f"replicas x{world}"}
+
+
 def run_reference(args, world, rank):
+    """The reference arm: the CPU oracle, as it stands, on this host's cores.
+
+    One worker process per core repeats full steps of the workload (images and
+    steps are independent, as on the GPU side) for about --cpu-budget seconds
+    (at least ceil(steps / cores) steps each, bounded to about two minutes)."""
     if rank != 0:
         return 0
     case, desc = make_case(args.workload)
     import oracle
+    from oracle import timing as OT
     keep = case.keep.numpy()
     q, k, v = (x.double().numpy() for x in (case.q, case.k, case.v))
     T = case.kept_tokens
     t0 = time.perf_counter()
     oracle.pipeline(keep, q, k, v, SCALE)
     t_one = time.perf_counter() - t0
-    steps = max(1, min(args.steps, int(120.0 / max(t_one, 1e-6))))   # about two minutes at most
-    warm = max(0, min(args.warmup, int(60.0 / max(t_one, 1e-6)) + 1))   # as asked, within about a minute
+    cores = OT.host_cores()
+    per_worker = max(1, math.ceil(args.steps / cores))
+    budget = min(120.0, max(args.cpu_budget, per_worker * t_one))
+    warm = max(0, min(args.warmup, int(60.0 / max(t_one, 1e-6)) + 1))
     for _ in range(warm):
         oracle.pipeline(keep, q, k, v, SCALE)
-    t0 = time.perf_counter()
-    for _ in range(steps):
-        oracle.pipeline(keep, q, k, v, SCALE)
-    el = time.perf_counter() - t0
-    value = T * steps / el
+    r = OT.time_pipeline(keep, q, k, v, SCALE, budget, cores)
+    value = r["tokens_per_s"]
+    steps = r["steps"]
     line = {
         "impl": "reference", "metric": METRIC, "value": round(value, 1), "unit": UNIT, "n_gpus": args.gpus,
-        "steps": steps, "warmup": warm, "ms_per_step": round(el / steps * 1e3, 3), "higher_is_better": True,
+        "steps": steps, "warmup": warm, "ms_per_step": round(T / value * 1e3, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": desc, "B": case.B, "N": case.N, "H": case.H, "d": case.d,
-                   "kept_tokens_per_step": T},
-        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": CPU_THREADS, "kind": "oracle",
-                         "sample": f"{steps} full steps of the workload (steps capped at ~2 min of CPU)"},
+        "config": workload_config(case, desc, world),
+        "cpu_baseline": {"value": round(value, 1), "unit": UNIT, "cores": cores, "threads": cores, "kind": "oracle",
+                         "sample": f"{steps} full steps of the workload on {cores} worker processes (one per core, "
+                                   f"fp64 numpy, BLAS 1 thread each) in {r['window_s']:.1f} s"},
         "e2e": {"value": round(value, 1), "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
         "gpu_launches": 0,
     }
@@ -575,9 +605,7 @@ def run_rra(args, world, rank, local):
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu:
-        tps, st, el = oracle_tokens_per_s(case, budget_s=args.cpu_budget)
-        cpu = {"value": round(tps, 1), "unit": UNIT, "cores": CPU_THREADS, "kind": "oracle",
-               "sample": f"{st} full steps of the same workload in {el:.1f} s (fp64 numpy, 1 thread)"}
+        cpu = cpu_baseline_obj(case, budget_s=args.cpu_budget)
 
     if rank == 0:
         line = {
@@ -585,11 +613,10 @@ def run_rra(args, world, rank, local):
             "warmup": max(3, args.warmup), "ms_per_step": round(el_ms / args.steps, 5), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if case.dtype == torch.bfloat16 else "f16",
             "data": "synthetic (seeded N(0,1) Q/K/V, seeded keep masks)",
-            "config": {"workload": desc, "B": B, "N": N, "H": H, "d": d, "kept_tokens_per_step": T,
-                       "path": f"CUDA graphs of {sets.R} rra_pipeline steps, replayed back to back",
+            "config": workload_config(case, desc, world),
+            "timing": {"graph": f"CUDA graphs of {sets.R} rra_pipeline steps, replayed back to back",
                        "l2": f"{sets.R} rotating input sets of {sets.per_set / 2**20:.1f} MiB "
-                             f"({sets.R * sets.per_set / 2**20:.0f} MiB > L2)",
-                       "parallelism": f"replicas x{world}"},
+                             f"({sets.R * sets.per_set / 2**20:.0f} MiB > L2)"},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms / args.steps, 5),
                     "path": "rra_pipeline_mapped (inputs and output in pinned host memory; pack + attend read the "

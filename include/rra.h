@@ -285,14 +285,24 @@ RRA_API rra_status rra_pipeline_mapped(const uint8_t* keep_h, const void* q_h, c
  * afford an allocation's implicit synchronisation -- and so cannot hand
  * rra_pipeline a workspace.  Same arguments and result as rra_pipeline
  * without the workspace: the scratch (cu_seqlens, pack indices, packed
- * Q/K/V) lives in one static device array of RRA_STATIC_SCRATCH_BYTES that
- * every GPU loading this library holds until the process exits.
+ * Q/K/V) lives in one static device array of RRA_STATIC_SCRATCH_BYTES.
+ *   - The array is taken on a device when the library's device code is
+ *     loaded there: under CUDA's default lazy module loading that is the
+ *     device's first rra_pipeline_static call (its address lookup below),
+ *     under eager loading when the library is loaded.  It is held until the
+ *     process exits.
+ *   - Of the workloads the paper's configurations describe, tiny, serving
+ *     (B <= 4) and batched B=64 (about 58 MB) fit; high-res B=32, N=577
+ *     (about 85 MB) and the progressive B=256 layers (about 116 MB) do not.
  *   - Allocates nothing and calls no allocating routine.
  *   - Sizes whose workspace (rra_workspace_bytes) exceeds the array return
  *     RRA_ERR_UNSUPPORTED with nothing enqueued.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture.
+ *     before any stream capture.  The address is cached per device for the
+ *     life of the process, like the rest of the library's per-device state
+ *     (see rra_get_device_error): after cudaDeviceReset on a device, do not
+ *     call this library on that device again in the same process.
  *   - All calls share the one array and it keeps the last call's contents
  *     (nothing in it has to start at zero).  Calls whose work overlaps on
  *     the GPU -- different streams without ordering between them -- race on

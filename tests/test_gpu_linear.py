@@ -81,3 +81,22 @@ def test_linear_packed_empty_and_bad_count():
     torch.cuda.synchronize()
     assert rra.get_device_error(clear=True) == rra.DEVERR_INDEX_RANGE
     assert bool(torch.isnan(c).all())
+
+
+@pytest.mark.parametrize("K,N", [(768, 2304), (384, 1152)])
+@pytest.mark.parametrize("T", [2569, 12608])
+def test_linear_packed_full_size(K, N, T):
+    """The sizes the benchmark times: cap = 12608 rows (B=64 x N=197), T kept rows
+    at 80% pruning (2569) and dense (12608); several waves of output tiles."""
+    cap = 12608
+    a, w, bias = _inputs(cap, K, N, seed=K + N + T)
+    c = torch.full((cap, N), float("nan"), dtype=torch.float32, device="cuda")
+    rra.get_device_error(clear=True)
+    rra.linear_packed(a.cuda(), w.cuda(), torch.tensor([0, T], dtype=torch.int32).cuda(), 1, c, bias=bias.cuda())
+    torch.cuda.synchronize()
+    assert rra.get_device_error() == 0
+    got = c.cpu().double().numpy()
+    ref = oracle.linear_packed(a.double().numpy(), w.double().numpy(), bias.double().numpy(), T)
+    err = float(np.abs(got[:T] - ref).max())
+    assert err <= ATOL, f"max-abs error {err}"
+    assert np.all(np.isnan(got[T:])), "rows past T were written"

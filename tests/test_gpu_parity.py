@@ -280,6 +280,61 @@ def test_graph_plan_and_host_pipeline_match_direct():
     assert torch.equal(out_h.view(torch.int16), direct.cpu().view(torch.int16))
 
 
+GRAPH_CASES = [("serving_B4", lambda: W.make_serving(4)), ("batched_p80", lambda: W.make_batched(0.8)),
+               ("tiny", lambda: W.make_tiny()), ("hires_p90", lambda: W.make_hires(0.9))]
+
+
+@pytest.mark.parametrize("name,make", GRAPH_CASES, ids=[c[0] for c in GRAPH_CASES])
+def test_graph_plan_matches_oracle(name, make, kernel):
+    """rra_plan_launch (the captured graph) against the oracle, over repeated replays
+    on a poisoned output."""
+    case = make()
+    ref = oracle_result(case)
+    keep_np = case.keep.numpy()
+    keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
+    B, N, H, d = case.B, case.N, case.H, case.d
+    for out_dtype in (case.dtype, torch.float32):
+        out = torch.empty((B, N, H, d), dtype=out_dtype, device="cuda")
+        ws = rra.alloc_workspace(B, N, H, d, case.dtype)
+        plan = rra.Plan(keep, q, k, v, out, ws, scale=SCALE)
+        try:
+            for _ in range(2):
+                out.view(torch.uint8).fill_(0xFF)
+                plan.launch()
+                torch.cuda.synchronize()
+                assert rra.get_device_error() == 0
+                check_output(out.cpu(), keep_np, ref["out"])
+        finally:
+            plan.close()
+
+
+@pytest.mark.parametrize("make", [lambda: W.make_serving(1), lambda: W.make_serving(4),
+                                  lambda: W.make_batched(0.8)], ids=["serving_B1", "serving_B4", "batched_p80"])
+def test_attend_wait_matches_oracle(make, kernel):
+    """rra_attend_wait's result, read right after it returns, against the oracle:
+    packed fp32 output and the padded scatter."""
+    case = make()
+    ref, qp, kp, vp, cu = _packed_inputs(case)
+    B, N, H, d = case.B, case.N, case.H, case.d
+    T = len(ref["src"])
+    src = torch.from_numpy(ref["src"]).to("cuda")
+    side = torch.cuda.Stream()
+    o = torch.full((B * N, H, d), float("nan"), dtype=torch.float32, device="cuda")
+    o_pad = torch.zeros((B, N, H, d), dtype=case.dtype, device="cuda")
+    torch.cuda.synchronize()
+    rra.attend_wait(qp, kp, vp, cu, B, N, o, scale=SCALE)
+    with torch.cuda.stream(side):
+        got = o[:T].clone()
+    side.synchronize()
+    err = float(np.abs(got.cpu().double().numpy() - ref["o"]).max())
+    assert err <= ATOL, err
+    rra.attend_wait(qp, kp, vp, cu, B, N, o_pad, scale=SCALE, src_idx=src, N=N)
+    with torch.cuda.stream(side):
+        got_pad = o_pad.clone()
+    side.synchronize()
+    check_output(got_pad.cpu(), case.keep.numpy(), ref["out"])
+
+
 def test_host_timed_helpers():
     case = W.make_serving(1)
     ref, qp, kp, vp, cu = _packed_inputs(case)
