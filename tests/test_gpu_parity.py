@@ -335,6 +335,27 @@ def test_attend_wait_matches_oracle(make, kernel):
     check_output(got_pad.cpu(), case.keep.numpy(), ref["out"])
 
 
+GATHER_CASES = GRAPH_CASES + [("no_cls_random", lambda: W.make_custom(5, 197, 3, [20, 197, 0, 100, 1], cls=False)),
+                               ("N1024_max", lambda: W.make_custom(2, 1024, 2, [1024, 777]))]
+
+
+@pytest.mark.parametrize("name,make", GATHER_CASES, ids=[c[0] for c in GATHER_CASES])
+def test_attend_gather_matches_oracle(name, make):
+    """rra_attend_gather (rows src_idx of the padded tensors in, padded output
+    out) against the oracle; pruned positions are left as they were."""
+    case = make()
+    ref = oracle_result(case)
+    keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
+    cu = torch.from_numpy(ref["cu"]).cuda()
+    src = torch.from_numpy(np.asarray(ref["src"], dtype=np.int32)).cuda()
+    for out_dtype in (case.dtype, torch.float32):
+        out = torch.zeros(q.shape, dtype=out_dtype, device="cuda")
+        rra.attend_gather(q, k, v, cu, src, out, scale=SCALE)
+        torch.cuda.synchronize()
+        assert rra.get_device_error() == 0
+        check_output(out.cpu(), case.keep.numpy(), ref["out"])
+
+
 def test_host_timed_helpers():
     case = W.make_serving(1)
     ref, qp, kp, vp, cu = _packed_inputs(case)
