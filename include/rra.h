@@ -342,8 +342,36 @@ typedef enum { RRA_ATTEND_TCGEN05 = 0, RRA_ATTEND_MMA_SYNC = 1, RRA_ATTEND_AUTO 
 RRA_API int rra_set_attend_kernel(int kernel);
 
 /* Reads (and with clear != 0 resets) the device-side error code of the
- * current device.  Synchronous: call it after the stream has been synced. */
+ * current device: the word every launch records into unless its host
+ * thread has bound one of its own (rra_bind_error_word).  Synchronous:
+ * call it after the stream has been synced.  The word's address is cached
+ * per device for the life of the process, like the rest of the library's
+ * per-device state: after cudaDeviceReset on a device, do not call this
+ * library on that device again in the same process. */
 RRA_API rra_status rra_get_device_error(int32_t* code, int clear);
+
+/* Per-call device error state.  rra_bind_error_word binds, for the calling
+ * host thread, a caller-owned int32 in device memory (4-byte aligned, else
+ * RRA_ERR_MISALIGNED) as the error word of every kernel this thread
+ * enqueues from then on; NULL restores the device's own word.  Each call
+ * (or stream, or plan) can so own its errors: two pipelines enqueued on two
+ * streams with different words never see each other's codes.  A plan
+ * records into the word bound when rra_plan_create ran.  The caller zeroes
+ * the word before use; the first code recorded wins (later ones are kept
+ * out).  rra_read_error_word copies the word to *code (and with clear != 0
+ * zeroes it), synchronously; it returns RRA_ERR_DEVICE when the code is
+ * nonzero. */
+RRA_API rra_status rra_bind_error_word(int32_t* word);
+RRA_API rra_status rra_read_error_word(int32_t* word, int32_t* code, int clear);
+
+/* Bound, in clock cycles, on any one on-chip wait of the tcgen05 attention
+ * kernels (0, the initial value: about one second).  A wait that runs out
+ * makes the CTA record RRA_DEVERR_WAIT_TIMEOUT, give its own copies and
+ * products a short grace period, release its tensor memory and return, its
+ * output incomplete; the device stays usable.  A test hook for that failure
+ * path: process-wide, applies to launches enqueued after the call; returns
+ * the previous value (-1, nothing changed, for a negative argument). */
+RRA_API long long rra_set_wait_limit(long long cycles);
 
 /* Host-timed latency of rra_attend: `warmup` then `reps` repetitions of
  * {t0 = steady_clock; rra_attend(...); cudaStreamSynchronize; t1}; the

@@ -20,6 +20,12 @@ __device__ int32_t g_device_error = 0;
 __global__ void null_kernel() {}
 
 thread_local char g_last_message[256] = "";
+// rra_bind_error_word: the error word of this host thread's launches (null:
+// the device's own word).
+thread_local int32_t* g_bound_error_word = nullptr;
+// rra_set_wait_limit: the attention kernels' bound on one on-chip wait, in
+// clock cycles (0: the kernels' default).
+std::atomic<long long> g_wait_limit{0};
 std::atomic<uint64_t> g_launches{0};
 std::atomic<int> g_attend_kernel{RRA_ATTEND_AUTO};
 
@@ -82,6 +88,9 @@ rra_status device_state(DeviceState** out) {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
+// Where the kernels this thread enqueues record device-side errors.
+int32_t* error_word(const DeviceState& st) { return g_bound_error_word != nullptr ? g_bound_error_word : st.err; }
+
 bool valid_in(rra_dtype t) { return t == RRA_F16 || t == RRA_BF16; }
 bool valid_out(rra_dtype t) { return t == RRA_F16 || t == RRA_BF16 || t == RRA_F32; }
 bool finite(float x) { return x == x && x != INFINITY && x != -INFINITY; }
@@ -141,7 +150,7 @@ rra_status enqueue_pack(const DeviceState& st, const uint8_t* keep, int B, int N
   PackArgs a{};
   a.src_rows = src_rows;
   a.src_cap = static_cast<long long>(B) * N;
-  a.err = st.err;
+  a.err = error_word(st);
   a.keep = keep;
   a.B = B;
   a.N = N;
@@ -243,7 +252,8 @@ rra_status enqueue_attend(const DeviceState& st, const void* qp, const void* kp,
   a.N = N;
   a.max_seqlen = max_seqlen;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.err = st.err;
+  a.err = error_word(st);
+  a.wait_limit = g_wait_limit.load();
   cudaError_t e;
   if (!coalesced_out && use_tcgen05(st, B, H)) {
     if (!attend_tc_available())
@@ -335,7 +345,8 @@ rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaSt
     a.N = p.N;
     a.max_seqlen = p.N;
     a.scale_log2 = p.scale * 1.4426950408889634f;
-    a.err = st.err;
+    a.err = error_word(st);
+    a.wait_limit = g_wait_limit.load();
     cudaError_t e = launch_attend_tc_fused(a, p.in, p.out_dt, st.num_sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "fused pipeline launch");
     return RRA_OK;
@@ -496,7 +507,7 @@ rra_status rra_linear_packed(const void* a, const void* w, const float* bias, co
   if (bias != nullptr && !aligned16(bias)) return fail(RRA_ERR_MISALIGNED, "bias not 16-byte aligned");
   DeviceState* st = nullptr;
   RRA_TRY(device_state(&st));
-  cudaError_t e = launch_linear_packed(a, w, bias, cu_seqlens, B, cap, K, N, in_dtype, c, out_dtype, st->err,
+  cudaError_t e = launch_linear_packed(a, w, bias, cu_seqlens, B, cap, K, N, in_dtype, c, out_dtype, error_word(*st),
                                        static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "linear_packed launch");
   g_launches += 1;
@@ -515,7 +526,7 @@ rra_status rra_cls_scores(const void* qp, const void* kp, const int32_t* cu_seql
     return fail(RRA_ERR_INVALID_ARG, "cu_seqlens, src_idx or scores is null");
   DeviceState* st = nullptr;
   RRA_TRY(device_state(&st));
-  cudaError_t e = launch_cls_scores(qp, kp, cu_seqlens, src_idx, B, N, H, scale, in_dtype, scores, st->err,
+  cudaError_t e = launch_cls_scores(qp, kp, cu_seqlens, src_idx, B, N, H, scale, in_dtype, scores, error_word(*st),
                                     static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "cls_scores launch");
   g_launches += 1;
@@ -625,7 +636,8 @@ rra_status rra_attend_gather(const void* q, const void* k, const void* v, const 
   a.N = N;
   a.max_seqlen = N;
   a.scale_log2 = scale * 1.4426950408889634f;
-  a.err = st->err;
+  a.err = error_word(*st);
+  a.wait_limit = g_wait_limit.load();
   cudaError_t e = launch_attend_tc_gather(a, in_dtype, out_dtype, st->num_sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attend (gather) launch");
   g_launches += 1;
@@ -648,7 +660,7 @@ rra_status rra_unpack(const void* op, const int32_t* dst_idx, int B, int N, int 
   a.B = B;
   a.N = N;
   a.row_vecs = H * d * dtype_bytes(dtype) / 16;
-  a.err = st->err;
+  a.err = error_word(*st);
   cudaError_t e = launch_unpack(a, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "unpack launch");
   g_launches += 1;
@@ -737,7 +749,8 @@ rra_status rra_pipeline_mapped(const uint8_t* keep_h, const void* q_h, const voi
     a.N = p.N;
     a.max_seqlen = p.N;
     a.scale_log2 = p.scale * 1.4426950408889634f;
-    a.err = st->err;
+    a.err = error_word(*st);
+    a.wait_limit = g_wait_limit.load();
     cudaError_t e = launch_attend_tc_fused_host(a, p.in, p.out_dt, st->num_sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "mapped pipeline launch");
     g_launches += 1;
@@ -825,6 +838,30 @@ rra_status rra_get_device_error(int32_t* code, int clear) {
     if (e != cudaSuccess) return cuda_fail(e, "clear device error");
   }
   return *code == 0 ? RRA_OK : RRA_ERR_DEVICE;
+}
+
+rra_status rra_bind_error_word(int32_t* word) {
+  if (word != nullptr && (reinterpret_cast<uintptr_t>(word) & 3u) != 0)
+    return fail(RRA_ERR_MISALIGNED, "error word not 4-byte aligned");
+  g_bound_error_word = word;
+  return RRA_OK;
+}
+
+rra_status rra_read_error_word(int32_t* word, int32_t* code, int clear) {
+  if (word == nullptr || code == nullptr) return fail(RRA_ERR_INVALID_ARG, "word or code is null");
+  cudaError_t e = cudaMemcpy(code, word, sizeof(int32_t), cudaMemcpyDeviceToHost);
+  if (e != cudaSuccess) return cuda_fail(e, "read error word");
+  if (clear) {
+    e = cudaMemset(word, 0, sizeof(int32_t));
+    if (e == cudaSuccess) e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return cuda_fail(e, "clear error word");
+  }
+  return *code == 0 ? RRA_OK : RRA_ERR_DEVICE;
+}
+
+long long rra_set_wait_limit(long long cycles) {
+  if (cycles < 0) return -1;
+  return g_wait_limit.exchange(cycles);
 }
 
 rra_status rra_time_attend_host(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens,

@@ -90,6 +90,7 @@ constexpr uint32_t B_OEMPTY = 72;     // unit's O read out (128 consumer arrival
 constexpr uint32_t B_DRAIN = 80;      // every product issued has completed
 constexpr uint32_t W_TMEM = 88;       // TMEM base written by tcgen05.alloc
 constexpr uint32_t W_ABORT = 92;      // abort flag
+constexpr uint32_t B_STAGED = 96;     // unit's output rows read back out of the stage (4 softmax warps)
 // Item descriptors, one per stage, then (fused pipeline) POS_SLOTS lists of
 // kept positions (int16, N each).
 constexpr uint32_t DESC_BYTES = 48;
@@ -173,6 +174,13 @@ __device__ __forceinline__ void store16_half(void* dst, const float* o, float in
                       pack2<T2>(o[8 * i + 4] * inv, o[8 * i + 5] * inv),
                       pack2<T2>(o[8 * i + 6] * inv, o[8 * i + 7] * inv));
 }
+// The packed-pair type of a 16-bit output type.
+template <typename T> struct Tout2Of;
+template <> struct Tout2Of<__nv_bfloat16> { using type = __nv_bfloat162; };
+template <> struct Tout2Of<__half> { using type = __half2; };
+template <> struct Tout2Of<float> { using type = __nv_bfloat162; };   // unused
+template <typename T> using Tout2 = typename Tout2Of<T>::type;
+
 template <>
 __device__ __forceinline__ void store16<__nv_bfloat16>(__nv_bfloat16* dst, const float* o, float inv) {
   store16_half<__nv_bfloat162>(dst, o, inv);
@@ -593,7 +601,7 @@ __device__ __forceinline__ void rescale_p32(uint32_t tS_row, float alpha) {
   }
 }
 
-template <typename Tin, typename Tout, bool SCATTER, int MODE>
+template <typename Tin, typename Tout, bool SCATTER, int MODE, bool LIMIT>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_q3,
@@ -605,6 +613,13 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   constexpr bool ZF_BULK = MODE == MODE_FUSED;
   constexpr int ZF = ZF_BULK ? ZF_BULK_TOKENS : (MODE == MODE_FUSED_HOST ? ZF_LIST_TOKENS : ZF_MASK_ROWS);
   constexpr bool HOSTLD = MODE == MODE_FUSED_HOST;   // cp.async loads (no tensor maps)
+  // On packed inputs, 16-bit outputs of tiles with more than 64 rows leave
+  // through the unit's last K/V stage (whole rows per store instruction);
+  // smaller tiles (where the extra round trip through shared memory costs
+  // more than it saves), fp32 outputs and the fused modes (whose producer
+  // needs that stage back sooner) store row by row.
+  constexpr bool STAGED = sizeof(Tout) == 2 && MODE == MODE_PACKED;
+  constexpr int STAGE_MIN_ROWS = 65;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -641,6 +656,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     mbar_init(bar_ofull, 1);
     mbar_init(bar_oempty, CONSUMERS);
     mbar_init(bar_drain, 1);
+    mbar_init(bars + B_STAGED, 4);
     st_shared_u32(abort_flag, 0u);
     fence_barrier_init();
   }
@@ -666,6 +682,9 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int BH = a.B * a.H;
   const int step = gridDim.x;
+  // The bound on one wait: a compile-time constant, except in the
+  // instantiation for a launch made with a wait limit set (rra_set_wait_limit).
+  const long long wlimit = LIMIT ? a.wait_limit : WAIT_LIMIT_CYCLES;
   bool bad = false;
 
   if (warp == PRODUCER_WARP) {
@@ -686,8 +705,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       const int nch = sentinel ? 1 : U.nchunks;
       for (int c = 0; c < nch; ++c) {
         const int st = static_cast<int>(j % STAGES);
-        if (j >= STAGES) bad |= !mbar_wait_or_abort(bar_empty(st), ((j / STAGES) - 1) & 1, abort_flag);
-        if (!sentinel && c == 0 && uidx >= 1) bad |= !mbar_wait_or_abort(bar_qempty, (uidx - 1) & 1, abort_flag);
+        if (j >= STAGES) bad |= !mbar_wait_or_abort(bar_empty(st), ((j / STAGES) - 1) & 1, abort_flag, wlimit);
+        if (!sentinel && c == 0 && uidx >= 1) bad |= !mbar_wait_or_abort(bar_qempty, (uidx - 1) & 1, abort_flag, wlimit);
         bad = __any_sync(0xffffffffu, bad);
         if (bad) break;
         const uint32_t d = desc_addr(st);
@@ -863,12 +882,13 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     for (;; ++j) {
       // S(j): loads, descriptor, then the product.
       const int st = static_cast<int>(j % STAGES);
-      bad |= !mbar_wait_or_abort(bar_full(st), (j / STAGES) & 1, abort_flag);
+      bad |= !mbar_wait_or_abort(bar_full(st), (j / STAGES) & 1, abort_flag, wlimit);
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
       const uint32_t d = desc_addr(st);
       if (static_cast<int>(ld_shared_u32(d + 0)) >= units) break;   // sentinel
       const int n = static_cast<int>(ld_shared_u32(d + 12));
+      const bool staged = STAGED && static_cast<int>(ld_shared_u32(d + 20)) >= STAGE_MIN_ROWS;
       nch = static_cast<int>(ld_shared_u32(d + 24));
       c = static_cast<int>(ld_shared_u32(d + 28));
       const int n_c = min(BN, n - c * BN);
@@ -888,12 +908,12 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       if (last && elect_one()) umma_commit(bar_qempty);
 
       // P(j) written, then the P.V product.
-      bad |= !mbar_wait_or_abort(bar_pready, ph_pready, abort_flag);
+      bad |= !mbar_wait_or_abort(bar_pready, ph_pready, abort_flag, wlimit);
       ph_pready ^= 1;
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
       if (first && ustarted >= 1) {
-        bad |= !mbar_wait_or_abort(bar_oempty, (ustarted - 1) & 1, abort_flag);
+        bad |= !mbar_wait_or_abort(bar_oempty, (ustarted - 1) & 1, abort_flag, wlimit);
         bad = __any_sync(0xffffffffu, bad);
         if (bad) break;
       }
@@ -915,11 +935,13 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
             if (leader) umma_f16_tmem_a(tO, tS + kk * 16 + 8, db, idesc_pv, 1u);
           }
         }
-        if (leader) umma_commit(bar_empty(st));
+        // (A unit's last stage is handed back by the epilogue, which stages
+        // 16-bit output rows in it.)
+        if (leader && !(staged && last)) umma_commit(bar_empty(st));
         if (leader && last) umma_commit(bar_ofull);
         if (leader) umma_commit(bar_sfree);
       }
-      bad |= !mbar_wait_or_abort(bar_sfree, ph_sfree, abort_flag);
+      bad |= !mbar_wait_or_abort(bar_sfree, ph_sfree, abort_flag, wlimit);
       ph_sfree ^= 1;
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
@@ -927,7 +949,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     if (!bad) {
       // Every product issued has completed (and with it the arrivals above).
       if (elect_one()) umma_commit(bar_drain);
-      bad |= !mbar_wait_or_abort(bar_drain, 0, abort_flag);
+      bad |= !mbar_wait_or_abort(bar_drain, 0, abort_flag, wlimit);
       bad = __any_sync(0xffffffffu, bad);
     }
   } else {
@@ -940,7 +962,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     long long out_elem = -1;          // this row's output offset in the current unit
     for (uint32_t j = 0;; ++j) {
       const int st = static_cast<int>(j % STAGES);
-      bad |= !mbar_wait_or_abort(bar_full(st), (j / STAGES) & 1, abort_flag);
+      bad |= !mbar_wait_or_abort(bar_full(st), (j / STAGES) & 1, abort_flag, wlimit);
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
       const uint32_t d = desc_addr(st);
@@ -976,7 +998,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
         }
         out_elem = dst_row < 0 ? -1 : (dst_row * a.H + h) * HD;
       }
-      bad |= !mbar_wait_or_abort(bar_sfull, ph_sfull, abort_flag);
+      bad |= !mbar_wait_or_abort(bar_sfull, ph_sfull, abort_flag, wlimit);
       ph_sfull ^= 1;
       bad = __any_sync(0xffffffffu, bad);
       if (bad) break;
@@ -1033,26 +1055,71 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
 
       if (last) {
         // Epilogue: this thread's row, normalised, to the packed or padded output.
-        bad |= !mbar_wait_or_abort(bar_ofull, uidx & 1, abort_flag);
+        bad |= !mbar_wait_or_abort(bar_ofull, uidx & 1, abort_flag, wlimit);
         bad = __any_sync(0xffffffffu, bad);
         if (bad) break;
         tc_fence_after();
-        if (rows_here) {
-          const float inv = 1.f / l_run;
-          Tout* out = static_cast<Tout*>(a.o) + (out_elem < 0 ? 0 : out_elem);
+        if (STAGED && rows_q >= STAGE_MIN_ROWS) {
+          // Each warp writes its 32 rows (128 bytes each) into 4 KB of the
+          // unit's last K/V stage (swizzled by row), then stores them back
+          // out with 8 lanes per row: every store instruction covers four
+          // whole rows.  The stage goes back to the producer afterwards.
+          const uint32_t stg = (warp < 2 ? sK(st) : sV(st)) + static_cast<uint32_t>(warp & 1) * 4096u;
+          if (rows_here) {
+            const float inv = 1.f / l_run;
 #pragma unroll
-          for (int g = 0; g < HD / 16; ++g) {
-            float o[16];
-            tmem_ld16(tO_row + g * 16, o);
-            if (g == HD / 16 - 1) {
-              tc_fence_before();
-              mbar_arrive(bar_oempty);   // O is in registers: the next unit may overwrite it
+            for (int g = 0; g < HD / 16; ++g) {
+              float o[16];
+              tmem_ld16(tO_row + g * 16, o);
+              if (g == HD / 16 - 1) {
+                tc_fence_before();
+                mbar_arrive(bar_oempty);   // O is in registers: the next unit may overwrite it
+              }
+              uint32_t w[8];
+#pragma unroll
+              for (int i = 0; i < 8; ++i) w[i] = pack2<Tout2<Tout>>(o[2 * i] * inv, o[2 * i + 1] * inv);
+              st_shared_v4(stg + lane * 128 + (((2 * g) ^ (lane & 7)) << 4), w[0], w[1], w[2], w[3]);
+              st_shared_v4(stg + lane * 128 + (((2 * g + 1) ^ (lane & 7)) << 4), w[4], w[5], w[6], w[7]);
             }
-            if (out_elem >= 0) store16<Tout>(out + g * 16, o, inv);
+            __syncwarp();
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+              const int rr = 4 * i + (lane >> 3), cc = lane & 7;
+              const long long dst = __shfl_sync(0xffffffffu, out_elem, rr);
+              const uint4 v = ld_shared_v4(stg + rr * 128 + ((cc ^ (rr & 7)) << 4));
+              if (dst >= 0) *reinterpret_cast<uint4*>(static_cast<Tout*>(a.o) + dst + cc * 8) = v;
+            }
+          } else {
+            tc_fence_before();
+            mbar_arrive(bar_oempty);
+          }
+          fence_proxy_async();   // these shared-memory accesses before the producer's next copies into the stage
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + B_STAGED);
+          if (warp == 0) {
+            bad |= !mbar_wait_or_abort(bars + B_STAGED, uidx & 1, abort_flag, wlimit);
+            bad = __any_sync(0xffffffffu, bad);
+            if (lane == 0 && !bad) mbar_arrive(bar_empty(st));
+            if (bad) break;
           }
         } else {
-          tc_fence_before();
-          mbar_arrive(bar_oempty);
+          if (rows_here) {
+            const float inv = 1.f / l_run;
+            Tout* out = static_cast<Tout*>(a.o) + (out_elem < 0 ? 0 : out_elem);
+#pragma unroll
+            for (int g = 0; g < HD / 16; ++g) {
+              float o[16];
+              tmem_ld16(tO_row + g * 16, o);
+              if (g == HD / 16 - 1) {
+                tc_fence_before();
+                mbar_arrive(bar_oempty);   // O is in registers: the next unit may overwrite it
+              }
+              if (out_elem >= 0) store16<Tout>(out + g * 16, o, inv);
+            }
+          } else {
+            tc_fence_before();
+            mbar_arrive(bar_oempty);
+          }
         }
         ++uidx;
       }
@@ -1130,13 +1197,13 @@ cudaError_t make_gather_map(CUtensorMap* map, const void* ptr, long long rows, b
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <typename Tin, typename Tout, bool SCATTER, int MODE>
+template <typename Tin, typename Tout, bool SCATTER, int MODE, bool LIMIT>
 cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t stream, uint32_t* ctas) {
   // Largest dynamic shared memory any launch of this instantiation asks for
   // (position lists for N <= 1024 in the fused mode).
   constexpr bool kFused = MODE == MODE_FUSED || MODE == MODE_FUSED_ROWS || MODE == MODE_FUSED_HOST;
   constexpr uint32_t kMaxSmem = SMEM_ALLOC + (kFused ? POS_SLOTS * 2048u : 0u);
-  auto kernel = attend_tc_kernel<Tin, Tout, SCATTER, MODE>;
+  auto kernel = attend_tc_kernel<Tin, Tout, SCATTER, MODE, LIMIT>;
   static bool attr_set[kMaxDev] = {};
   static uint32_t occ_smem[kMaxDev] = {};
   static int occ_blocks[kMaxDev] = {};
@@ -1220,6 +1287,14 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
   return cudaLaunchKernelEx(&cfg, kernel, mq, mk, mv, mq3, mk3, mv3, b, static_cast<int>(units), pos_stride);
 }
 
+// A launch made with a wait limit set runs its own instantiation, so that the
+// kernels every other launch runs keep the bound a compile-time constant.
+template <typename Tin, typename Tout, bool SCATTER, int MODE>
+cudaError_t launch_tc_lim(const AttendArgs& a, int num_sms, cudaStream_t stream, uint32_t* ctas) {
+  if (a.wait_limit > 0) return launch_tc_typed<Tin, Tout, SCATTER, MODE, true>(a, num_sms, stream, ctas);
+  return launch_tc_typed<Tin, Tout, SCATTER, MODE, false>(a, num_sms, stream, ctas);
+}
+
 template <typename Tin, typename Tout>
 cudaError_t launch_tc_out(const AttendArgs& a, int mode, int num_sms, cudaStream_t stream, uint32_t* ctas) {
   if (mode == MODE_FUSED) {
@@ -1228,13 +1303,13 @@ cudaError_t launch_tc_out(const AttendArgs& a, int mode, int num_sms, cudaStream
     // sooner: measured 6.0 against 6.6 us on the serving workload).
     const long long units = static_cast<long long>(a.B) * a.H * ((a.max_seqlen + BM - 1) / BM);
     if (units <= (num_sms > 0 ? num_sms : 152))
-      return launch_tc_typed<Tin, Tout, true, MODE_FUSED_ROWS>(a, num_sms, stream, ctas);
-    return launch_tc_typed<Tin, Tout, true, MODE_FUSED>(a, num_sms, stream, ctas);
+      return launch_tc_lim<Tin, Tout, true, MODE_FUSED_ROWS>(a, num_sms, stream, ctas);
+    return launch_tc_lim<Tin, Tout, true, MODE_FUSED>(a, num_sms, stream, ctas);
   }
-  if (mode == MODE_FUSED_HOST) return launch_tc_typed<Tin, Tout, true, MODE_FUSED_HOST>(a, num_sms, stream, ctas);
-  if (mode == MODE_GATHER) return launch_tc_typed<Tin, Tout, true, MODE_GATHER>(a, num_sms, stream, ctas);
-  if (a.src_idx != nullptr) return launch_tc_typed<Tin, Tout, true, MODE_PACKED>(a, num_sms, stream, ctas);
-  return launch_tc_typed<Tin, Tout, false, MODE_PACKED>(a, num_sms, stream, ctas);
+  if (mode == MODE_FUSED_HOST) return launch_tc_lim<Tin, Tout, true, MODE_FUSED_HOST>(a, num_sms, stream, ctas);
+  if (mode == MODE_GATHER) return launch_tc_lim<Tin, Tout, true, MODE_GATHER>(a, num_sms, stream, ctas);
+  if (a.src_idx != nullptr) return launch_tc_lim<Tin, Tout, true, MODE_PACKED>(a, num_sms, stream, ctas);
+  return launch_tc_lim<Tin, Tout, false, MODE_PACKED>(a, num_sms, stream, ctas);
 }
 
 template <typename Tin>

@@ -59,6 +59,7 @@ struct AttendArgs {
   uint32_t done_target;     // its value before this launch (the launcher adds the grid size)
   uint32_t* done_word;      // device address of a page-locked host word, or nullptr
   uint32_t done_ticket;     // value published to *done_word
+  long long wait_limit;     // clock cycles one on-chip wait may take before giving up (0: the default)
 };
 
 // Each CTA adds one to *done_count once all its threads' output stores are

@@ -193,6 +193,12 @@ __device__ __forceinline__ void st_shared_v4(uint32_t addr, uint32_t a, uint32_t
                : "memory");
 }
 
+__device__ __forceinline__ uint4 ld_shared_v4(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.b32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr) : "memory");
+  return v;
+}
+
 // 16 consecutive output elements of one row, o[i] * inv, as Tout.
 // 32 consecutive fp32 columns of this thread's TMEM lane (wait tied to the
 // destination registers, as in tmem_ld16).
@@ -260,11 +266,25 @@ __device__ __forceinline__ uint32_t ld_shared_volatile_u32(uint32_t addr) {
   return v;
 }
 // Bounded wait that also gives up as soon as the CTA's abort flag is set.
-__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, uint32_t abort_flag) {
+// Bounded wait.  A bound below WAIT_POLL_BELOW cycles (a test hook for
+// this path) polls with test_wait, out of line: a suspended try_wait sleeps
+// until the phase completes, past such a bound.
+constexpr long long WAIT_POLL_BELOW = 1000000LL;
+static __device__ __noinline__ bool mbar_poll_or_abort(uint32_t bar, uint32_t parity, uint32_t abort_flag, long long limit) {
+  const long long t0 = clock64();
+  while (!mbar_test_wait(bar, parity)) {
+    if (ld_shared_volatile_u32(abort_flag) != 0u) return false;
+    if (clock64() - t0 > limit) return false;
+  }
+  return true;
+}
+__device__ __forceinline__ bool mbar_wait_or_abort(uint32_t bar, uint32_t parity, uint32_t abort_flag,
+                                                   long long limit = WAIT_LIMIT_CYCLES) {
+  if (limit < WAIT_POLL_BELOW) return mbar_poll_or_abort(bar, parity, abort_flag, limit);
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (ld_shared_volatile_u32(abort_flag) != 0u) return false;
-    if (clock64() - t0 > WAIT_LIMIT_CYCLES) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }

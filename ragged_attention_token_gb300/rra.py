@@ -59,6 +59,9 @@ _SIGNATURES = {
     "rra_time_plan_host": (_i, [_vp, _vp, _i, _i, _dp]),
     "rra_time_null_host": (_i, [_vp, _i, _i, _dp]),
     "rra_set_attend_kernel": (_i, [_i]),
+    "rra_bind_error_word": (_i, [_vp]),
+    "rra_read_error_word": (_i, [_vp, ctypes.POINTER(ctypes.c_int32), _i]),
+    "rra_set_wait_limit": (ctypes.c_longlong, [ctypes.c_longlong]),
     "rra_status_string": (ctypes.c_char_p, [_i]),
     "rra_last_error_message": (ctypes.c_char_p, []),
     "rra_launch_count": (ctypes.c_uint64, []),
@@ -300,6 +303,28 @@ def get_device_error(clear: bool = True) -> int:
     if st not in (RRA_OK, RRA_ERR_DEVICE):
         _check(st)
     return int(code.value)
+
+
+def bind_error_word(word=None) -> None:
+    """rra_bind_error_word: this thread's launches record device errors into `word`
+    (an int32 CUDA tensor of one element), or into the device's own word (None)."""
+    if word is not None and (word.dtype != torch.int32 or word.numel() < 1):
+        raise ValueError("expected an int32 CUDA tensor")
+    _check(lib().rra_bind_error_word(_ptr(word)))
+
+
+def read_error_word(word, clear: bool = True) -> int:
+    """rra_read_error_word: the code in a bound error word (0: none), zeroed if clear."""
+    code = ctypes.c_int32(0)
+    st = lib().rra_read_error_word(_ptr(word), ctypes.byref(code), 1 if clear else 0)
+    if st not in (RRA_OK, RRA_ERR_DEVICE):
+        _check(st)
+    return int(code.value)
+
+
+def set_wait_limit(cycles: int) -> int:
+    """rra_set_wait_limit: bound (clock cycles) on one on-chip wait; 0 = default. Returns the previous."""
+    return int(lib().rra_set_wait_limit(int(cycles)))
 
 
 def time_attend_host(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, warmup: int, reps: int,

@@ -123,3 +123,16 @@ def check_output(out: torch.Tensor, keep: np.ndarray, ref_out: np.ndarray):
     bad = err > tol
     assert not bad.any(), f"max-abs err {err.max():.3e} over tolerance at {int(bad.sum())} elements"
     return float(err.max()) if err.size else 0.0
+
+
+def packed_inputs(case):
+    """Oracle result plus device packed Q/K/V (rows past T poisoned with NaN) and cu_seqlens."""
+    ref = oracle_result(case)
+    B, N, H, d = case.B, case.N, case.H, case.d
+    cap = B * N
+    qp, kp, vp = (torch.empty((cap, H, d), dtype=case.dtype, device="cuda") for _ in range(3))
+    for t, r in zip((qp, kp, vp), ref["packed_bits"]):
+        t.view(torch.uint8).fill_(0xFF)
+        t[: len(ref["src"])].view(torch.int16).copy_(torch.from_numpy(r))
+    cu = torch.from_numpy(ref["cu"]).to("cuda")
+    return ref, qp, kp, vp, cu

@@ -15,7 +15,7 @@ import torch
 
 import oracle
 from gpu_util import (ATOL, SCALE, bits, check_indices, check_indices_and_packing, check_output, oracle_result,
-                      run_pack, run_pipeline)
+                      packed_inputs, run_pack, run_pipeline)
 from ragged_attention_token_gb300 import rra
 from ragged_attention_token_gb300 import workloads as W
 
@@ -147,15 +147,7 @@ def test_repeat_runs_and_batch_permutation_bit_exact(kernel):
 
 
 def _packed_inputs(case):
-    ref = oracle_result(case)
-    B, N, H, d = case.B, case.N, case.H, case.d
-    cap = B * N
-    qp, kp, vp = (torch.empty((cap, H, d), dtype=case.dtype, device="cuda") for _ in range(3))
-    for t, r in zip((qp, kp, vp), ref["packed_bits"]):
-        t.view(torch.uint8).fill_(0xFF)
-        t[: len(ref["src"])].view(torch.int16).copy_(torch.from_numpy(r))
-    cu = torch.from_numpy(ref["cu"]).to("cuda")
-    return ref, qp, kp, vp, cu
+    return packed_inputs(case)
 
 
 @pytest.mark.parametrize("make", [lambda: W.make_tiny(), lambda: W.make_hires(0.5)], ids=["tiny", "hires_p50"])
