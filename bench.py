@@ -208,11 +208,14 @@ def graph_time_per_launch(fn_list, stream, reps=5):
 def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
     """Per-launch device µs on cold inputs (graphs of back-to-back launches).
 
-    fused_us: rra_pipeline with the tcgen05 kernel -- ONE launch (mask scan,
-    gather, attention, every output row written).  With packed=True also the
-    two-launch packed path: pack_copy_us (rra_pack with the row copy and zero
-    fill) and attend_packed_us (rra_attend on the packed buffers with the
-    mma.sync kernel), plus attend_packed_tc_us (the same with tcgen05)."""
+    fused_us: rra_pipeline under the current kernel selection -- ONE launch
+    (mask scan, gather, attention, every output row written).  With
+    packed=True also: fused_tc_us (the warp-specialised tcgen05 kernel
+    forced), the two-launch packed path (pack_copy_us: rra_pack with the row
+    copy and zero fill; attend_packed_us: rra_attend on the packed buffers
+    with the mma.sync kernel; attend_packed_tc_us: the same with the
+    warp-specialised tcgen05 kernel) and, for N <= 256, the small-grid
+    tcgen05 kernel (attend_packed_tcl_us, fused_tcl_us)."""
     B, N, H, d = case.B, case.N, case.H, case.d
     R = sets.R
     n_launch = n_launch or max(R, 64)
@@ -222,10 +225,13 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
         keep, q, k, v, out, ws = sets.sets[i % R]
         return lambda: rra.pipeline(keep, q, k, v, out, ws, scale=SCALE, stream=stream)
 
+    # fused_us: rra_pipeline under the current kernel selection (what the
+    # timed steps run); the rest force one kernel each.
+    res = {"fused_us": graph_time_per_launch([fused_fn(i) for i in range(n_launch)], stream)}
     prev = rra.set_attend_kernel(rra.ATTEND_TCGEN05)
     try:
-        res = {"fused_us": graph_time_per_launch([fused_fn(i) for i in range(n_launch)], stream)}
         if packed:
+            res["fused_tc_us"] = graph_time_per_launch([fused_fn(i) for i in range(n_launch)], stream)
             def pack_fn(i):
                 keep, q, k, v, out, ws = sets.sets[i % R]
                 cu, dst, src, qp, kp, vp = views[i % R]
@@ -239,6 +245,10 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
 
             res["pack_copy_us"] = graph_time_per_launch([pack_fn(i) for i in range(n_launch)], stream)
             res["attend_packed_tc_us"] = graph_time_per_launch([attend_fn(i) for i in range(n_launch)], stream)
+            if N <= 256:
+                rra.set_attend_kernel(rra.ATTEND_TCGEN05_LATENCY)
+                res["attend_packed_tcl_us"] = graph_time_per_launch([attend_fn(i) for i in range(n_launch)], stream)
+                res["fused_tcl_us"] = graph_time_per_launch([fused_fn(i) for i in range(n_launch)], stream)
             rra.set_attend_kernel(rra.ATTEND_MMA_SYNC)
             res["attend_packed_us"] = graph_time_per_launch([attend_fn(i) for i in range(n_launch)], stream)
     finally:
@@ -252,6 +262,14 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
 # changes the traffic is reported as null until it is captured again.
 TRAFFIC_SRC_SHA = "84f8ec8241cdb73e"
 TRAFFIC_BYTES = {"serving_B4": 430587, "batched_b64_p80": 11922603}
+
+
+def pipeline_kernel_name(case, n_sms):
+    """The kernel rra_pipeline launches for this workload under the automatic choice."""
+    units = case.B * case.H * ((case.N + 127) // 128)
+    if units <= 2 * n_sms and case.N <= 256:
+        return "attend_small_kernel (fused pipeline, small-grid form: mask scan, gather, attention, zero fill)"
+    return "attend_tc_kernel (fused pipeline: mask scan, gather, attention, zero fill)"
 
 
 def measured_traffic(key):
@@ -577,10 +595,10 @@ def run_rra(args, world, rank, local):
         kern = {"fused_us": round(kt["fused_us"], 3)}
         roof = roofline_obj(by["fused_min"], by["flops"], kt["fused_us"], peaks)
         roof["traffic"] = measured_traffic(case.name)
-        roof["kernel"] = "attend_tc_kernel (fused pipeline: mask scan, gather, attention, zero fill)"
+        roof["kernel"] = pipeline_kernel_name(case, n_sms)
     else:
         kern = {"pack_copy_us": round(kt["pack_copy_us"], 3), "attend_packed_us": round(kt["attend_packed_us"], 3),
-                "fused_tcgen05_us": round(kt["fused_us"], 3)}
+                "fused_tcgen05_us": round(kt["fused_tc_us"], 3)}
         if kt["attend_packed_us"] >= kt["pack_copy_us"]:
             roof = roofline_obj(by["attend"], by["flops"], kt["attend_packed_us"], peaks)
             roof["kernel"] = "attend_mma_kernel (packed)"

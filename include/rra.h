@@ -328,17 +328,28 @@ RRA_API void rra_plan_destroy(rra_plan* plan);
 /* Which kernel rra_attend and rra_pipeline launch; process-wide, returns
  * the previous choice (or -1 for an unknown value).
  *   RRA_ATTEND_TCGEN05  TMA tile loads + tcgen05.mma with TMEM accumulators,
- *                       persistent CTAs; rra_pipeline gathers rows from the
- *                       padded inputs (no packed copy);
+ *                       warp-specialised persistent CTAs; rra_pipeline
+ *                       gathers rows from the padded inputs (no packed copy);
  *   RRA_ATTEND_MMA_SYNC warp-level mma.sync kernel on packed buffers;
  *                       rra_pipeline packs with the row copy first;
- *   RRA_ATTEND_AUTO     (default) rra_attend: MMA_SYNC when B*H is below the
- *                       device's SM count (too few (image, head) pairs to
- *                       fill the GPU: the shorter per-CTA latency chain
- *                       wins), TCGEN05 otherwise; rra_pipeline: always the
- *                       fused one-launch TCGEN05 path (one launch beats two
- *                       at every measured size). */
-typedef enum { RRA_ATTEND_TCGEN05 = 0, RRA_ATTEND_MMA_SYNC = 1, RRA_ATTEND_AUTO = 2 } rra_attend_kernel;
+ *   RRA_ATTEND_TCGEN05_LATENCY  tcgen05.mma with TMEM accumulators, one CTA
+ *                       of four warps per (image, head, query tile) doing
+ *                       every step in turn (cp.async loads, no warp
+ *                       specialisation): the shortest chain for grids of
+ *                       about one unit per SM; max_seqlen (rra_pipeline: N)
+ *                       up to 256, the TCGEN05 kernel beyond;
+ *   RRA_ATTEND_AUTO     (default) while the grid (B * H *
+ *                       ceil(max_seqlen / 128) units) fits in one wave of
+ *                       two CTAs per SM and max_seqlen <= 256: rra_pipeline
+ *                       TCGEN05_LATENCY, rra_attend MMA_SYNC (the shortest
+ *                       chain on packed buffers at these sizes); TCGEN05
+ *                       otherwise. */
+typedef enum {
+  RRA_ATTEND_TCGEN05 = 0,
+  RRA_ATTEND_MMA_SYNC = 1,
+  RRA_ATTEND_AUTO = 2,
+  RRA_ATTEND_TCGEN05_LATENCY = 3
+} rra_attend_kernel;
 RRA_API int rra_set_attend_kernel(int kernel);
 
 /* Reads (and with clear != 0 resets) the device-side error code of the

@@ -135,12 +135,26 @@ void workspace_layout(int B, int N, int H, int d, rra_dtype in, size_t off[6], s
 
 // ---------------------------------------------------------------- enqueue
 
-// The kernel a call with B images of H heads runs under the current choice.
-bool use_tcgen05(const DeviceState& st, int B, int H) {
+// The attention kernel a call runs under the current choice: the
+// warp-specialised tcgen05 kernel, its small-grid form (one warpgroup per
+// unit, max_seqlen <= 256), or the mma.sync kernel.
+enum AttendKernelChoice { KC_TC = 0, KC_TC_SMALL = 1, KC_MMA = 2 };
+AttendKernelChoice attend_choice(const DeviceState& st, int B, int H, int max_seqlen, bool pipeline) {
   const int k = g_attend_kernel.load();
-  if (k == RRA_ATTEND_TCGEN05) return true;
-  if (k == RRA_ATTEND_MMA_SYNC) return false;
-  return static_cast<long long>(B) * H >= st.num_sms;
+  const bool small_ok = max_seqlen <= ATTEND_SMALL_MAX_KEYS;
+  if (k == RRA_ATTEND_MMA_SYNC) return KC_MMA;
+  if (k == RRA_ATTEND_TCGEN05) return KC_TC;
+  if (k == RRA_ATTEND_TCGEN05_LATENCY) return small_ok ? KC_TC_SMALL : KC_TC;
+  // Automatic.  While the grid fits in one wave of two CTAs per SM the call
+  // is one latency chain per CTA: the pipeline takes the small-grid tcgen05
+  // form (one launch that also scans the mask and writes the zero rows:
+  // 5.0 against 5.4 us for the warp-specialised fused kernel at serving
+  // B=4), rra_attend on packed buffers the mma.sync kernel (its
+  // register-resident chain: 3.4 against 4.1 us).  Beyond, the
+  // warp-specialised kernel.
+  const long long units = static_cast<long long>(B) * H * ((max_seqlen + 127) / 128);
+  if (units <= 2LL * st.num_sms && small_ok) return pipeline ? KC_TC_SMALL : KC_MMA;
+  return KC_TC;
 }
 
 rra_status enqueue_pack(const DeviceState& st, const uint8_t* keep, int B, int N, int H, int d,
@@ -255,10 +269,13 @@ rra_status enqueue_attend(const DeviceState& st, const void* qp, const void* kp,
   a.err = error_word(st);
   a.wait_limit = g_wait_limit.load();
   cudaError_t e;
-  if (!coalesced_out && use_tcgen05(st, B, H)) {
+  const AttendKernelChoice kc = coalesced_out ? KC_MMA : attend_choice(st, B, H, max_seqlen, false);
+  if (kc == KC_TC) {
     if (!attend_tc_available())
       return fail(RRA_ERR_CUDA, "attend: the driver's tensor-map encoder is unavailable");
     e = launch_attend_tc(a, in, out_dt, st.num_sms, s, ctas);
+  } else if (kc == KC_TC_SMALL) {
+    e = launch_attend_small(a, in, out_dt, false, s, ctas);
   } else {
     e = launch_attend(a, in, out_dt, s, ctas);
   }
@@ -347,7 +364,9 @@ rra_status enqueue_pipeline(const DeviceState& st, const PipelineArgs& p, cudaSt
     a.scale_log2 = p.scale * 1.4426950408889634f;
     a.err = error_word(st);
     a.wait_limit = g_wait_limit.load();
-    cudaError_t e = launch_attend_tc_fused(a, p.in, p.out_dt, st.num_sms, s);
+    cudaError_t e = attend_choice(st, p.B, p.H, p.N, true) == KC_TC_SMALL
+                        ? launch_attend_small(a, p.in, p.out_dt, true, s)
+                        : launch_attend_tc_fused(a, p.in, p.out_dt, st.num_sms, s);
     if (e != cudaSuccess) return cuda_fail(e, "fused pipeline launch");
     return RRA_OK;
   }
@@ -410,7 +429,9 @@ const char* rra_last_error_message(void) { return g_last_message; }
 uint64_t rra_launch_count(void) { return g_launches.load(); }
 
 int rra_set_attend_kernel(int kernel) {
-  if (kernel != RRA_ATTEND_TCGEN05 && kernel != RRA_ATTEND_MMA_SYNC && kernel != RRA_ATTEND_AUTO) return -1;
+  if (kernel != RRA_ATTEND_TCGEN05 && kernel != RRA_ATTEND_MMA_SYNC && kernel != RRA_ATTEND_AUTO &&
+      kernel != RRA_ATTEND_TCGEN05_LATENCY)
+    return -1;
   return g_attend_kernel.exchange(kernel);
 }
 

@@ -132,6 +132,16 @@ cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype
 // (padded), a.o, a.B, a.N, a.H, a.scale_log2, a.err are used.
 cudaError_t launch_attend_tc_fused(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
                                    cudaStream_t stream);
+// Longest image (kept tokens) the small-grid kernel takes: its K and V rows
+// stay in shared memory for the whole unit.
+constexpr int ATTEND_SMALL_MAX_KEYS = 256;
+// Small grids (about one unit per SM): one CTA of four warps per (image,
+// head, query tile), no warp specialisation; max_seqlen <= 256.  fused:
+// the whole pipeline (a.keep scanned, rows gathered from the padded
+// a.qp/kp/vp, every output row written; a.max_seqlen == a.N); else packed
+// inputs as launch_attend_tc.
+cudaError_t launch_attend_small(const AttendArgs& a, rra_dtype in, rra_dtype out, bool fused, cudaStream_t stream,
+                                uint32_t* ctas = nullptr);
 // The same pipeline for keep/q/k/v/o in page-locked host memory (device
 // addresses of the mapping): the rows come in by cp.async copies instead of
 // TMA, every output row leaves by plain stores.

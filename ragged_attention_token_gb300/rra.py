@@ -19,7 +19,7 @@ HEADER_PATH = os.path.join(os.path.dirname(_PKG_DIR), "include", "rra.h")
 
 RRA_OK, RRA_ERR_INVALID_ARG, RRA_ERR_UNSUPPORTED, RRA_ERR_MISALIGNED, RRA_ERR_CUDA, RRA_ERR_DEVICE = range(6)
 RRA_F16, RRA_BF16, RRA_F32 = 0, 1, 2
-ATTEND_TCGEN05, ATTEND_MMA_SYNC, ATTEND_AUTO = 0, 1, 2
+ATTEND_TCGEN05, ATTEND_MMA_SYNC, ATTEND_AUTO, ATTEND_TCGEN05_LATENCY = 0, 1, 2, 3
 DEVERR_NONE, DEVERR_SEQ_TOO_LONG, DEVERR_SEQ_NEGATIVE, DEVERR_INDEX_RANGE, DEVERR_WAIT_TIMEOUT = range(5)
 
 _DTYPE = {torch.float16: RRA_F16, torch.bfloat16: RRA_BF16, torch.float32: RRA_F32}
@@ -356,7 +356,7 @@ def time_null_host(warmup: int, reps: int, stream=None) -> list[float]:
 
 
 def set_attend_kernel(kernel: int) -> int:
-    """Select the attention kernel (ATTEND_TCGEN05, ATTEND_MMA_SYNC or ATTEND_AUTO); returns the previous one."""
+    """Select the attention kernel (ATTEND_TCGEN05, ATTEND_MMA_SYNC, ATTEND_TCGEN05_LATENCY or ATTEND_AUTO); returns the previous one."""
     prev = int(lib().rra_set_attend_kernel(int(kernel)))
     if prev < 0:
         raise ValueError(f"unknown attention kernel {kernel}")

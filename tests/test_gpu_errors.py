@@ -20,7 +20,8 @@ from ragged_attention_token_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [("tcgen05", rra.ATTEND_TCGEN05), ("mma_sync", rra.ATTEND_MMA_SYNC)]
+KERNELS = [("tcgen05", rra.ATTEND_TCGEN05), ("mma_sync", rra.ATTEND_MMA_SYNC),
+           ("tcgen05_latency", rra.ATTEND_TCGEN05_LATENCY)]
 
 
 @pytest.fixture(params=KERNELS, ids=[k[0] for k in KERNELS])
@@ -81,9 +82,10 @@ def _serving_launch(path, case):
     return out, lambda: rra.attend(qp, kp, vp, cu, B, N, out, scale=SCALE, src_idx=src, N=N)
 
 
+@pytest.mark.parametrize("tc", [rra.ATTEND_TCGEN05, rra.ATTEND_TCGEN05_LATENCY], ids=["tcgen05", "tcgen05_latency"])
 @pytest.mark.parametrize("path", ["attend", "pipeline"])
-def test_wait_timeout_is_recorded_and_the_next_call_is_correct(path):
-    prev = rra.set_attend_kernel(rra.ATTEND_TCGEN05)
+def test_wait_timeout_is_recorded_and_the_next_call_is_correct(path, tc):
+    prev = rra.set_attend_kernel(tc)
     try:
         case = W.make_serving(1)
         ref = oracle_result(case)
@@ -105,8 +107,9 @@ def test_wait_timeout_is_recorded_and_the_next_call_is_correct(path):
         rra.set_attend_kernel(prev)
 
 
-def test_plan_records_into_the_word_bound_at_creation():
-    prev = rra.set_attend_kernel(rra.ATTEND_TCGEN05)
+@pytest.mark.parametrize("tc", [rra.ATTEND_TCGEN05, rra.ATTEND_TCGEN05_LATENCY], ids=["tcgen05", "tcgen05_latency"])
+def test_plan_records_into_the_word_bound_at_creation(tc):
+    prev = rra.set_attend_kernel(tc)
     case = W.make_serving(2)
     keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
     B, N, H, d = case.B, case.N, case.H, case.d

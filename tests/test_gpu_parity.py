@@ -40,7 +40,8 @@ CASES = (
 )
 
 
-KERNELS = [("tcgen05", rra.ATTEND_TCGEN05), ("mma_sync", rra.ATTEND_MMA_SYNC)]
+KERNELS = [("tcgen05", rra.ATTEND_TCGEN05), ("mma_sync", rra.ATTEND_MMA_SYNC),
+           ("tcgen05_latency", rra.ATTEND_TCGEN05_LATENCY)]
 DEFAULT_KERNEL = rra.ATTEND_AUTO
 
 
@@ -421,7 +422,7 @@ def test_launch_count_counts_kernels(kernel):
     keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
     n0 = rra.launch_count()
     rra.run_pipeline(keep, q, k, v)
-    assert rra.launch_count() - n0 == (1 if kernel == "tcgen05" else 2)   # fused single launch vs pack + attend
+    assert rra.launch_count() - n0 == (2 if kernel == "mma_sync" else 1)   # fused single launch vs pack + attend
 
 
 def test_attend_kernel_selector():
@@ -433,14 +434,19 @@ def test_attend_kernel_selector():
     rra.set_attend_kernel(prev)
 
 
-@pytest.mark.parametrize("make", [lambda: W.make_serving(4), lambda: W.make_batched(0.8)], ids=["small", "large"])
+@pytest.mark.parametrize("make", [lambda: W.make_serving(4), lambda: W.make_tiny(), lambda: W.make_batched(0.8)],
+                         ids=["serving", "tiny", "large"])
 def test_auto_kernel_matches_explicit(make):
-    """AUTO: the pipeline runs the fused tcgen05 kernel; rra_attend picks mma.sync
-    below one (image, head) pair per SM and tcgen05 above -- bit for bit."""
+    """AUTO, while B*H*ceil(N/128) units fit in one wave of two CTAs per SM
+    (N <= 256): the pipeline runs the small-grid tcgen05 kernel and rra_attend
+    the mma.sync one; beyond, the warp-specialised kernel -- bit for bit."""
     case = make()
-    small = case.B * case.H < torch.cuda.get_device_properties(0).multi_processor_count
+    units = case.B * case.H * ((case.N + 127) // 128)
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    small = units <= 2 * sms and case.N <= 256
+    expect = rra.ATTEND_TCGEN05_LATENCY if small else rra.ATTEND_TCGEN05
     outs = {}
-    for k in (rra.ATTEND_AUTO, rra.ATTEND_TCGEN05):
+    for k in (rra.ATTEND_AUTO, expect):
         prev = rra.set_attend_kernel(k)
         outs[k] = run_pipeline(case)["out"]
         rra.set_attend_kernel(prev)
