@@ -138,8 +138,9 @@ __device__ __forceinline__ void store_pair<__half>(__half* p, float x, float y) 
   *reinterpret_cast<__half2*>(p) = __floats2half2_rn(x, y);
 }
 
+// Returns whether the CTA stored output.
 template <typename Tin, typename Tout, bool SCATTER>
-__device__ __forceinline__ void attend_mma_tile(const AttendArgs& a) {
+__device__ __forceinline__ bool attend_mma_tile(const AttendArgs& a) {
   constexpr bool BF16 = IsBf16<Tin>::value;
   // Q tile, then two stages of (K block, V block); all 64 x 64 x 2 B, 1024-B aligned.
   __shared__ __align__(1024) uint8_t smem[BM * 128 + 2 * 2 * BN * 128];
@@ -149,14 +150,14 @@ __device__ __forceinline__ void attend_mma_tile(const AttendArgs& a) {
   const int n = __ldg(a.cu_seqlens + b + 1) - seq_start;
   if (n < 0) {
     if (qtile == 0 && h == 0 && threadIdx.x == 0) record_error(a.err, RRA_DEVERR_SEQ_NEGATIVE);
-    return;
+    return false;
   }
   if (n > a.max_seqlen) {
     if (qtile == 0 && h == 0 && threadIdx.x == 0) record_error(a.err, RRA_DEVERR_SEQ_TOO_LONG);
-    return;
+    return false;
   }
   const int m0 = qtile * BM;
-  if (m0 >= n) return;
+  if (m0 >= n) return false;
 
   const Tin* qp = static_cast<const Tin*>(a.qp);
   const Tin* kp = static_cast<const Tin*>(a.kp);
@@ -353,14 +354,15 @@ __device__ __forceinline__ void attend_mma_tile(const AttendArgs& a) {
     uint4* gp = reinterpret_cast<uint4*>(out + (static_cast<size_t>(dst_rows[k]) * H + h) * HD) + c;
     *gp = val;
   }
+  return true;
 }
 
 // One CTA per (query tile, head, image); CTAs whose tile lies past the
 // image's length (or whose image has a bad length) return at once.
 template <typename Tin, typename Tout, bool SCATTER>
 __global__ void __launch_bounds__(THREADS) attend_mma_kernel(const AttendArgs a) {
-  attend_mma_tile<Tin, Tout, SCATTER>(a);
-  if (a.done_count != nullptr) signal_done(a);
+  const bool wrote = attend_mma_tile<Tin, Tout, SCATTER>(a);
+  if (a.done_count != nullptr) signal_done(a, wrote);
 }
 
 template <typename Tin, typename Tout>

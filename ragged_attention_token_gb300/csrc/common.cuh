@@ -73,12 +73,16 @@ struct AttendArgs {
 //   otherwise: the count is a device word; the CTA whose add brings it to
 //     done_target publishes done_ticket to the host word with a
 //     system-scope release store.
-// Called by all threads of the CTA (it holds a CTA barrier).
-__device__ __forceinline__ void signal_done(const AttendArgs& a) {
+// Called by all threads of the CTA (it holds a CTA barrier).  `wrote`: the
+// CTA stored output; a CTA that stored nothing adds with a relaxed
+// reduction (it has nothing to publish; the release sequence of the other
+// CTAs' adds continues through it).
+__device__ __forceinline__ void signal_done(const AttendArgs& a, bool wrote = true) {
   __syncthreads();
   if (threadIdx.x == 0) {
     if (a.done_word == nullptr) {
-      asm volatile("red.release.sys.global.add.u32 [%0], 1;" ::"l"(a.done_count) : "memory");
+      if (wrote) asm volatile("red.release.sys.global.add.u32 [%0], 1;" ::"l"(a.done_count) : "memory");
+      else asm volatile("red.relaxed.sys.global.add.u32 [%0], 1;" ::"l"(a.done_count) : "memory");
     } else {
       uint32_t prev;
       asm volatile("atom.acq_rel.gpu.global.add.u32 %0, [%1], 1;" : "=r"(prev) : "l"(a.done_count) : "memory");
