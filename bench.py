@@ -660,13 +660,17 @@ def run_rra(args, world, rank, local):
 
 
 def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
-    """The 12-layer progressive workload at batch B, one CUDA graph per pass, two ways.
+    """The 12-layer progressive workload at batch B, one CUDA graph per pass, three ways.
 
-    chain: layer 1 packs its padded Q/K/V; every later layer receives its Q/K/V
-    in the previous layer's packed layout (as projections of packed features
-    would) and re-packs them at a pruning layer (rra_repack); attention runs on
-    packed buffers; one unpack after the last layer.  per_layer: rra_pipeline
-    (padded in, padded out) for every layer."""
+    Every layer after the first receives its Q/K/V in the previous layer's
+    packed layout (as projections of packed features would).
+    chain (in place): at layer 1 and at each pruning layer an index pass
+    (rra_pack_index) and attention reading the layer's input rows where they
+    are (rra_attend_rows, packed output); rra_attend at the other layers; one
+    unpack after the last layer.  No Q/K/V row is copied.
+    chain_copy: layer 1 packs its padded Q/K/V (rra_pack) and each pruning
+    layer re-packs them (rra_repack) before rra_attend.
+    per_layer: rra_pipeline (padded in, padded out) for every layer."""
     dev = torch.device("cuda", 0)
     masks, cases = W.make_progressive_chain(B)
     N, H, d = cases[0].N, cases[0].H, cases[0].d
@@ -705,6 +709,18 @@ def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
             rra.attend(*src, idx[l][0], B, N, outs[l], scale=SCALE, stream=stream)
         rra.unpack(outs[L - 1], idx[L - 1][1], B, N, final, stream=stream)
 
+    rows = [torch.empty(B * N, dtype=torch.int32, device=dev) if (l == 0 or event[l]) else None for l in range(L)]
+    flat = [tuple(x.view(-1, H, d) for x in inputs[l]) for l in range(L)]
+
+    def chain_in_place():
+        for l in range(L):
+            if l == 0 or event[l]:
+                rra.pack_index(keeps[l], *idx[l], rows[l], dst_prev=None if l == 0 else idx[l - 1][1], stream=stream)
+                rra.attend_rows(*flat[l], rows[l], idx[l][0], B, N, outs[l], scale=SCALE, stream=stream)
+            else:
+                rra.attend(*inputs[l], idx[l][0], B, N, outs[l], scale=SCALE, stream=stream)
+        rra.unpack(outs[L - 1], idx[L - 1][1], B, N, final, stream=stream)
+
     ws = rra.alloc_workspace(B, N, H, d, torch.bfloat16)
     outs_pl = [torch.empty_like(padded[l][0]) for l in range(L)]
 
@@ -712,23 +728,29 @@ def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
         for l in range(L):
             rra.pipeline(keeps[l], *padded[l], outs_pl[l], ws, scale=SCALE, stream=stream)
 
-    t_chain = graph_time_per_launch([chain], stream, reps)
+    t_copy = graph_time_per_launch([chain], stream, reps)
+    t_chain = graph_time_per_launch([chain_in_place], stream, reps)
     t_layer = graph_time_per_launch([per_layer], stream, reps)
     kept = [int((m != 0).sum()) for m in masks]
     row = H * d * 2
-    chain_bytes = B * N + 6 * kept[0] * row + B * N * row + kept[-1] * row
+    # Algorithmic bytes of the in-place chain: per index pass the mask, the
+    # previous dst (pruning layers), dst/src/rows/cu written; per layer Q, K,
+    # V read and O written; the final unpack (packed rows in, padded out).
+    chain_bytes = B * N * row + kept[-1] * row
     for l in range(L):
-        chain_bytes += 4 * kept[l] * row                       # attention: Q, K, V in, O out
-        if l > 0 and event[l]:
-            chain_bytes += B * N + 4 * B * N + 6 * kept[l] * row   # mask, previous dst, rows in and out
+        chain_bytes += 4 * kept[l] * row
+        if l == 0 or event[l]:
+            chain_bytes += B * N + (4 * B * N if l > 0 else 0) + 4 * B * N + 8 * kept[l] + 4 * (B + 1)
     t_min = chain_bytes / (peaks["hbm_gbs"] * 1e9) * 1e6
+    events = sum(event)
     line = {"case": f"progressive_chain_B{B}", "B": B, "N": N, "H": H, "layers": L, "kept_tokens_all_layers": sum(kept),
-            "chain_us": round(t_chain, 2), "per_layer_fused_us": round(t_layer, 2),
+            "chain_us": round(t_chain, 2), "chain_copy_us": round(t_copy, 2), "per_layer_fused_us": round(t_layer, 2),
             "chain_speedup": round(t_layer / t_chain, 3),
             "chain_tokens_per_s": round(sum(kept) / (t_chain * 1e-6), 1),
             "chain_min_us": round(t_min, 2), "chain_frac": round(t_min / t_chain, 4),
-            "launches_chain": 1 + L + sum(event) + 1, "launches_per_layer": L}
-    del padded, inputs, packed, outs, outs_pl, final, ws
+            "launches_chain": 2 * (1 + events) + (L - 1 - events) + 1,
+            "launches_chain_copy": 1 + L + events + 1, "launches_per_layer": L}
+    del padded, inputs, packed, outs, outs_pl, final, ws, rows, flat
     torch.cuda.empty_cache()
     return line
 

@@ -130,6 +130,24 @@ RRA_API rra_status rra_repack(const uint8_t* keep_new, const int32_t* dst_prev, 
                               const void* vp_prev, int32_t* cu_seqlens, int32_t* dst_idx,
                               int32_t* src_idx, void* qp, void* kp, void* vp, void* stream);
 
+/* The index pass of rra_pack / rra_repack alone, for attention that reads
+ * its rows in place (rra_attend_rows) instead of from a packed copy.
+ *   keep      uint8 [B, N]: the layer's mask over the ORIGINAL positions;
+ *   dst_prev  NULL (first layer), or the previous layer's dst_idx [B*N]
+ *             (keep must then be a subset of the previous layer's mask);
+ *   rows      NULL, or int32 [B*N]: rows[t] for every packed row t < T =
+ *             cu_seqlens[B] is the row holding that token's data in the
+ *             layer's input: src_idx[t] (the flat position, padded input)
+ *             without dst_prev, dst_prev[src_idx[t]] (the row in the
+ *             previous layer's packed buffers) with it.
+ * Writes cu_seqlens, dst_idx and src_idx exactly as rra_pack(keep) does; no
+ * row is copied.  A kept position that dst_prev marks pruned records
+ * RRA_DEVERR_INDEX_RANGE and gets rows[t] = -1.  dst_prev must not be dst_idx
+ * (RRA_ERR_INVALID_ARG).  One launch, asynchronous on `stream`. */
+RRA_API rra_status rra_pack_index(const uint8_t* keep, const int32_t* dst_prev, int B, int N,
+                                  int32_t* cu_seqlens, int32_t* dst_idx, int32_t* src_idx, int32_t* rows,
+                                  void* stream);
+
 /* Packed linear layer: the rest of a ViT block (QKV projection, output
  * projection, MLP) on the compact buffer, so pruned tokens cost no multiplies
  * there either (article, problem section: padding wastes bandwidth and
@@ -217,6 +235,22 @@ RRA_API rra_status rra_attend_gather(const void* q, const void* k, const void* v
                                      const int32_t* cu_seqlens, const int32_t* src_idx, int B, int N,
                                      int H, int d, float scale, rra_dtype in_dtype, void* out,
                                      rra_dtype out_dtype, void* stream);
+
+/* rra_attend with the pack's row copy folded into the tile loads: the
+ * sequence of image b is packed rows t = cu[b] .. cu[b+1]-1 as usual, but the
+ * Q/K/V data of row t is read from row rows[t] of q/k/v [src_rows, H, d]
+ * (TMA gather of 4 rows at a time), and the output is packed: o[t] for
+ * t < T (o [cap, H, d], rows >= T untouched).  With rows from
+ * rra_pack_index this is one layer of progressive pruning without a packed
+ * copy: padded q/k/v (src_rows = B*N) at the first layer, the previous
+ * layer's packed q/k/v at a pruning layer.  max_seqlen bounds every image's
+ * length (longer images record RRA_DEVERR_SEQ_TOO_LONG and are skipped); a
+ * row outside [0, src_rows) records RRA_DEVERR_INDEX_RANGE (its data read
+ * as row 0's).  tcgen05 kernel only; one launch. */
+RRA_API rra_status rra_attend_rows(const void* q, const void* k, const void* v, long long src_rows,
+                                   const int32_t* rows, const int32_t* cu_seqlens, int B, int max_seqlen,
+                                   int H, int d, float scale, rra_dtype in_dtype, void* o,
+                                   rra_dtype out_dtype, void* stream);
 
 /* Unpack (method overview, bullet 3): out[b, j] = op[dst_idx[b*N+j]] when
  * dst_idx >= 0, else +0.  `op` is packed [cap, H, d] and `out` padded

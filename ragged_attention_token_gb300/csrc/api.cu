@@ -160,9 +160,11 @@ AttendKernelChoice attend_choice(const DeviceState& st, int B, int H, int max_se
 rra_status enqueue_pack(const DeviceState& st, const uint8_t* keep, int B, int N, int H, int d,
                         rra_dtype in, const void* q, const void* k, const void* v, int32_t* cu,
                         int32_t* dst, int32_t* src, void* qp, void* kp, void* vp, void* outz,
-                        rra_dtype out_dt, cudaStream_t s, const int32_t* src_rows = nullptr) {
+                        rra_dtype out_dt, cudaStream_t s, const int32_t* src_rows = nullptr,
+                        int32_t* rows_out = nullptr) {
   PackArgs a{};
   a.src_rows = src_rows;
+  a.rows_out = rows_out;
   a.src_cap = static_cast<long long>(B) * N;
   a.err = error_word(st);
   a.keep = keep;
@@ -511,6 +513,21 @@ rra_status rra_repack(const uint8_t* keep_new, const int32_t* dst_prev, int B, i
   return RRA_OK;
 }
 
+rra_status rra_pack_index(const uint8_t* keep, const int32_t* dst_prev, int B, int N, int32_t* cu_seqlens,
+                          int32_t* dst_idx, int32_t* src_idx, int32_t* rows, void* stream) {
+  RRA_TRY(check_shape(B, N, 1, 64));
+  if (keep == nullptr) return fail(RRA_ERR_INVALID_ARG, "keep is null");
+  if (cu_seqlens == nullptr || dst_idx == nullptr || src_idx == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "index buffer is null");
+  if (dst_prev != nullptr && dst_prev == dst_idx) return fail(RRA_ERR_INVALID_ARG, "dst_prev is dst_idx");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  RRA_TRY(enqueue_pack(*st, keep, B, N, 1, 64, RRA_BF16, nullptr, nullptr, nullptr, cu_seqlens, dst_idx, src_idx,
+                       nullptr, nullptr, nullptr, nullptr, RRA_F32, static_cast<cudaStream_t>(stream), dst_prev, rows));
+  g_launches += 1;
+  return RRA_OK;
+}
+
 rra_status rra_linear_packed(const void* a, const void* w, const float* bias, const int32_t* cu_seqlens, int B,
                              int cap, int K, int N, rra_dtype in_dtype, void* c, rra_dtype out_dtype,
                              void* stream) {
@@ -661,6 +678,37 @@ rra_status rra_attend_gather(const void* q, const void* k, const void* v, const 
   a.wait_limit = g_wait_limit.load();
   cudaError_t e = launch_attend_tc_gather(a, in_dtype, out_dtype, st->num_sms, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return cuda_fail(e, "attend (gather) launch");
+  g_launches += 1;
+  return RRA_OK;
+}
+
+rra_status rra_attend_rows(const void* q, const void* k, const void* v, long long src_rows, const int32_t* rows,
+                           const int32_t* cu_seqlens, int B, int max_seqlen, int H, int d, float scale,
+                           rra_dtype in_dtype, void* o, rra_dtype out_dtype, void* stream) {
+  RRA_TRY(check_attend(q, k, v, cu_seqlens, B, max_seqlen, H, d, scale, in_dtype, o, out_dtype, nullptr, 0));
+  if (rows == nullptr) return fail(RRA_ERR_INVALID_ARG, "rows is null");
+  if (src_rows < 1) return fail(RRA_ERR_INVALID_ARG, "src_rows=%lld < 1", src_rows);
+  if (src_rows * H * d >= (1LL << 31)) return fail(RRA_ERR_UNSUPPORTED, "src_rows*H*d >= 2^31");
+  if (!attend_tc_available()) return fail(RRA_ERR_CUDA, "attend_rows: tensor-map encoder unavailable");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  AttendArgs a{};
+  a.qp = q;
+  a.kp = k;
+  a.vp = v;
+  a.cu_seqlens = cu_seqlens;
+  a.src_idx = rows;
+  a.src_rows = src_rows;
+  a.o = o;
+  a.B = B;
+  a.H = H;
+  a.N = max_seqlen;
+  a.max_seqlen = max_seqlen;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = error_word(*st);
+  a.wait_limit = g_wait_limit.load();
+  cudaError_t e = launch_attend_tc_rows(a, in_dtype, out_dtype, st->num_sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attend (rows) launch");
   g_launches += 1;
   return RRA_OK;
 }

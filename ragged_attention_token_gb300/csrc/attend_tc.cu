@@ -327,6 +327,17 @@ __device__ Unit next_unit_fused(int u, int step, int units, int BH, const Attend
 
 
 
+// Source row of packed row t for the gather loads; a row outside [0, lim)
+// records RRA_DEVERR_INDEX_RANGE and reads row 0 instead.
+__device__ __forceinline__ int gather_row(const AttendArgs& a, int t, long long lim) {
+  const int r = __ldg(a.src_idx + t);
+  if (r < 0 || r >= lim) {
+    record_error(a.err, RRA_DEVERR_INDEX_RANGE);
+    return 0;
+  }
+  return r;
+}
+
 template <typename Tin, typename Tout, bool SCATTER, int MODE, bool LIMIT>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
@@ -339,12 +350,12 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   constexpr bool ZF_BULK = MODE == MODE_FUSED;
   constexpr int ZF = ZF_BULK ? ZF_BULK_TOKENS : (MODE == MODE_FUSED_HOST ? ZF_LIST_TOKENS : ZF_MASK_ROWS);
   constexpr bool HOSTLD = MODE == MODE_FUSED_HOST;   // cp.async loads (no tensor maps)
-  // On packed inputs, 16-bit outputs of tiles with more than 64 rows leave
+  // On packed or row-gathered inputs, 16-bit outputs of tiles with more than 64 rows leave
   // through the unit's last K/V stage (whole rows per store instruction);
   // smaller tiles (where the extra round trip through shared memory costs
   // more than it saves), fp32 outputs and the fused modes (whose producer
   // needs that stage back sooner) store row by row.
-  constexpr bool STAGED = sizeof(Tout) == 2 && MODE == MODE_PACKED;
+  constexpr bool STAGED = sizeof(Tout) == 2 && (MODE == MODE_PACKED || MODE == MODE_GATHER);
   constexpr int STAGE_MIN_ROWS = 65;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
@@ -411,6 +422,8 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
   // The bound on one wait: a compile-time constant, except in the
   // instantiation for a launch made with a wait limit set (rra_set_wait_limit).
   const long long wlimit = LIMIT ? a.wait_limit : WAIT_LIMIT_CYCLES;
+  // Rows the gather loads may read (row-gather inputs span a.src_rows rows).
+  const long long src_lim = a.src_rows > 0 ? a.src_rows : static_cast<long long>(a.B) * a.N;
   bool bad = false;
 
   if (warp == PRODUCER_WARP) {
@@ -516,7 +529,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
               for (int i = 0; i < 4; ++i) {
                 const int t = min(U.q0 + 4 * lane + i, U.q0 + U.rows_q - 1);
                 if constexpr (FUSED) rows[i] = (U.b * a.N + ld_shared_u16(pslot + 2 * t)) * a.H + U.h;
-                else rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+                else rows[i] = gather_row(a, U.s0 + t, src_lim) * a.H + U.h;
               }
               tma_gather4(sQ + lane * 512, &tmap_q, rows, bar_full(st));
             }
@@ -527,7 +540,7 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
               for (int i = 0; i < 4; ++i) {
                 const int t = min(k0 + 4 * g + i, k0 + n_c - 1);
                 if constexpr (FUSED) rows[i] = (U.b * a.N + ld_shared_u16(pslot + 2 * t)) * a.H + U.h;
-                else rows[i] = __ldg(a.src_idx + U.s0 + t) * a.H + U.h;
+                else rows[i] = gather_row(a, U.s0 + t, src_lim) * a.H + U.h;
               }
               if (lane < 16) tma_gather4(sK(st) + g * 512, &tmap_k, rows, bar_full(st));
               else tma_gather4(sV(st) + g * 512, &tmap_v, rows, bar_full(st));
@@ -928,7 +941,7 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
   if constexpr (MODE == MODE_FUSED_HOST) {
     // cp.async loads: the kernel takes no tensor map (the zeroed ones are unused).
   } else if constexpr (MODE != MODE_PACKED) {
-    const long long rows = static_cast<long long>(a.B) * a.N * a.H;
+    const long long rows = (a.src_rows > 0 ? a.src_rows : static_cast<long long>(a.B) * a.N) * a.H;
     if ((e = make_gather_map(&mq, a.qp, rows, bf16)) != cudaSuccess) return e;
     if ((e = make_gather_map(&mk, a.kp, rows, bf16)) != cudaSuccess) return e;
     if ((e = make_gather_map(&mv, a.vp, rows, bf16)) != cudaSuccess) return e;
@@ -988,7 +1001,10 @@ cudaError_t launch_tc_out(const AttendArgs& a, int mode, int num_sms, cudaStream
     return launch_tc_lim<Tin, Tout, true, MODE_FUSED>(a, num_sms, stream, ctas);
   }
   if (mode == MODE_FUSED_HOST) return launch_tc_lim<Tin, Tout, true, MODE_FUSED_HOST>(a, num_sms, stream, ctas);
-  if (mode == MODE_GATHER) return launch_tc_lim<Tin, Tout, true, MODE_GATHER>(a, num_sms, stream, ctas);
+  if (mode == MODE_GATHER) {
+    if (a.src_rows > 0) return launch_tc_lim<Tin, Tout, false, MODE_GATHER>(a, num_sms, stream, ctas);
+    return launch_tc_lim<Tin, Tout, true, MODE_GATHER>(a, num_sms, stream, ctas);
+  }
   if (a.src_idx != nullptr) return launch_tc_lim<Tin, Tout, true, MODE_PACKED>(a, num_sms, stream, ctas);
   return launch_tc_lim<Tin, Tout, false, MODE_PACKED>(a, num_sms, stream, ctas);
 }
@@ -1017,6 +1033,15 @@ cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype
                                     cudaStream_t stream) {
   if (!encode_fn()) return cudaErrorNotSupported;
   if (a.src_idx == nullptr) return cudaErrorInvalidValue;
+  if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, MODE_GATHER, num_sms, stream);
+  return launch_tc_in<__half>(a, out, MODE_GATHER, num_sms, stream);
+}
+
+cudaError_t launch_attend_tc_rows(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
+                                  cudaStream_t stream) {
+  if (!encode_fn()) return cudaErrorNotSupported;
+  if (a.src_idx == nullptr || a.src_rows < 1 || a.src_rows * a.H >= (1LL << 31)) return cudaErrorInvalidValue;
+  if (static_cast<long long>(a.B) * a.max_seqlen >= (1LL << 31)) return cudaErrorInvalidValue;
   if (in == RRA_BF16) return launch_tc_in<__nv_bfloat16>(a, out, MODE_GATHER, num_sms, stream);
   return launch_tc_in<__half>(a, out, MODE_GATHER, num_sms, stream);
 }

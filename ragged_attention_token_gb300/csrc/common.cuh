@@ -38,6 +38,9 @@ struct PackArgs {
   // (a previous layer's packed buffers, src_cap rows) instead of row g.
   const int32_t* src_rows;
   long long src_cap;
+  // Optional: rows_out[t] = the row copied (or, with row_vecs == 0, to be
+  // read) for packed row t: src_rows[g], or g itself without src_rows.
+  int32_t* rows_out;
   int32_t* err;
 };
 
@@ -60,6 +63,10 @@ struct AttendArgs {
   uint32_t* done_word;      // device address of a page-locked host word, or nullptr
   uint32_t done_ticket;     // value published to *done_word
   long long wait_limit;     // clock cycles one on-chip wait may take before giving up (0: the default)
+  // Row-gather inputs with a packed output (launch_attend_tc_rows): q/k/v
+  // span src_rows rows and packed row t is read from row src_idx[t].
+  // 0: the padded gather (B*N rows, output scattered to src_idx).
+  long long src_rows;
 };
 
 // Each CTA adds one to *done_count once all its threads' output stores are
@@ -130,6 +137,10 @@ cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, i
 // tensors (a.qp/kp/vp) at rows src_idx[t], scattering to the padded output.
 cudaError_t launch_attend_tc_gather(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
                                     cudaStream_t stream);
+// Same kernel reading packed row t of Q/K/V from row a.src_idx[t] of the
+// [a.src_rows, H, 64] buffers a.qp/kp/vp and writing the packed output row t.
+cudaError_t launch_attend_tc_rows(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms,
+                                  cudaStream_t stream);
 // The whole pipeline in one launch: the same kernel scanning the keep mask
 // per image, gathering from the padded q/k/v, writing every output row
 // (attention at kept positions, +0 at pruned ones).  a.keep, a.qp/kp/vp

@@ -117,6 +117,7 @@ __global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const PackArgs a) {
             srow = -1;
           }
         }
+        if (a.rows_out != nullptr) a.rows_out[excl] = static_cast<int32_t>(srow);
         s_kept_src[local_rank] = srow;
         s_kept_dst[local_rank] = excl;
       } else {

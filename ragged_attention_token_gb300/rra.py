@@ -40,6 +40,8 @@ _SIGNATURES = {
     "rra_linear_packed": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _i, _vp, _i, _vp]),
     "rra_topk_keep": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "rra_attend_gather": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "rra_pack_index": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
+    "rra_attend_rows": (_i, [_vp, _vp, _vp, ctypes.c_longlong, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "rra_unpack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "rra_pipeline": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
     "rra_pipeline_static": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
@@ -218,6 +220,21 @@ def attend_gather(q, k, v, cu_seqlens, src_idx, out, scale: float = 0.125, strea
     B, N, H, d = q.shape
     _check(lib().rra_attend_gather(_ptr(q), _ptr(k), _ptr(v), _ptr(cu_seqlens), _ptr(src_idx), B, N, H, d,
                                    float(scale), _DTYPE[q.dtype], _ptr(out), _DTYPE[out.dtype], _stream(stream)))
+
+
+def pack_index(keep, cu_seqlens, dst_idx, src_idx, rows=None, dst_prev=None, stream=None):
+    """rra_pack_index: cu_seqlens/dst_idx/src_idx of `keep` and (optionally) the input row of each packed row."""
+    B, N = keep.shape
+    _check(lib().rra_pack_index(_ptr(keep), _ptr(dst_prev), B, N, _ptr(cu_seqlens), _ptr(dst_idx), _ptr(src_idx),
+                                _ptr(rows), _stream(stream)))
+
+
+def attend_rows(q, k, v, rows, cu_seqlens, B: int, max_seqlen: int, o, scale: float = 0.125, stream=None):
+    """rra_attend_rows: packed attention whose row t is read from row rows[t] of q/k/v [src_rows, H, d]."""
+    H, d = q.shape[-2], q.shape[-1]
+    src_rows = q.numel() // (H * d)
+    _check(lib().rra_attend_rows(_ptr(q), _ptr(k), _ptr(v), src_rows, _ptr(rows), _ptr(cu_seqlens), B, max_seqlen,
+                                 H, d, float(scale), _DTYPE[q.dtype], _ptr(o), _DTYPE[o.dtype], _stream(stream)))
 
 
 def unpack(op, dst_idx, B: int, N: int, out, stream=None):

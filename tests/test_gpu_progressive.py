@@ -15,7 +15,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import ATOL, SCALE, bits
+from gpu_util import ATOL, SCALE, bits, out_tolerance
 from ragged_attention_token_gb300 import rra
 from ragged_attention_token_gb300 import workloads as W
 
@@ -98,6 +98,121 @@ def test_repack_flags_positions_pruned_before():
     assert np.array_equal(bits(packed[0])[: len(good)][good], want[good])
 
 
+def test_pack_index_matches_oracle():
+    """rra_pack_index: the indices of rra_pack and, per packed row, the row of the layer's input holding it."""
+    masks, cases = W.make_progressive_chain(B=16)
+    B, N = cases[0].B, cases[0].N
+    for layer in (1,) + tuple(W.PROGRESSIVE_EVENTS):
+        keep_np = masks[layer - 1].numpy()
+        cu_r, dst_r, src_r = oracle.pack_indices(keep_np)
+        T = int(cu_r[-1])
+        cu, dst, src = _index_buffers(B, N)
+        rows = torch.full((B * N,), -9, dtype=torch.int32, device="cuda")
+        dst_prev = None
+        if layer == 1:
+            rows_r = src_r                                    # padded input: the flat position
+        else:
+            _, dst_prev_r, _ = oracle.pack_indices(masks[layer - 2].numpy())
+            rows_r = dst_prev_r[src_r]                         # the row in the previous packed layout
+            dst_prev = torch.from_numpy(dst_prev_r).cuda()
+        rra.get_device_error(clear=True)
+        rra.pack_index(masks[layer - 1].cuda(), cu, dst, src, rows, dst_prev=dst_prev)
+        torch.cuda.synchronize()
+        assert rra.get_device_error() == 0
+        assert np.array_equal(cu.cpu().numpy(), cu_r)
+        assert np.array_equal(dst.cpu().numpy(), dst_r)
+        assert np.array_equal(src.cpu().numpy()[:T], src_r)
+        got_rows = rows.cpu().numpy()
+        assert np.array_equal(got_rows[:T], rows_r), f"layer {layer}: rows differ"
+        assert np.all(got_rows[T:] == -9), "rows past T written"
+
+
+def test_pack_index_flags_positions_pruned_before():
+    masks, cases = W.make_progressive_chain(B=4)
+    B, N = cases[0].B, cases[0].N
+    prev = masks[3].clone()
+    drop = int(torch.nonzero(prev[1])[-1])
+    prev[1, drop] = 0
+    _, dst_prev_r, _ = oracle.pack_indices(prev.numpy())
+    cu_r, dst_r, src_r = oracle.pack_indices(masks[3].numpy())
+    cu, dst, src = _index_buffers(B, N)
+    rows = torch.full((B * N,), -9, dtype=torch.int32, device="cuda")
+    rra.get_device_error(clear=True)
+    rra.pack_index(masks[3].cuda(), cu, dst, src, rows, dst_prev=torch.from_numpy(dst_prev_r).cuda())
+    torch.cuda.synchronize()
+    assert rra.get_device_error(clear=True) == rra.DEVERR_INDEX_RANGE
+    T = int(cu_r[-1])
+    want = dst_prev_r[src_r]
+    assert np.array_equal(cu.cpu().numpy(), cu_r)
+    got = rows.cpu().numpy()[:T]
+    assert got[dst_r[1 * N + drop]] == -1
+    assert np.array_equal(got, want)                       # want holds -1 there too
+
+
+def _attend_rows_reference(case, src_r, cu_r):
+    p64 = [oracle.pack_rows(x.double().numpy(), src_r) for x in (case.q, case.k, case.v)]
+    return oracle.attend(*p64, cu_r, SCALE)
+
+
+@pytest.mark.parametrize("in_dtype", [torch.bfloat16, torch.float16], ids=["bf16", "f16"])
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16, torch.float16], ids=["f32o", "bf16o", "f16o"])
+@pytest.mark.parametrize("source", ["padded", "previous_packed"])
+def test_attend_rows_matches_oracle(source, out_dtype, in_dtype):
+    """rra_attend_rows at the first layer (rows of the padded input) and at a
+    pruning layer (rows of the previous layer's packed buffers)."""
+    masks, cases = W.make_progressive_chain(B=16)
+    layer = W.PROGRESSIVE_EVENTS[0]
+    case = cases[layer - 1]
+    B, N, H, d = case.B, case.N, case.H, case.d
+    qkv = [x.to(in_dtype) for x in (case.q, case.k, case.v)]
+    keep_np = case.keep.numpy()
+    cu_r, dst_r, src_r = oracle.pack_indices(keep_np)
+    T = int(cu_r[-1])
+    ref_case = type("C", (), {})()
+    ref_case.q, ref_case.k, ref_case.v = qkv
+    o_ref = _attend_rows_reference(ref_case, src_r, cu_r)
+    q, k, v = (x.cuda() for x in qkv)
+    if source == "padded":
+        src_in = (q.view(B * N, H, d), k.view(B * N, H, d), v.view(B * N, H, d))
+        rows_r = src_r
+    else:
+        prev = masks[layer - 2].numpy()
+        _, dst_prev_r, src_prev_r = oracle.pack_indices(prev)
+        src_in = tuple(torch.full((B * N, H, d), float("nan"), dtype=in_dtype, device="cuda") for _ in range(3))
+        Tp = len(src_prev_r)
+        for buf, x in zip(src_in, (q, k, v)):
+            buf[:Tp] = x.view(B * N, H, d)[torch.from_numpy(src_prev_r).long().cuda()]
+        rows_r = dst_prev_r[src_r]
+    rows = torch.from_numpy(rows_r.astype(np.int32)).cuda()
+    cu = torch.from_numpy(cu_r).cuda()
+    o = torch.full((B * N, H, d), float("nan"), dtype=out_dtype, device="cuda")
+    rra.get_device_error(clear=True)
+    rra.attend_rows(*src_in, rows, cu, B, N, o, scale=SCALE)
+    torch.cuda.synchronize()
+    assert rra.get_device_error() == 0
+    got = o[:T].cpu()
+    err = np.abs(got.double().numpy() - o_ref)
+    tol = out_tolerance(o_ref, out_dtype)
+    assert np.all(err <= tol), f"max-abs error {err.max():.3e}"
+    assert torch.isnan(o[T:].float()).all(), "rows past T written"
+
+
+def test_attend_rows_flags_a_row_out_of_range():
+    masks, cases = W.make_progressive_chain(B=4)
+    case = cases[0]
+    B, N, H, d = case.B, case.N, case.H, case.d
+    cu_r, dst_r, src_r = oracle.pack_indices(case.keep.numpy())
+    rows_r = src_r.astype(np.int32).copy()
+    rows_r[3] = B * N                                      # one past the last row
+    q, k, v = (x.cuda().view(B * N, H, d) for x in (case.q, case.k, case.v))
+    o = torch.empty((B * N, H, d), dtype=torch.float32, device="cuda")
+    rra.get_device_error(clear=True)
+    rra.attend_rows(q, k, v, torch.from_numpy(rows_r).cuda(), torch.from_numpy(cu_r).cuda(), B, N, o, scale=SCALE)
+    torch.cuda.synchronize()
+    assert rra.get_device_error(clear=True) == rra.DEVERR_INDEX_RANGE
+    assert torch.isfinite(o[: len(src_r)]).all()
+
+
 def _run_chain(cases, inputs, bufs, B, N):
     """The chain after its inputs are in place: pack, attend, re-pack at pruning layers, final unpack."""
     first = cases[0]
@@ -176,3 +291,80 @@ def test_progressive_chain_matches_oracle_and_replays_in_a_graph(kernel):
     torch.cuda.synchronize()
     for a, b in zip(eager, bufs["out"] + [bufs["final"]]):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+def _run_chain_in_place(cases, inputs, bufs, B, N):
+    """The chain without packed copies: at the first layer and at every pruning
+    layer an index pass (rra_pack_index) and attention reading the layer's
+    input rows in place (rra_attend_rows); rra_attend elsewhere; final unpack."""
+    for l in range(len(cases)):
+        cu = bufs["idx"][l][0]
+        if l == 0 or bufs["event"][l]:
+            dst_prev = None if l == 0 else bufs["idx"][l - 1][1]
+            src_in = tuple(x.view(-1, x.shape[-2], x.shape[-1]) for x in inputs[l])
+            rra.pack_index(bufs["keep"][l], *bufs["idx"][l], bufs["rows"][l], dst_prev=dst_prev)
+            rra.attend_rows(*src_in, bufs["rows"][l], cu, B, N, bufs["out"][l], scale=SCALE)
+        else:
+            rra.attend(*inputs[l], cu, B, N, bufs["out"][l], scale=SCALE)
+    last = len(cases) - 1
+    rra.unpack(bufs["out"][last], bufs["idx"][last][1], B, N, bufs["final"])
+
+
+@pytest.mark.parametrize("out_dtype", [torch.float32, torch.bfloat16], ids=["f32o", "bf16o"])
+def test_progressive_chain_in_place_matches_oracle_and_replays_in_a_graph(out_dtype):
+    masks, cases = W.make_progressive_chain(B=16)
+    B, N, H, d = cases[0].B, cases[0].N, cases[0].H, cases[0].d
+    L = len(cases)
+    inputs = []
+    for l, case in enumerate(cases):
+        q, k, v = (x.cuda() for x in (case.q, case.k, case.v))
+        if l == 0:
+            inputs.append((q, k, v))
+        else:
+            _, _, _, packed_prev = _pack(masks[l - 1].cuda(), q, k, v)
+            inputs.append(tuple(packed_prev))
+    event = [l > 0 and not torch.equal(masks[l], masks[l - 1]) for l in range(L)]
+    idx = []
+    for l in range(L):
+        idx.append(_index_buffers(B, N) if (l == 0 or event[l]) else idx[l - 1])
+    bufs = {
+        "keep": [m.cuda() for m in masks],
+        "event": event,
+        "idx": idx,
+        "rows": [torch.full((B * N,), -9, dtype=torch.int32, device="cuda") if (l == 0 or event[l]) else None
+                 for l in range(L)],
+        "out": [torch.full((B * N, H, d), float("nan"), dtype=out_dtype, device="cuda") for _ in range(L)],
+        "final": torch.full((B, N, H, d), float("nan"), dtype=out_dtype, device="cuda"),
+    }
+    rra.get_device_error(clear=True)
+    _run_chain_in_place(cases, inputs, bufs, B, N)
+    torch.cuda.synchronize()
+    assert rra.get_device_error() == 0
+    for l, case in enumerate(cases):
+        keep_np = case.keep.numpy()
+        cu_r, dst_r, src_r = oracle.pack_indices(keep_np)
+        T = int(cu_r[-1])
+        o_ref = _attend_rows_reference(case, src_r, cu_r)
+        got = bufs["out"][l][:T].cpu().double().numpy()
+        err = np.abs(got - o_ref)
+        assert np.all(err <= out_tolerance(o_ref, out_dtype)), f"layer {l + 1}: max-abs error {err.max()}"
+        if l == L - 1:
+            want = oracle.unpack(o_ref, dst_r, B, N)
+            fin = bufs["final"].cpu()
+            m = keep_np != 0
+            assert np.all(bits(fin)[~m] == 0)
+            e = np.abs(fin.double().numpy()[m] - want[m])
+            assert np.all(e <= out_tolerance(want[m], out_dtype))
+    eager = [o.clone() for o in bufs["out"]] + [bufs["final"].clone()]
+    for o in bufs["out"] + [bufs["final"]]:
+        o.fill_(float("nan"))
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    with torch.cuda.stream(side):
+        with torch.cuda.graph(graph, stream=side):
+            _run_chain_in_place(cases, inputs, bufs, B, N)
+    graph.replay()
+    torch.cuda.synchronize()
+    for a, b in zip(eager, bufs["out"] + [bufs["final"]]):
+        assert np.array_equal(bits(a), bits(b))
