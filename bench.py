@@ -660,7 +660,7 @@ def run_rra(args, world, rank, local):
 
 
 def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
-    """The 12-layer progressive workload at batch B, one CUDA graph per pass, three ways.
+    """The 12-layer progressive workload at batch B, one CUDA graph per pass, four ways.
 
     Every layer after the first receives its Q/K/V in the previous layer's
     packed layout (as projections of packed features would).
@@ -670,6 +670,8 @@ def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
     unpack after the last layer.  No Q/K/V row is copied.
     chain_copy: layer 1 packs its padded Q/K/V (rra_pack) and each pruning
     layer re-packs them (rra_repack) before rra_attend.
+    chain_device: the in-place chain with the three pruning decisions made on
+    the device from the attention's class-token side output (rra_prune_index).
     per_layer: rra_pipeline (padded in, padded out) for every layer."""
     dev = torch.device("cuda", 0)
     masks, cases = W.make_progressive_chain(B)
@@ -721,6 +723,35 @@ def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
                 rra.attend(*inputs[l], idx[l][0], B, N, outs[l], scale=SCALE, stream=stream)
         rra.unpack(outs[L - 1], idx[L - 1][1], B, N, final, stream=stream)
 
+    # chain_device: the same chain with every pruning decision made on the
+    # device -- the layer before an event writes the class-token side output
+    # (rra_attend_cls / rra_attend_rows) and one rra_prune_index launch gives
+    # the next layer's indices (the workload's keep fraction, so the kept
+    # counts equal the fixed masks').
+    stride = (N + 15) // 16 * 16
+    cls_bufs = {l - 1: torch.empty((B, H, stride), dtype=torch.float32, device=dev)
+                for l in range(1, L) if event[l]}
+    idx_d = [index_bufs() if (l == 0 or event[l]) else None for l in range(L)]
+    for l in range(L):
+        idx_d[l] = idx_d[l] if idx_d[l] is not None else idx_d[l - 1]
+    rows_d = [torch.empty(B * N, dtype=torch.int32, device=dev) if (l == 0 or event[l]) else None for l in range(L)]
+    num, den = round(W.PROGRESSIVE_KEEP * 10), 10
+
+    def chain_device():
+        rra.pack_index(keeps[0], *idx_d[0], rows_d[0], stream=stream)
+        for l in range(L):
+            cls = cls_bufs.get(l)
+            if l == 0 or event[l]:
+                rra.attend_rows(*flat[l], rows_d[l], idx_d[l][0], B, N, outs[l], scale=SCALE, cls=cls, stream=stream)
+            elif cls is not None:
+                rra.attend_cls(*inputs[l], idx_d[l][0], B, N, outs[l], cls, scale=SCALE, stream=stream)
+            else:
+                rra.attend(*inputs[l], idx_d[l][0], B, N, outs[l], scale=SCALE, stream=stream)
+            if cls is not None:
+                rra.prune_index(cls, idx_d[l][0], idx_d[l][2], N, num, den, *idx_d[l + 1], rows_d[l + 1],
+                                stream=stream)
+        rra.unpack(outs[L - 1], idx_d[L - 1][1], B, N, final, stream=stream)
+
     ws = rra.alloc_workspace(B, N, H, d, torch.bfloat16)
     outs_pl = [torch.empty_like(padded[l][0]) for l in range(L)]
 
@@ -730,6 +761,8 @@ def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
 
     t_copy = graph_time_per_launch([chain], stream, reps)
     t_chain = graph_time_per_launch([chain_in_place], stream, reps)
+    t_device = graph_time_per_launch([chain_device], stream, reps)
+    same_counts = all(torch.equal(idx_d[l][0], idx[l][0]) for l in range(L))
     t_layer = graph_time_per_launch([per_layer], stream, reps)
     kept = [int((m != 0).sum()) for m in masks]
     row = H * d * 2
@@ -745,12 +778,14 @@ def progressive_chain_times(rra, stream, peaks, B=256, reps=10):
     events = sum(event)
     line = {"case": f"progressive_chain_B{B}", "B": B, "N": N, "H": H, "layers": L, "kept_tokens_all_layers": sum(kept),
             "chain_us": round(t_chain, 2), "chain_copy_us": round(t_copy, 2), "per_layer_fused_us": round(t_layer, 2),
+            "chain_device_decisions_us": round(t_device, 2), "device_decisions_same_lengths": bool(same_counts),
+            "per_device_decision_us": round((t_device - t_chain) / max(1, sum(event)), 2),
             "chain_speedup": round(t_layer / t_chain, 3),
             "chain_tokens_per_s": round(sum(kept) / (t_chain * 1e-6), 1),
             "chain_min_us": round(t_min, 2), "chain_frac": round(t_min / t_chain, 4),
             "launches_chain": 2 * (1 + events) + (L - 1 - events) + 1,
             "launches_chain_copy": 1 + L + events + 1, "launches_per_layer": L}
-    del padded, inputs, packed, outs, outs_pl, final, ws, rows, flat
+    del padded, inputs, packed, outs, outs_pl, final, ws, rows, flat, cls_bufs, idx_d, rows_d
     torch.cuda.empty_cache()
     return line
 
@@ -775,9 +810,32 @@ def device_pruning_times(rra, stream, B=256, reps=10):
                                                              stream=stream)] * 20, stream, reps)
     t_topk = graph_time_per_launch([lambda: rra.topk_keep(scores, keep, 7, 10, keep_new, stream=stream)] * 20,
                                    stream, reps)
+    # The same step from the attention's class-token side output: the layer's
+    # attention with the side output plus one decision launch, against the
+    # plain attention (tcgen05 kernel both).
+    o = torch.empty((B * N, H, d), dtype=c.dtype, device=dev)
+    cls = torch.empty((B, H, (N + 15) // 16 * 16), dtype=torch.float32, device=dev)
+    keep_cls = torch.empty_like(keep)
+    prev = rra.set_attend_kernel(rra.ATTEND_TCGEN05)
+    try:
+        t_attend = graph_time_per_launch([lambda: rra.attend(qp, kp, vp, cu, B, N, o, scale=SCALE, stream=stream)] * 10,
+                                         stream, reps)
+        t_attend_cls = graph_time_per_launch(
+            [lambda: rra.attend_cls(qp, kp, vp, cu, B, N, o, cls, scale=SCALE, stream=stream)] * 10, stream, reps)
+        t_step = graph_time_per_launch(
+            [lambda: rra.attend_cls(qp, kp, vp, cu, B, N, o, cls, scale=SCALE, stream=stream),
+             lambda: rra.topk_keep_cls(cls, cu, src, N, 7, 10, keep_cls, stream=stream)] * 10, stream, reps) * 2
+    finally:
+        rra.set_attend_kernel(prev)
+    t_topk_cls = graph_time_per_launch([lambda: rra.topk_keep_cls(cls, cu, src, N, 7, 10, keep_cls, stream=stream)]
+                                       * 20, stream, reps)
     return {"case": f"device_pruning_B{B}", "B": B, "N": N, "H": H, "kept_before": int((c.keep != 0).sum()),
             "kept_after": int((keep_new != 0).sum()), "cls_scores_us": round(t_scores, 2),
-            "topk_keep_us": round(t_topk, 2)}
+            "topk_keep_us": round(t_topk, 2),
+            "side_output": {"attend_us": round(t_attend, 2), "attend_cls_us": round(t_attend_cls, 2),
+                            "topk_keep_cls_us": round(t_topk_cls, 2), "attend_cls_and_topk_us": round(t_step, 2),
+                            "pruning_over_attention_us": round(t_step - t_attend, 2),
+                            "same_keep": bool(torch.equal(keep_cls, keep_new))}}
 
 
 def linear_times(rra, stream, peaks, reps=10):

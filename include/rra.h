@@ -250,7 +250,53 @@ RRA_API rra_status rra_attend_gather(const void* q, const void* k, const void* v
 RRA_API rra_status rra_attend_rows(const void* q, const void* k, const void* v, long long src_rows,
                                    const int32_t* rows, const int32_t* cu_seqlens, int B, int max_seqlen,
                                    int H, int d, float scale, rra_dtype in_dtype, void* o,
-                                   rra_dtype out_dtype, void* stream);
+                                   rra_dtype out_dtype, float* cls, int cls_stride, void* stream);
+
+/* rra_attend on packed buffers (src_idx NULL, packed output) that also
+ * writes the class-token attention as a side output, for the pruning step
+ * that follows a layer (EViT-like pruners rank tokens by the class token's
+ * attention; abstract, both revisions):
+ *   cls  float [B, H, cls_stride], 16-byte aligned: cls[b, h, i] for
+ *        i < n_b = cu[b+1] - cu[b] is image b's class token's (its first
+ *        row's) softmax weight, head h, on the image's row i, in fp32 from
+ *        the same scores as the attention's; entries i >= n_b are
+ *        unspecified, images with no rows leave theirs untouched.
+ *   cls_stride  a multiple of 4, >= max_seqlen rounded up to a multiple of 16.
+ * out_dtype must equal in_dtype (else RRA_ERR_UNSUPPORTED).  tcgen05 kernel
+ * at every size; one launch.  rra_attend_rows takes the same two arguments
+ * (cls NULL: no side output). */
+RRA_API rra_status rra_attend_cls(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens,
+                                  int B, int max_seqlen, int H, int d, float scale, rra_dtype in_dtype, void* o,
+                                  rra_dtype out_dtype, float* cls, int cls_stride, void* stream);
+
+/* The pruning decision from that side output, one launch: image b's score
+ * for its row i is the mean over the H heads of cls[b, h, i]; row 0 (the
+ * class token) is kept with the top ceil((n_b-1) * keep_num / keep_den) of
+ * rows 1 .. n_b-1 by score, exactly as rra_topk_keep ranks (equal scores to
+ * the lower position, NaN as -inf).  keep_new [B, N] is written whole, at
+ * the ORIGINAL positions src_idx[cu[b] + i] - b*N (rra_pack's src_idx);
+ * scores, when not NULL, [B, N] receives each kept row's score there and 0
+ * elsewhere (what rra_cls_scores would give).  cls_stride >= N.  An image
+ * with n_b outside [0, N] records a device error and keeps nothing. */
+RRA_API rra_status rra_topk_keep_cls(const float* cls, int cls_stride, const int32_t* cu_seqlens,
+                                     const int32_t* src_idx, int B, int N, int H, int keep_num, int keep_den,
+                                     uint8_t* keep_new, float* scores, void* stream);
+
+/* The whole pruning step between two layers in one launch: the decision of
+ * rra_topk_keep_cls from the side output of the layer before (cu_prev and
+ * src_prev are that layer's indices) and the next layer's indices, exactly
+ * as rra_pack_index(keep_new, dst_prev) would write them: cu_seqlens [B+1],
+ * dst_idx [B*N], src_idx and rows [B*N] (rows[t]: the row of the previous
+ * layer's packed buffers, cu_prev[b] + i, that holds the new row t -- the
+ * input rra_attend_rows reads).  keep_new and scores may be NULL.  Image b's
+ * new length is 1 + ceil((n_b-1) * keep_num / keep_den) (0 for n_b = 0), so
+ * each image's new offset follows from cu_prev alone: every CTA sums the
+ * lengths of the images before it, O(B) reads per image.  The new and
+ * previous index buffers must not alias (RRA_ERR_INVALID_ARG). */
+RRA_API rra_status rra_prune_index(const float* cls, int cls_stride, const int32_t* cu_prev,
+                                   const int32_t* src_prev, int B, int N, int H, int keep_num, int keep_den,
+                                   int32_t* cu_seqlens, int32_t* dst_idx, int32_t* src_idx, int32_t* rows,
+                                   uint8_t* keep_new, float* scores, void* stream);
 
 /* Unpack (method overview, bullet 3): out[b, j] = op[dst_idx[b*N+j]] when
  * dst_idx >= 0, else +0.  `op` is packed [cap, H, d] and `out` padded

@@ -182,6 +182,29 @@ def cls_scores(qp, kp, cu_seqlens, src_idx, N, scale):
     return out
 
 
+def cls_weights(qp, kp, cu_seqlens, scale):
+    """Per head, before the mean: a list over images b of fp64 [H, n_b]
+    arrays, entry [h, i] the softmax weight (scale * <q, k> over the image's
+    rows, head h) of the image's first row on its row i (packed order).
+    Empty images give [H, 0] arrays."""
+    qp = np.asarray(qp, dtype=np.float64)
+    kp = np.asarray(kp, dtype=np.float64)
+    T, H, d = qp.shape
+    B = len(cu_seqlens) - 1
+    out = []
+    for b in range(B):
+        s0, s1 = int(cu_seqlens[b]), int(cu_seqlens[b + 1])
+        w = np.zeros((H, max(s1 - s0, 0)), dtype=np.float64)
+        for h in range(H):
+            if s1 <= s0:
+                break
+            s = scale * (kp[s0:s1, h, :] @ qp[s0, h, :])
+            p = np.exp(s - s.max())
+            w[h] = p / p.sum()
+        out.append(w)
+    return out
+
+
 def topk_keep(scores, keep_prev, num, den):
     """[B, N] uint8: each image's first kept token plus the top
     ceil(m * num / den) of its m other kept tokens by score (descending,

@@ -528,6 +528,49 @@ rra_status rra_pack_index(const uint8_t* keep, const int32_t* dst_prev, int B, i
   return RRA_OK;
 }
 
+rra_status rra_topk_keep_cls(const float* cls, int cls_stride, const int32_t* cu_seqlens, const int32_t* src_idx,
+                             int B, int N, int H, int keep_num, int keep_den, uint8_t* keep_new, float* scores,
+                             void* stream) {
+  RRA_TRY(check_shape(B, N, H, 64));
+  if (cls == nullptr || cu_seqlens == nullptr || src_idx == nullptr || keep_new == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "a required buffer is null");
+  if (cls_stride < N) return fail(RRA_ERR_INVALID_ARG, "cls_stride=%d < N=%d", cls_stride, N);
+  if (static_cast<long long>(B) * H * cls_stride >= (1LL << 31)) return fail(RRA_ERR_UNSUPPORTED, "cls too large");
+  if (keep_den < 1 || keep_num < 0 || keep_num > keep_den)
+    return fail(RRA_ERR_INVALID_ARG, "keep fraction %d/%d outside [0, 1]", keep_num, keep_den);
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  cudaError_t e = launch_prune_cls(cls, cls_stride, cu_seqlens, src_idx, B, N, H, keep_num, keep_den, keep_new, scores,
+                                   nullptr, nullptr, nullptr, nullptr, error_word(*st),
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "topk_keep_cls launch");
+  g_launches += 1;
+  return RRA_OK;
+}
+
+rra_status rra_prune_index(const float* cls, int cls_stride, const int32_t* cu_prev, const int32_t* src_prev, int B,
+                           int N, int H, int keep_num, int keep_den, int32_t* cu_seqlens, int32_t* dst_idx,
+                           int32_t* src_idx, int32_t* rows, uint8_t* keep_new, float* scores, void* stream) {
+  RRA_TRY(check_shape(B, N, H, 64));
+  if (cls == nullptr || cu_prev == nullptr || src_prev == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "cls, cu_prev or src_prev is null");
+  if (cu_seqlens == nullptr || dst_idx == nullptr || src_idx == nullptr || rows == nullptr)
+    return fail(RRA_ERR_INVALID_ARG, "index buffer is null");
+  if (cu_seqlens == cu_prev || src_idx == src_prev) return fail(RRA_ERR_INVALID_ARG, "new and previous indices alias");
+  if (cls_stride < N) return fail(RRA_ERR_INVALID_ARG, "cls_stride=%d < N=%d", cls_stride, N);
+  if (static_cast<long long>(B) * H * cls_stride >= (1LL << 31)) return fail(RRA_ERR_UNSUPPORTED, "cls too large");
+  if (keep_den < 1 || keep_num < 0 || keep_num > keep_den)
+    return fail(RRA_ERR_INVALID_ARG, "keep fraction %d/%d outside [0, 1]", keep_num, keep_den);
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  cudaError_t e = launch_prune_cls(cls, cls_stride, cu_prev, src_prev, B, N, H, keep_num, keep_den, keep_new, scores,
+                                   cu_seqlens, dst_idx, src_idx, rows, error_word(*st),
+                                   static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "prune_index launch");
+  g_launches += 1;
+  return RRA_OK;
+}
+
 rra_status rra_linear_packed(const void* a, const void* w, const float* bias, const int32_t* cu_seqlens, int B,
                              int cap, int K, int N, rra_dtype in_dtype, void* c, rra_dtype out_dtype,
                              void* stream) {
@@ -682,17 +725,65 @@ rra_status rra_attend_gather(const void* q, const void* k, const void* v, const 
   return RRA_OK;
 }
 
+// Checks of the class-token side output shared by rra_attend_cls and rra_attend_rows.
+rra_status check_cls(const float* cls, int cls_stride, int max_seqlen, rra_dtype in_dtype, rra_dtype out_dtype) {
+  if (cls == nullptr) return RRA_OK;
+  if (!aligned16(cls)) return fail(RRA_ERR_MISALIGNED, "cls not 16-byte aligned");
+  if (out_dtype != in_dtype) return fail(RRA_ERR_UNSUPPORTED, "a cls output needs out_dtype == in_dtype");
+  const int need = (max_seqlen + 15) & ~15;
+  if (cls_stride < need || cls_stride % 4 != 0)
+    return fail(RRA_ERR_INVALID_ARG, "cls_stride=%d: a multiple of 4, at least %d", cls_stride, need);
+  return RRA_OK;
+}
+
+rra_status rra_attend_cls(const void* qp, const void* kp, const void* vp, const int32_t* cu_seqlens, int B,
+                          int max_seqlen, int H, int d, float scale, rra_dtype in_dtype, void* o, rra_dtype out_dtype,
+                          float* cls, int cls_stride, void* stream) {
+  RRA_TRY(check_attend(qp, kp, vp, cu_seqlens, B, max_seqlen, H, d, scale, in_dtype, o, out_dtype, nullptr, 0));
+  if (cls == nullptr) return fail(RRA_ERR_INVALID_ARG, "cls is null");
+  RRA_TRY(check_cls(cls, cls_stride, max_seqlen, in_dtype, out_dtype));
+  if (static_cast<long long>(B) * H * cls_stride >= (1LL << 31)) return fail(RRA_ERR_UNSUPPORTED, "cls too large");
+  if (!attend_tc_available()) return fail(RRA_ERR_CUDA, "attend_cls: tensor-map encoder unavailable");
+  DeviceState* st = nullptr;
+  RRA_TRY(device_state(&st));
+  AttendArgs a{};
+  a.qp = qp;
+  a.kp = kp;
+  a.vp = vp;
+  a.cu_seqlens = cu_seqlens;
+  a.o = o;
+  a.B = B;
+  a.H = H;
+  a.N = max_seqlen;
+  a.max_seqlen = max_seqlen;
+  a.scale_log2 = scale * 1.4426950408889634f;
+  a.err = error_word(*st);
+  a.wait_limit = g_wait_limit.load();
+  a.cls = cls;
+  a.cls_stride = cls_stride;
+  cudaError_t e = launch_attend_tc(a, in_dtype, out_dtype, st->num_sms, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return cuda_fail(e, "attend (cls) launch");
+  g_launches += 1;
+  return RRA_OK;
+}
+
 rra_status rra_attend_rows(const void* q, const void* k, const void* v, long long src_rows, const int32_t* rows,
                            const int32_t* cu_seqlens, int B, int max_seqlen, int H, int d, float scale,
-                           rra_dtype in_dtype, void* o, rra_dtype out_dtype, void* stream) {
+                           rra_dtype in_dtype, void* o, rra_dtype out_dtype, float* cls, int cls_stride,
+                           void* stream) {
   RRA_TRY(check_attend(q, k, v, cu_seqlens, B, max_seqlen, H, d, scale, in_dtype, o, out_dtype, nullptr, 0));
   if (rows == nullptr) return fail(RRA_ERR_INVALID_ARG, "rows is null");
   if (src_rows < 1) return fail(RRA_ERR_INVALID_ARG, "src_rows=%lld < 1", src_rows);
   if (src_rows * H * d >= (1LL << 31)) return fail(RRA_ERR_UNSUPPORTED, "src_rows*H*d >= 2^31");
+  RRA_TRY(check_cls(cls, cls_stride, max_seqlen, in_dtype, out_dtype));
+  if (cls != nullptr && static_cast<long long>(B) * H * cls_stride >= (1LL << 31))
+    return fail(RRA_ERR_UNSUPPORTED, "cls too large");
   if (!attend_tc_available()) return fail(RRA_ERR_CUDA, "attend_rows: tensor-map encoder unavailable");
   DeviceState* st = nullptr;
   RRA_TRY(device_state(&st));
   AttendArgs a{};
+  a.cls = cls;
+  a.cls_stride = cls_stride;
   a.qp = q;
   a.kp = k;
   a.vp = v;

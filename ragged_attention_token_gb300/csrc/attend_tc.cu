@@ -54,6 +54,7 @@
 #include <cudaTypedefs.h>
 
 #include <mutex>
+#include <type_traits>
 
 #include "common.cuh"
 #include "tc_ptx.cuh"
@@ -338,7 +339,7 @@ __device__ __forceinline__ int gather_row(const AttendArgs& a, int t, long long 
   return r;
 }
 
-template <typename Tin, typename Tout, bool SCATTER, int MODE, bool LIMIT>
+template <typename Tin, typename Tout, bool SCATTER, int MODE, bool LIMIT, bool CLS>
 __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     attend_tc_kernel(const __grid_constant__ CUtensorMap tmap_q, const __grid_constant__ CUtensorMap tmap_k,
                      const __grid_constant__ CUtensorMap tmap_v, const __grid_constant__ CUtensorMap tmap_q3,
@@ -699,6 +700,10 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     uint32_t uidx = 0, ph_sfull = 0;
     float m_run = 0.f, l_run = 0.f;   // this row's reference (log2 units) and weight sum
     long long out_elem = -1;          // this row's output offset in the current unit
+    float* cls_row = nullptr;         // CLS: the unit's class-token row of a.cls (warp 0, first tile), or null
+    // CLS: the class token's raw scores of the unit so far (lane 0 of warp 0
+    // writes them chunk by chunk; the warp turns them into weights at the end).
+    float* const cls_buf = reinterpret_cast<float*>(gbase + OFF_POS);
     for (uint32_t j = 0;; ++j) {
       const int st = static_cast<int>(j % STAGES);
       bad |= !mbar_wait_or_abort(bar_full(st), (j / STAGES) & 1, abort_flag, wlimit);
@@ -736,6 +741,13 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
           }
         }
         out_elem = dst_row < 0 ? -1 : (dst_row * a.H + h) * HD;
+        if constexpr (CLS) {
+          cls_row = nullptr;
+          if (warp == 0 && q0 == 0) {
+            const int ib = static_cast<int>(ld_shared_u32(d + 32));
+            cls_row = a.cls + (static_cast<size_t>(ib) * a.H + h) * a.cls_stride;
+          }
+        }
       }
       bad |= !mbar_wait_or_abort(bar_sfull, ph_sfull, abort_flag, wlimit);
       ph_sfull ^= 1;
@@ -743,9 +755,26 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
       if (bad) break;
       tc_fence_after();
 
-      if (rows_here) softmax_chunk64<BF>(tS_row, tO_row, nk16, n_c, c, tid < rows_q, c2, m_run, l_run);
+      if constexpr (CLS) {
+        if (rows_here)
+          softmax_chunk64<BF, true>(tS_row, tO_row, nk16, n_c, c, tid < rows_q, c2, m_run, l_run,
+                                    (cls_row != nullptr && lane == 0) ? cls_buf + c * BN : nullptr);
+      } else {
+        if (rows_here) softmax_chunk64<BF>(tS_row, tO_row, nk16, n_c, c, tid < rows_q, c2, m_run, l_run);
+      }
       tc_fence_before();
       mbar_arrive(bar_pready);
+      if constexpr (CLS) {
+        if (last && cls_row != nullptr) {
+          // The class token's row is complete: its raw scores (stashed in
+          // shared memory by lane 0) leave as weights 2^(c2*s - m) / l.
+          const float m0 = __shfl_sync(0xffffffffu, m_run, 0);
+          const float inv = 1.f / __shfl_sync(0xffffffffu, l_run, 0);
+          __syncwarp();
+          for (int i = lane; i < n; i += 32) cls_row[i] = fast_exp2(fmaf(cls_buf[i], c2, -m0)) * inv;
+          __syncwarp();   // read out before lane 0 writes the next unit's scores
+        }
+      }
 
       if (last) {
         // Epilogue: this thread's row, normalised, to the packed or padded output.
@@ -891,13 +920,13 @@ cudaError_t make_gather_map(CUtensorMap* map, const void* ptr, long long rows, b
   return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <typename Tin, typename Tout, bool SCATTER, int MODE, bool LIMIT>
+template <typename Tin, typename Tout, bool SCATTER, int MODE, bool LIMIT, bool CLS>
 cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t stream, uint32_t* ctas) {
   // Largest dynamic shared memory any launch of this instantiation asks for
   // (position lists for N <= 1024 in the fused mode).
   constexpr bool kFused = MODE == MODE_FUSED || MODE == MODE_FUSED_ROWS || MODE == MODE_FUSED_HOST;
-  constexpr uint32_t kMaxSmem = SMEM_ALLOC + (kFused ? POS_SLOTS * 2048u : 0u);
-  auto kernel = attend_tc_kernel<Tin, Tout, SCATTER, MODE, LIMIT>;
+  constexpr uint32_t kMaxSmem = SMEM_ALLOC + (kFused ? POS_SLOTS * 2048u : 0u) + (CLS ? 4096u : 0u);
+  auto kernel = attend_tc_kernel<Tin, Tout, SCATTER, MODE, LIMIT, CLS>;
   static bool attr_set[kMaxDev] = {};
   static uint32_t occ_smem[kMaxDev] = {};
   static int occ_blocks[kMaxDev] = {};
@@ -907,7 +936,9 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
   if (e != cudaSuccess) return e;
   if (dev < 0 || dev >= kMaxDev) return cudaErrorInvalidDevice;
   const int pos_stride = kFused ? ((2 * a.N + 15) & ~15) : 0;
-  const uint32_t smem = SMEM_ALLOC + static_cast<uint32_t>(POS_SLOTS * pos_stride);
+  // CLS: the class-token score buffer (max_seqlen rounded up to 16 floats) where the position lists would be.
+  const uint32_t cls_bytes = CLS ? static_cast<uint32_t>(((a.max_seqlen + 15) & ~15) * 4) : 0u;
+  const uint32_t smem = SMEM_ALLOC + static_cast<uint32_t>(POS_SLOTS * pos_stride) + cls_bytes;
   int per_sm = 0;
   {
     std::lock_guard<std::mutex> lock(m);
@@ -983,14 +1014,24 @@ cudaError_t launch_tc_typed(const AttendArgs& a, int num_sms, cudaStream_t strea
 
 // A launch made with a wait limit set runs its own instantiation, so that the
 // kernels every other launch runs keep the bound a compile-time constant.
-template <typename Tin, typename Tout, bool SCATTER, int MODE>
+template <typename Tin, typename Tout, bool SCATTER, int MODE, bool CLS = false>
 cudaError_t launch_tc_lim(const AttendArgs& a, int num_sms, cudaStream_t stream, uint32_t* ctas) {
-  if (a.wait_limit > 0) return launch_tc_typed<Tin, Tout, SCATTER, MODE, true>(a, num_sms, stream, ctas);
-  return launch_tc_typed<Tin, Tout, SCATTER, MODE, false>(a, num_sms, stream, ctas);
+  if (a.wait_limit > 0) return launch_tc_typed<Tin, Tout, SCATTER, MODE, true, CLS>(a, num_sms, stream, ctas);
+  return launch_tc_typed<Tin, Tout, SCATTER, MODE, false, CLS>(a, num_sms, stream, ctas);
 }
 
 template <typename Tin, typename Tout>
 cudaError_t launch_tc_out(const AttendArgs& a, int mode, int num_sms, cudaStream_t stream, uint32_t* ctas) {
+  if (a.cls != nullptr) {
+    // The class-token side output: packed outputs of the input's own type.
+    if constexpr (std::is_same<Tin, Tout>::value) {
+      if (mode == MODE_PACKED && a.src_idx == nullptr)
+        return launch_tc_lim<Tin, Tout, false, MODE_PACKED, true>(a, num_sms, stream, ctas);
+      if (mode == MODE_GATHER && a.src_rows > 0)
+        return launch_tc_lim<Tin, Tout, false, MODE_GATHER, true>(a, num_sms, stream, ctas);
+    }
+    return cudaErrorInvalidValue;
+  }
   if (mode == MODE_FUSED) {
     // Zero fill by bulk copies unless the grid has at most one unit per SM
     // (there the kernel is one latency chain per CTA and plain stores finish

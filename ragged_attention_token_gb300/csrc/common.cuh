@@ -67,6 +67,11 @@ struct AttendArgs {
   // span src_rows rows and packed row t is read from row src_idx[t].
   // 0: the padded gather (B*N rows, output scattered to src_idx).
   long long src_rows;
+  // Class-token side output (launches with a CLS instantiation only): cls
+  // [B, H, cls_stride] fp32 receives, for every image's first row, its
+  // softmax weights over the image's rows (see rra_attend_cls).
+  float* cls;
+  int cls_stride;
 };
 
 // Each CTA adds one to *done_count once all its threads' output stores are
@@ -129,6 +134,12 @@ cudaError_t launch_cls_scores(const void* qp, const void* kp, const int32_t* cu,
                               int H, float scale, rra_dtype in, float* scores, int32_t* err, cudaStream_t stream);
 cudaError_t launch_topk_keep(const float* scores, const uint8_t* keep_prev, int B, int N, int num, int den,
                              uint8_t* keep_new, cudaStream_t stream);
+// The keep decision from the attention's class-token side output cls
+// [B, H, stride] (one CTA per image); keep_new and scores [B, N] optional;
+// with cu_new (not null) also the next layer's cu/dst/src and rows.
+cudaError_t launch_prune_cls(const float* cls, int stride, const int32_t* cu, const int32_t* src, int B, int N, int H,
+                             int num, int den, uint8_t* keep_new, float* scores, int32_t* cu_new, int32_t* dst_new,
+                             int32_t* src_new, int32_t* rows_new, int32_t* err, cudaStream_t stream);
 // tcgen05 + TMA attention; needs the driver's tensor-map encoder.
 bool attend_tc_available();
 cudaError_t launch_attend_tc(const AttendArgs& a, rra_dtype in, rra_dtype out, int num_sms, cudaStream_t stream,

@@ -289,6 +289,15 @@ __device__ __forceinline__ void rescale_p32(uint32_t tS_row, float alpha) {
 }
 
 
+// The raw scores of one group of a row (16 or 32 columns) to global memory,
+// 16 bytes per store (dst 16-byte aligned).
+__device__ __forceinline__ void stash_row(float* dst, const float (&t)[32], int cols) {
+  float4* d4 = reinterpret_cast<float4*>(dst);
+#pragma unroll
+  for (int i = 0; i < 8; ++i)
+    if (i < 4 || cols > 16) d4[i] = make_float4(t[4 * i], t[4 * i + 1], t[4 * i + 2], t[4 * i + 3]);
+}
+
 // Softmax of one 64-key chunk (nk16 columns of S, the first n_c valid) for
 // this thread's query row, in two 32-column groups: each group's row max
 // (from the registers it was loaded into), then its weights written over S.
@@ -298,14 +307,20 @@ __device__ __forceinline__ void rescale_p32(uint32_t tS_row, float alpha) {
 // below 2^8.  On a unit's first chunk (c == 0) m and l start from this chunk.
 // `vote`: this thread's row is one of the tile's rows (only those may move
 // the reference; lanes past the tile see whatever the Q buffer held).
-template <bool BF>
+// CLS: a thread given `stash` (not null) also stores its row's raw scores of
+// the chunk's nk16 columns there.
+template <bool BF, bool CLS = false>
 __device__ __forceinline__ void softmax_chunk64(uint32_t tS_row, uint32_t tO_row, int nk16, int n_c, int c,
-                                                bool vote, float c2, float& m_run, float& l_run) {
+                                                bool vote, float c2, float& m_run, float& l_run,
+                                                float* stash = nullptr) {
   const int cols_a = min(32, nk16), cols_b = nk16 - 32;
   const int va = min(32, n_c), vb = n_c - 32;
   float m = m_run;
   float t[32];
   load_group(tS_row, cols_a, t);
+  if constexpr (CLS) {
+    if (stash != nullptr) stash_row(stash, t, cols_a);
+  }
   {
     const float e = (c2 >= 0.f ? group_extreme<false>(t, va) : group_extreme<true>(t, va)) * c2;
     if (c == 0) {
@@ -323,6 +338,9 @@ __device__ __forceinline__ void softmax_chunk64(uint32_t tS_row, uint32_t tO_row
   }
   if (cols_b > 0) {
     load_group(tS_row + 32, cols_b, t);
+    if constexpr (CLS) {
+      if (stash != nullptr) stash_row(stash + 32, t, cols_b);
+    }
     const float e = (c2 >= 0.f ? group_extreme<false>(t, vb) : group_extreme<true>(t, vb)) * c2;
     if (__any_sync(0xffffffffu, vote && e > m + 8.f)) {
       const float m_new = fmaxf(m, e);

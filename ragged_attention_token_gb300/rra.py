@@ -41,7 +41,11 @@ _SIGNATURES = {
     "rra_topk_keep": (_i, [_vp, _vp, _i, _i, _i, _i, _vp, _vp]),
     "rra_attend_gather": (_i, [_vp, _vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
     "rra_pack_index": (_i, [_vp, _vp, _i, _i, _vp, _vp, _vp, _vp, _vp]),
-    "rra_attend_rows": (_i, [_vp, _vp, _vp, ctypes.c_longlong, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
+    "rra_attend_rows": (_i, [_vp, _vp, _vp, ctypes.c_longlong, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i,
+                             _vp]),
+    "rra_attend_cls": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _i, _vp]),
+    "rra_topk_keep_cls": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp]),
+    "rra_prune_index": (_i, [_vp, _i, _vp, _vp, _i, _i, _i, _i, _i, _vp, _vp, _vp, _vp, _vp, _vp, _vp]),
     "rra_unpack": (_i, [_vp, _vp, _i, _i, _i, _i, _i, _vp, _vp]),
     "rra_pipeline": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp, _sz, _vp]),
     "rra_pipeline_static": (_i, [_vp, _vp, _vp, _vp, _i, _i, _i, _i, _f, _i, _vp, _i, _vp]),
@@ -229,12 +233,41 @@ def pack_index(keep, cu_seqlens, dst_idx, src_idx, rows=None, dst_prev=None, str
                                 _ptr(rows), _stream(stream)))
 
 
-def attend_rows(q, k, v, rows, cu_seqlens, B: int, max_seqlen: int, o, scale: float = 0.125, stream=None):
-    """rra_attend_rows: packed attention whose row t is read from row rows[t] of q/k/v [src_rows, H, d]."""
+def attend_rows(q, k, v, rows, cu_seqlens, B: int, max_seqlen: int, o, scale: float = 0.125, cls=None,
+                stream=None):
+    """rra_attend_rows: packed attention whose row t is read from row rows[t] of q/k/v [src_rows, H, d];
+    `cls` ([B, H, stride] float32) receives the class-token side output when given."""
     H, d = q.shape[-2], q.shape[-1]
     src_rows = q.numel() // (H * d)
+    stride = cls.shape[-1] if cls is not None else 0
     _check(lib().rra_attend_rows(_ptr(q), _ptr(k), _ptr(v), src_rows, _ptr(rows), _ptr(cu_seqlens), B, max_seqlen,
-                                 H, d, float(scale), _DTYPE[q.dtype], _ptr(o), _DTYPE[o.dtype], _stream(stream)))
+                                 H, d, float(scale), _DTYPE[q.dtype], _ptr(o), _DTYPE[o.dtype], _ptr(cls), stride,
+                                 _stream(stream)))
+
+
+def attend_cls(qp, kp, vp, cu_seqlens, B: int, max_seqlen: int, o, cls, scale: float = 0.125, stream=None):
+    """rra_attend_cls: packed attention plus the class-token weights cls [B, H, stride] (float32)."""
+    H, d = qp.shape[-2], qp.shape[-1]
+    _check(lib().rra_attend_cls(_ptr(qp), _ptr(kp), _ptr(vp), _ptr(cu_seqlens), B, max_seqlen, H, d, float(scale),
+                                _DTYPE[qp.dtype], _ptr(o), _DTYPE[o.dtype], _ptr(cls), cls.shape[-1],
+                                _stream(stream)))
+
+
+def topk_keep_cls(cls, cu_seqlens, src_idx, N: int, keep_num: int, keep_den: int, keep_new, scores=None,
+                  stream=None):
+    """rra_topk_keep_cls: the keep decision [B, N] from the class-token side output cls [B, H, stride]."""
+    B, H, stride = cls.shape
+    _check(lib().rra_topk_keep_cls(_ptr(cls), stride, _ptr(cu_seqlens), _ptr(src_idx), B, N, H, keep_num, keep_den,
+                                   _ptr(keep_new), _ptr(scores), _stream(stream)))
+
+
+def prune_index(cls, cu_prev, src_prev, N: int, keep_num: int, keep_den: int, cu_seqlens, dst_idx, src_idx, rows,
+                keep_new=None, scores=None, stream=None):
+    """rra_prune_index: the keep decision from cls [B, H, stride] and the next layer's indices in one launch."""
+    B, H, stride = cls.shape
+    _check(lib().rra_prune_index(_ptr(cls), stride, _ptr(cu_prev), _ptr(src_prev), B, N, H, keep_num, keep_den,
+                                 _ptr(cu_seqlens), _ptr(dst_idx), _ptr(src_idx), _ptr(rows), _ptr(keep_new),
+                                 _ptr(scores), _stream(stream)))
 
 
 def unpack(op, dst_idx, B: int, N: int, out, stream=None):

@@ -368,3 +368,63 @@ def test_progressive_chain_in_place_matches_oracle_and_replays_in_a_graph(out_dt
     torch.cuda.synchronize()
     for a, b in zip(eager, bufs["out"] + [bufs["final"]]):
         assert np.array_equal(bits(a), bits(b))
+
+
+def test_progressive_chain_with_device_decisions_matches_oracle():
+    """The chain with every pruning decision made on the device: the layer
+    before an event writes the class-token side output, one launch turns it
+    into the next layer's mask and indices, and that layer attends in place.
+    Each decision is checked bit-exact against the oracle's rule on the
+    device's scores, each layer's attention against the oracle on the
+    device's masks."""
+    masks, cases = W.make_progressive_chain(B=16)
+    B, N, H, d = cases[0].B, cases[0].N, cases[0].H, cases[0].d
+    L = len(cases)
+    events = set(l - 1 for l in W.PROGRESSIVE_EVENTS)        # 0-indexed layers whose input is pruned
+    stride = (N + 15) // 16 * 16
+    keep = cases[0].keep.cuda()
+    cu, dst, src = _index_buffers(B, N)
+    rows = torch.empty(B * N, dtype=torch.int32, device="cuda")
+    rra.get_device_error(clear=True)
+    rra.pack_index(keep, cu, dst, src, rows)
+    keep_np = cases[0].keep.numpy()
+    for l, case in enumerate(cases):
+        # This layer's inputs arrive in the previous layer's packed layout (layer 1: padded).
+        q, k, v = (x.cuda() for x in (case.q, case.k, case.v))
+        if l == 0:
+            src_in = tuple(x.view(B * N, H, d) for x in (q, k, v))
+        else:
+            src_in = tuple(_pack(torch.from_numpy(prev_keep_np).cuda(), q, k, v)[3])
+        o = torch.empty((B * N, H, d), dtype=torch.bfloat16, device="cuda")
+        decide = (l + 1) in events
+        cls = torch.empty((B, H, stride), dtype=torch.float32, device="cuda") if decide else None
+        if l == 0 or l in events:
+            rra.attend_rows(*src_in, rows, cu, B, N, o, scale=SCALE, cls=cls)
+        elif decide:
+            rra.attend_cls(*src_in, cu, B, N, o, cls, scale=SCALE)
+        else:
+            rra.attend(*src_in, cu, B, N, o, scale=SCALE)
+        torch.cuda.synchronize()
+        assert rra.get_device_error() == 0
+        # This layer against the oracle on the device's mask.
+        cu_r, dst_r, src_r = oracle.pack_indices(keep_np)
+        T = int(cu_r[-1])
+        assert np.array_equal(cu.cpu().numpy(), cu_r)
+        p64 = [oracle.pack_rows(x.double().numpy(), src_r) for x in (case.q, case.k, case.v)]
+        ref = oracle.attend(*p64, cu_r, SCALE)
+        err = np.abs(o[:T].cpu().double().numpy() - ref)
+        assert np.all(err <= out_tolerance(ref, torch.bfloat16)), f"layer {l + 1}: max-abs error {err.max()}"
+        prev_keep_np = keep_np
+        if decide:
+            keep_new = torch.empty_like(keep)
+            scores = torch.empty((B, N), dtype=torch.float32, device="cuda")
+            cu2, dst2, src2 = _index_buffers(B, N)
+            rows2 = torch.empty(B * N, dtype=torch.int32, device="cuda")
+            rra.prune_index(cls, cu, src, N, 7, 10, cu2, dst2, src2, rows2, keep_new=keep_new, scores=scores)
+            torch.cuda.synchronize()
+            assert rra.get_device_error() == 0
+            keep_np = keep_new.cpu().numpy()
+            want = oracle.topk_keep(scores.cpu().double().numpy(), prev_keep_np, 7, 10)
+            assert np.array_equal(keep_np, want), f"decision after layer {l + 1}"
+            assert int(keep_np.sum()) == int(masks[l + 1].sum())   # the workload's counts
+            cu, dst, src, rows = cu2, dst2, src2, rows2

@@ -93,6 +93,42 @@ def test_scores_ignore_a_shift_common_to_all_keys_and_follow_permutations():
     assert s2[b, pj] == pytest.approx(base[b, pi], rel=1e-12)
 
 
+def test_cls_weights_per_head_closed_forms():
+    # Zero class query: every head's weights are uniform; two rows: sigmoid per head.
+    rng = np.random.default_rng(6)
+    keep, q, k, cu, src, qp, kp = _packed(rng, 3, 13, 3, 4)
+    for b in range(3):
+        qp[cu[b]] = 0.0
+    w = oracle.cls_weights(qp, kp, cu, 0.5)
+    for b in range(3):
+        n = int(cu[b + 1] - cu[b])
+        assert w[b].shape == (3, n)
+        assert np.allclose(w[b], 1.0 / n, atol=1e-15)
+    H, d, scale = 4, 6, 0.7
+    keep = np.zeros((2, 9), dtype=np.uint8)
+    keep[0, [2, 7]] = 1                                  # image 1 keeps nothing
+    q = rng.standard_normal((2, 9, H, d))
+    k = rng.standard_normal((2, 9, H, d))
+    cu, dst, src = oracle.pack_indices(keep)
+    w = oracle.cls_weights(oracle.pack_rows(q, src), oracle.pack_rows(k, src), cu, scale)
+    for h in range(H):
+        sig = 1.0 / (1.0 + math.exp(-scale * float(q[0, 2, h] @ (k[0, 7, h] - k[0, 2, h]))))
+        assert w[0][h, 1] == pytest.approx(sig, rel=1e-13)
+        assert w[0][h, 0] == pytest.approx(1.0 - sig, rel=1e-13)
+    assert w[1].shape == (H, 0)
+
+
+def test_cls_weights_rows_sum_to_one_and_their_mean_is_the_score():
+    rng = np.random.default_rng(7)
+    keep, q, k, cu, src, qp, kp = _packed(rng, 4, 21, 3, 8)
+    w = oracle.cls_weights(qp, kp, cu, 0.3)
+    s = oracle.cls_scores(qp, kp, cu, src, 21, 0.3)
+    for b in range(4):
+        assert np.allclose(w[b].sum(axis=1), 1.0, atol=1e-12)
+        pos = src[cu[b]:cu[b + 1]] - b * 21
+        assert np.allclose(w[b].mean(axis=0), s[b, pos], atol=1e-15)
+
+
 def test_topk_counts_and_ties():
     keep = np.ones((4, 197), dtype=np.uint8)
     keep[1, 100:] = 0
