@@ -256,12 +256,13 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
     return res
 
 
-# DRAM bytes (read + write) per launch of the fused attend_tc_kernel, each from one ncu
-# capture of the same launches (dram__bytes_read.sum + dram__bytes_write.sum).  They
-# describe the kernel source whose SHA-256 starts with TRAFFIC_SRC_SHA; once that file
-# changes the traffic is reported as null until it is captured again.
-TRAFFIC_SRC_SHA = "84f8ec8241cdb73e"
-TRAFFIC_BYTES = {"serving_B4": 430587, "batched_b64_p80": 11922603}
+# DRAM bytes (read + write) per launch of the kernel rra_pipeline runs on a workload,
+# each from one ncu capture of the same launches (dram__bytes_read.sum +
+# dram__bytes_write.sum): (kernel source, the SHA-256 prefix of that source when it was
+# captured, bytes).  Once the source changes, the traffic is reported as null until it
+# is captured again.
+TRAFFIC = {"serving_B4": ("attend_small.cu", "da8613365881d1be", 420450),
+           "batched_b64_p80": ("attend_tc.cu", "8b1315f0a5ab8725", 11920043)}
 
 
 def pipeline_kernel_name(case, n_sms):
@@ -273,13 +274,16 @@ def pipeline_kernel_name(case, n_sms):
 
 
 def measured_traffic(key):
-    src = os.path.join(ROOT, "ragged_attention_token_gb300", "csrc", "attend_tc.cu")
+    if key not in TRAFFIC:
+        return None
+    name, sha, nbytes = TRAFFIC[key]
+    src = os.path.join(ROOT, "ragged_attention_token_gb300", "csrc", name)
     try:
         with open(src, "rb") as f:
-            ok = hashlib.sha256(f.read()).hexdigest().startswith(TRAFFIC_SRC_SHA)
+            ok = hashlib.sha256(f.read()).hexdigest().startswith(sha)
     except OSError:
         ok = False
-    return TRAFFIC_BYTES.get(key) if ok else None
+    return nbytes if ok else None
 
 
 def packed_qkvo_frac(case, us, peaks):
@@ -890,10 +894,13 @@ def run_sweep(args):
     n_sms = torch.cuda.get_device_properties(device).multi_processor_count
     stream = torch.cuda.Stream(device=device)
     peaks = measured_peaks()
-    cases = [W.make_tiny()] + [W.make_serving(b) for b in W.SERVING_BATCHES] + \
-            [W.make_batched(p) for p in W.BATCHED_RATES] + [W.make_hires(p) for p in W.HIRES_RATES]
-    masks = W.progressive_masks()
-    cases += [W.make_progressive_layer(L, masks) for L in (1, 4, 7, 10)]
+    parts = set(args.sweep_parts.split(","))
+    cases = []
+    if "kernels" in parts:
+        cases = [W.make_tiny()] + [W.make_serving(b) for b in W.SERVING_BATCHES] + \
+                [W.make_batched(p) for p in W.BATCHED_RATES] + [W.make_hires(p) for p in W.HIRES_RATES]
+        masks = W.progressive_masks()
+        cases += [W.make_progressive_layer(L, masks) for L in (1, 4, 7, 10)]
     for case in cases:
         sets = InputSets(case, device, rra, case.dtype)
         kt = kernel_times(case, sets, rra, stream, packed=True)
@@ -910,10 +917,13 @@ def run_sweep(args):
                 "fused_tokens_per_s": round(case.kept_tokens / (kt["fused_us"] * 1e-6), 1)}
         print(json.dumps(line), flush=True)
         del sets
-    print(json.dumps(progressive_chain_times(rra, stream, peaks)), flush=True)
-    print(json.dumps(device_pruning_times(rra, stream)), flush=True)
-    for line in linear_times(rra, stream, peaks):
-        print(json.dumps(line), flush=True)
+    if "chain" in parts:
+        print(json.dumps(progressive_chain_times(rra, stream, peaks)), flush=True)
+    if "pruning" in parts:
+        print(json.dumps(device_pruning_times(rra, stream)), flush=True)
+    if "linear" in parts:
+        for line in linear_times(rra, stream, peaks):
+            print(json.dumps(line), flush=True)
     return 0
 
 
@@ -925,6 +935,8 @@ def main(argv=None):
     ap.add_argument("--impl", choices=("rra", "reference"), default="rra")
     ap.add_argument("--workload", default="serving", choices=("serving", "tiny", "batched", "hires"))
     ap.add_argument("--sweep", action="store_true", help="per-workload kernel timings, one line each")
+    ap.add_argument("--sweep-parts", default="kernels,chain,pruning,linear",
+                    help="comma-separated parts of --sweep: kernels, chain, pruning, linear")
     ap.add_argument("--quick", action="store_true", help="skip host-latency and B=64 extras")
     ap.add_argument("--no-cpu", action="store_true", help="skip the CPU oracle baseline")
     ap.add_argument("--cpu-budget", type=float, default=10.0, help="seconds of CPU oracle work")
