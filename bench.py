@@ -258,11 +258,21 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
 
 # DRAM bytes (read + write) per launch of the kernel rra_pipeline runs on a workload,
 # each from one ncu capture of the same launches (dram__bytes_read.sum +
-# dram__bytes_write.sum): (kernel source, the SHA-256 prefix of that source when it was
-# captured, bytes).  Once the source changes, the traffic is reported as null until it
-# is captured again.
-TRAFFIC = {"serving_B4": ("attend_small.cu", "da8613365881d1be", 420450),
-           "batched_b64_p80": ("attend_tc.cu", "8b1315f0a5ab8725", 11920043)}
+# dram__bytes_write.sum): (kernel source, the SHA-256 prefix of that source and the
+# headers it includes when it was captured, bytes).  Once any of them changes, the
+# traffic is reported as null until it is captured again.
+KERNEL_HEADERS = ("common.cuh", "tc_ptx.cuh", "softmax_tc.cuh")
+TRAFFIC = {"serving_B4": ("attend_small.cu", "SMALL_SHA", 420450),
+           "batched_b64_p80": ("attend_tc.cu", "TC_SHA", 11920043)}
+
+
+def kernel_source_sha(name):
+    """SHA-256 of a kernel source followed by the headers it includes."""
+    h = hashlib.sha256()
+    for f in (name,) + KERNEL_HEADERS:
+        with open(os.path.join(ROOT, "ragged_attention_token_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()
 
 
 def pipeline_kernel_name(case, n_sms):
@@ -277,10 +287,8 @@ def measured_traffic(key):
     if key not in TRAFFIC:
         return None
     name, sha, nbytes = TRAFFIC[key]
-    src = os.path.join(ROOT, "ragged_attention_token_gb300", "csrc", name)
     try:
-        with open(src, "rb") as f:
-            ok = hashlib.sha256(f.read()).hexdigest().startswith(sha)
+        ok = kernel_source_sha(name).startswith(sha)
     except OSError:
         ok = False
     return nbytes if ok else None

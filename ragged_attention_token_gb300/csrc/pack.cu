@@ -74,11 +74,6 @@ __global__ void __launch_bounds__(PACK_THREADS) pack_kernel(const PackArgs a) {
   __shared__ int s_kept_dst[PACK_THREADS];
   __shared__ int s_pruned_g[PACK_THREADS];
 
-  // A programmatic dependent of the kernel before it in the stream: nothing
-  // in global memory is touched before that kernel has completed.  (No early
-  // release of the next kernel: an attention grid launched while this one
-  // still holds the SMs places its persistent CTAs unevenly.)
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long total = static_cast<long long>(a.B) * a.N;
   const long long g0 = static_cast<long long>(blockIdx.x) * a.tok_per_cta;
   if (g0 >= total) return;
@@ -188,16 +183,11 @@ cudaError_t launch_pack(const PackArgs& a, int num_sms, cudaStream_t stream) {
   if (tpc < 32) tpc = 32;
   args.tok_per_cta = static_cast<int>(tpc);
   const long long grid = (total + tpc - 1) / tpc;
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(PACK_THREADS);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, pack_kernel, args);
+  // A plain launch: as a programmatic dependent of a persistent attention
+  // grid, the copy's CTAs took the SMs in the order that grid's CTAs
+  // finished and ran unevenly (+17 us over the 12-layer chain with copies).
+  pack_kernel<<<static_cast<unsigned>(grid), PACK_THREADS, 0, stream>>>(args);
+  return cudaGetLastError();
 }
 
 }  // namespace rra

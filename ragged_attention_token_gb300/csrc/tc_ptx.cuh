@@ -11,7 +11,6 @@
 
 namespace rra {
 
-constexpr uint32_t WAIT_SUSPEND_NS = 20000;            // try_wait suspend hint
 constexpr long long WAIT_LIMIT_CYCLES = 2000000000LL;  // ~1 s at 2 GHz
 
 template <typename T> struct IsBf16;
@@ -33,12 +32,14 @@ __device__ __forceinline__ void fence_barrier_init() {
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
   asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
 }
+// Potentially blocking test of a phase, with no suspend-time hint (a 20 us
+// hint measured 1-4 % slower on the attention kernels).
 __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   uint32_t ok;
   asm volatile(
-      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n selp.u32 %0, 1, 0, p;\n}\n"
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n selp.u32 %0, 1, 0, p;\n}\n"
       : "=r"(ok)
-      : "r"(bar), "r"(parity), "r"(WAIT_SUSPEND_NS)
+      : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
 }
@@ -266,9 +267,9 @@ __device__ __forceinline__ uint32_t ld_shared_volatile_u32(uint32_t addr) {
   return v;
 }
 // Bounded wait that also gives up as soon as the CTA's abort flag is set.
-// Bounded wait.  A bound below WAIT_POLL_BELOW cycles (a test hook for
-// this path) polls with test_wait, out of line: a suspended try_wait sleeps
-// until the phase completes, past such a bound.
+// A bound below WAIT_POLL_BELOW cycles (a test hook for this path) polls
+// with test_wait, out of line: one try_wait may block for a time the
+// hardware chooses, past such a bound.
 constexpr long long WAIT_POLL_BELOW = 1000000LL;
 static __device__ __noinline__ bool mbar_poll_or_abort(uint32_t bar, uint32_t parity, uint32_t abort_flag, long long limit) {
   const long long t0 = clock64();

@@ -15,8 +15,6 @@ namespace {
 constexpr int THREADS = 256;
 
 __global__ void __launch_bounds__(THREADS) unpack_kernel(const UnpackArgs a) {
-  // A programmatic dependent of the kernel before it in the stream (see launch_unpack).
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const long long total = static_cast<long long>(a.B) * a.N;
   const long long items = total * a.row_vecs;
   const long long cap = total;
@@ -45,19 +43,8 @@ cudaError_t launch_unpack(const UnpackArgs& a, cudaStream_t stream) {
   long long grid = (items + THREADS - 1) / THREADS;
   if (grid > 8 * 152 * 4) grid = 8 * 152 * 4;
   if (grid < 1) grid = 1;
-  // Programmatic stream serialisation: the launch overlaps the tail of the
-  // kernel before it; nothing in global memory is touched before that
-  // kernel has completed.
-  cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(static_cast<unsigned>(grid));
-  cfg.blockDim = dim3(THREADS);
-  cfg.stream = stream;
-  cudaLaunchAttribute attr[1];
-  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[0].val.programmaticStreamSerializationAllowed = 1;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, unpack_kernel, a);
+  unpack_kernel<<<static_cast<unsigned>(grid), THREADS, 0, stream>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace rra
