@@ -245,6 +245,11 @@ __global__ void __launch_bounds__(STHREADS)
     if (warp == 0 && q0 - SBM < n) zero_pruned_rows<Tout>(a, b, h, lane);
   }
 
+  // Host completion word (rra_attend_wait): every output store of the CTA is
+  // issued, so the host may see the count move before the teardown below.
+  if constexpr (!FUSED) {
+    if (a.done_count != nullptr) signal_done(a);
+  }
   if (bad && tid == 0) {
     st_shared_u32(abort_flag, 1u);
     record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
@@ -264,9 +269,6 @@ __global__ void __launch_bounds__(STHREADS)
     tmem_dealloc(tmem, STMEM_COLS);
   }
   asm volatile("griddepcontrol.launch_dependents;" :::);
-  if constexpr (!FUSED) {
-    if (a.done_count != nullptr) signal_done(a);
-  }
 }
 
 constexpr int kMaxDevSmall = 64;

@@ -852,6 +852,12 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     st_shared_u32(abort_flag, 1u);
     record_error(a.err, RRA_DEVERR_WAIT_TIMEOUT);
   }
+  // Host completion word (rra_attend_wait): the packed and gather modes
+  // write their output with plain stores only, all issued by now, so the
+  // host may see the count move before the teardown below.
+  if constexpr (!FUSED) {
+    if (a.done_count != nullptr) signal_done(a);
+  }
 
   // Teardown.  After an abort, copies or products still in flight get a
   // bounded grace period (~1 ms) to land before the TMEM is released and the
@@ -867,11 +873,6 @@ __global__ void __launch_bounds__(THREADS, CTAS_PER_SM)
     __syncwarp();
     tc_fence_after();
     tmem_dealloc(tmem, TMEM_COLS);
-  }
-  // Host completion word (rra_attend_wait): the packed and gather modes
-  // write their output with plain stores only, all issued by now.
-  if constexpr (!FUSED) {
-    if (a.done_count != nullptr) signal_done(a);
   }
 }
 
