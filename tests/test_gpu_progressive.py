@@ -428,3 +428,96 @@ def test_progressive_chain_with_device_decisions_matches_oracle():
             assert np.array_equal(keep_np, want), f"decision after layer {l + 1}"
             assert int(keep_np.sum()) == int(masks[l + 1].sum())   # the workload's counts
             cu, dst, src, rows = cu2, dst2, src2, rows2
+
+
+def _sampled_rows_check(case, keep_np, o, n_samples=48, seed=0):
+    """Sampled output rows of a layer's packed attention against oracle.attend_row."""
+    cu_r, _, src_r = oracle.pack_indices(keep_np)
+    T = int(cu_r[-1])
+    rng = np.random.default_rng(seed)
+    ts = rng.integers(0, T, n_samples)
+    hs = rng.integers(0, case.H, n_samples)
+    q64, k64, v64 = (x.double().numpy().reshape(case.B * case.N, case.H, case.d) for x in (case.q, case.k, case.v))
+    got = o.float().cpu().double().numpy()
+    for t, h in zip(ts, hs):
+        b = int(np.searchsorted(cu_r, t, side="right")) - 1
+        s0, s1 = int(cu_r[b]), int(cu_r[b + 1])
+        rows = src_r[s0:s1]
+        mini_cu = np.array([0, s1 - s0], dtype=np.int64)
+        ref = oracle.attend_row(q64[rows], k64[rows], v64[rows], mini_cu, SCALE, int(t) - s0, int(h))
+        err = np.abs(got[t, h] - ref)
+        assert np.all(err <= out_tolerance(ref, o.dtype)), f"row {t} head {h}: max-abs error {err.max()}"
+
+
+def test_progressive_chain_full_size_with_device_decisions():
+    """The B=256 chain with device decisions in the launch sequence bench.py
+    times (index pass, rows attention with the side output, decision + next
+    indices in one launch): indices and decisions bit-exact against the oracle
+    at every layer, class-token weights and sampled attention rows within
+    tolerance, the final unpack's pruned rows +0."""
+    masks, cases = W.make_progressive_chain(B=256)
+    B, N, H, d = cases[0].B, cases[0].N, cases[0].H, cases[0].d
+    L = len(cases)
+    events = set(l - 1 for l in W.PROGRESSIVE_EVENTS)
+    stride = (N + 15) // 16 * 16
+    keep_np = cases[0].keep.numpy()
+    cu, dst, src = _index_buffers(B, N)
+    rows = torch.empty(B * N, dtype=torch.int32, device="cuda")
+    rra.get_device_error(clear=True)
+    rra.pack_index(cases[0].keep.cuda(), cu, dst, src, rows)
+    prev_keep_np = None
+    for l, case in enumerate(cases):
+        q, k, v = (x.cuda() for x in (case.q, case.k, case.v))
+        if l == 0:
+            src_in = tuple(x.view(B * N, H, d) for x in (q, k, v))
+        else:
+            src_in = tuple(_pack(torch.from_numpy(prev_keep_np).cuda(), q, k, v)[3])
+        o = torch.empty((B * N, H, d), dtype=torch.bfloat16, device="cuda")
+        decide = (l + 1) in events
+        cls = torch.full((B, H, stride), float("nan"), dtype=torch.float32, device="cuda") if decide else None
+        if l == 0 or l in events:
+            rra.attend_rows(*src_in, rows, cu, B, N, o, scale=SCALE, cls=cls)
+        elif decide:
+            rra.attend_cls(*src_in, cu, B, N, o, cls, scale=SCALE)
+        else:
+            rra.attend(*src_in, cu, B, N, o, scale=SCALE)
+        torch.cuda.synchronize()
+        assert rra.get_device_error() == 0
+        cu_r, dst_r, src_r = oracle.pack_indices(keep_np)
+        T = int(cu_r[-1])
+        assert np.array_equal(cu.cpu().numpy(), cu_r), f"layer {l + 1}: cu_seqlens"
+        assert np.array_equal(dst.cpu().numpy(), dst_r), f"layer {l + 1}: dst_idx"
+        assert np.array_equal(src.cpu().numpy()[:T], src_r), f"layer {l + 1}: src_idx"
+        _sampled_rows_check(case, keep_np, o, seed=l)
+        prev_keep_np = keep_np
+        if decide:
+            # Class-token weights of a few images against the oracle, per head.
+            got_cls = cls.cpu().double().numpy()
+            for b in (0, 77, 255):
+                rows_b = src_r[cu_r[b]:cu_r[b + 1]]
+                qb = case.q.double().numpy().reshape(B * N, H, d)[rows_b]
+                kb = case.k.double().numpy().reshape(B * N, H, d)[rows_b]
+                ref = oracle.cls_weights(qb, kb, np.array([0, len(rows_b)]), SCALE)[0]
+                assert float(np.abs(got_cls[b, :, :len(rows_b)] - ref).max()) <= 1e-5
+            keep_new = torch.empty((B, N), dtype=torch.uint8, device="cuda")
+            scores = torch.empty((B, N), dtype=torch.float32, device="cuda")
+            cu2, dst2, src2 = _index_buffers(B, N)
+            rows2 = torch.empty(B * N, dtype=torch.int32, device="cuda")
+            rra.prune_index(cls, cu, src, N, 7, 10, cu2, dst2, src2, rows2, keep_new=keep_new, scores=scores)
+            torch.cuda.synchronize()
+            assert rra.get_device_error() == 0
+            keep_np = keep_new.cpu().numpy()
+            assert np.array_equal(keep_np, oracle.topk_keep(scores.cpu().double().numpy(), prev_keep_np, 7, 10))
+            _, dst_prev_r, _ = oracle.pack_indices(prev_keep_np)
+            cu_n, _, src_n = oracle.pack_indices(keep_np)
+            assert np.array_equal(rows2.cpu().numpy()[:int(cu_n[-1])], dst_prev_r[src_n])
+            assert int(keep_np.sum()) == int(masks[l + 1].sum())
+            cu, dst, src, rows = cu2, dst2, src2, rows2
+    final = torch.full((B, N, H, d), float("nan"), dtype=torch.bfloat16, device="cuda")
+    rra.unpack(o, dst, B, N, final)
+    torch.cuda.synchronize()
+    fin_bits = bits(final)
+    assert np.all(fin_bits[keep_np == 0] == 0), "pruned positions are not +0"
+    _, dst_r, _ = oracle.pack_indices(keep_np)
+    kept = np.nonzero(keep_np.reshape(-1))[0][:64]
+    assert np.array_equal(fin_bits.reshape(B * N, H, d)[kept], bits(o)[dst_r[kept]])
