@@ -897,7 +897,10 @@ rra_status rra_pipeline_mapped(const uint8_t* keep_h, const void* q_h, const voi
     // batches move more bytes than latency, and there pack's coalesced
     // 256-thread row copies use the link better than one loading warp per
     // CTA (measured on B=64: 142 against 190 us at 80% pruning, 399 against
-    // 740 us dense).
+    // 740 us dense).  The warp-specialised kernel even where the device
+    // pipeline takes the small-grid one: its producer warp writes the
+    // pruned rows as whole tokens right behind its first loads, and the
+    // small-grid kernel's step took 9.8-10.4 against 9.1 us at serving B=4.
     AttendArgs a{};
     a.keep = p.keep;
     a.qp = p.q;

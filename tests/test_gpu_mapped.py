@@ -19,7 +19,8 @@ from ragged_attention_token_gb300 import workloads as W
 
 pytestmark = pytest.mark.gpu
 
-KERNELS = [("tcgen05", rra.ATTEND_TCGEN05), ("mma_sync", rra.ATTEND_MMA_SYNC), ("auto", rra.ATTEND_AUTO)]
+KERNELS = [("tcgen05", rra.ATTEND_TCGEN05), ("tcgen05_latency", rra.ATTEND_TCGEN05_LATENCY),
+           ("mma_sync", rra.ATTEND_MMA_SYNC), ("auto", rra.ATTEND_AUTO)]
 
 CASES = [
     ("tiny", lambda: W.make_tiny()),
