@@ -157,3 +157,62 @@ def test_host_side_errors_of_the_next_step_entry_points(L):
     assert lin(a=0x10008) == rra.RRA_ERR_MISALIGNED
     assert lin(bias=0x50004) == rra.RRA_ERR_MISALIGNED
     assert lin(ind=rra.RRA_F32) == rra.RRA_ERR_INVALID_ARG
+
+
+def test_host_side_errors_of_the_chain_and_pruning_entry_points(L):
+    # rra_pack_index: shape, nulls, aliasing of the previous and new dst.
+    assert L.rra_pack_index(None, None, 2, 197, 0x300, 0x400, 0x500, None, None) == rra.RRA_ERR_INVALID_ARG
+    assert L.rra_pack_index(0x100, None, 2, 197, None, 0x400, 0x500, None, None) == rra.RRA_ERR_INVALID_ARG
+    assert L.rra_pack_index(0x100, None, 0, 197, 0x300, 0x400, 0x500, None, None) == rra.RRA_ERR_INVALID_ARG
+    assert L.rra_pack_index(0x100, None, 2, 1025, 0x300, 0x400, 0x500, None, None) == rra.RRA_ERR_UNSUPPORTED
+    assert L.rra_pack_index(0x100, 0x400, 2, 197, 0x300, 0x400, 0x500, 0x600, None) == rra.RRA_ERR_INVALID_ARG
+
+    # rra_attend_rows: rra_attend's checks, then rows, src_rows and the side output's.
+    def rows(**kw):
+        a = dict(q=0x10000, k=0x20000, v=0x30000, src_rows=394, rows=0x600, cu=0x300, B=2, S=197, H=6, d=64,
+                 scale=0.125, ind=rra.RRA_BF16, o=0x40000, outd=rra.RRA_BF16, cls=None, stride=0)
+        a.update(kw)
+        return L.rra_attend_rows(a["q"], a["k"], a["v"], a["src_rows"], a["rows"], a["cu"], a["B"], a["S"],
+                                 a["H"], a["d"], a["scale"], a["ind"], a["o"], a["outd"], a["cls"], a["stride"],
+                                 None)
+    assert rows(d=32) == rra.RRA_ERR_UNSUPPORTED
+    assert rows(rows=None) == rra.RRA_ERR_INVALID_ARG
+    assert rows(src_rows=0) == rra.RRA_ERR_INVALID_ARG
+    assert rows(q=0x10008) == rra.RRA_ERR_MISALIGNED
+    assert rows(cls=0x50000, stride=210) == rra.RRA_ERR_INVALID_ARG          # not a multiple of 4
+    assert rows(cls=0x50000, stride=204) == rra.RRA_ERR_INVALID_ARG          # below max_seqlen rounded up to 16
+    assert rows(cls=0x50004, stride=208) == rra.RRA_ERR_MISALIGNED
+    assert rows(cls=0x50000, stride=208, outd=rra.RRA_F32) == rra.RRA_ERR_UNSUPPORTED
+
+    # rra_attend_cls: the side output is required.
+    def cls(**kw):
+        a = dict(qp=0x10000, kp=0x20000, vp=0x30000, cu=0x300, B=2, S=197, H=6, d=64, scale=0.125,
+                 ind=rra.RRA_BF16, o=0x40000, outd=rra.RRA_BF16, cls=0x50000, stride=208)
+        a.update(kw)
+        return L.rra_attend_cls(a["qp"], a["kp"], a["vp"], a["cu"], a["B"], a["S"], a["H"], a["d"], a["scale"],
+                                a["ind"], a["o"], a["outd"], a["cls"], a["stride"], None)
+    assert cls(cls=None) == rra.RRA_ERR_INVALID_ARG
+    assert cls(outd=rra.RRA_F16) == rra.RRA_ERR_UNSUPPORTED
+    assert cls(stride=192) == rra.RRA_ERR_INVALID_ARG
+    assert cls(cu=None) == rra.RRA_ERR_INVALID_ARG
+
+    # rra_topk_keep_cls / rra_prune_index: fraction, stride, nulls, aliasing.
+    assert L.rra_topk_keep_cls(0x50000, 208, 0x300, 0x400, 2, 197, 6, 8, 7, 0x9000, None, None) == \
+        rra.RRA_ERR_INVALID_ARG                                             # num > den
+    assert L.rra_topk_keep_cls(0x50000, 100, 0x300, 0x400, 2, 197, 6, 7, 10, 0x9000, None, None) == \
+        rra.RRA_ERR_INVALID_ARG                                             # stride < N
+    assert L.rra_topk_keep_cls(0x50000, 208, None, 0x400, 2, 197, 6, 7, 10, 0x9000, None, None) == \
+        rra.RRA_ERR_INVALID_ARG
+
+    def prune(**kw):
+        a = dict(cls=0x50000, stride=208, cu_prev=0x300, src_prev=0x400, B=2, N=197, H=6, num=7, den=10,
+                 cu=0x700, dst=0x800, src=0x900, rows=0xa00)
+        a.update(kw)
+        return L.rra_prune_index(a["cls"], a["stride"], a["cu_prev"], a["src_prev"], a["B"], a["N"], a["H"],
+                                 a["num"], a["den"], a["cu"], a["dst"], a["src"], a["rows"], None, None, None)
+    assert prune(rows=None) == rra.RRA_ERR_INVALID_ARG
+    assert prune(cu=0x300) == rra.RRA_ERR_INVALID_ARG                     # new indices alias the previous
+    assert b"alias" in L.rra_last_error_message()
+    assert prune(den=0) == rra.RRA_ERR_INVALID_ARG
+    assert prune(stride=150) == rra.RRA_ERR_INVALID_ARG
+    assert prune(N=2000) == rra.RRA_ERR_UNSUPPORTED
