@@ -262,8 +262,8 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
 # headers it includes when it was captured, bytes).  Once any of them changes, the
 # traffic is reported as null until it is captured again.
 KERNEL_HEADERS = ("common.cuh", "tc_ptx.cuh", "softmax_tc.cuh")
-TRAFFIC = {"serving_B4": ("attend_small.cu", "SMALL_SHA", 420450),
-           "batched_b64_p80": ("attend_tc.cu", "TC_SHA", 11920043)}
+TRAFFIC = {"serving_B4": ("attend_small.cu", "c89141ab65683d81", 420387),
+           "batched_b64_p80": ("attend_tc.cu", "be714d8c0419632c", 11919360)}
 
 
 def kernel_source_sha(name):
