@@ -186,6 +186,9 @@ def capture(fn_list, stream):
     return g
 
 
+SLEEP_CYCLES = 200_000      # ~0.1 ms at the GB300's 2.07 GHz
+
+
 def graph_time_per_launch(fn_list, stream, reps=5):
     """Median device µs per launch of a CUDA graph of back-to-back launches.
 
@@ -535,6 +538,11 @@ def run_rra(args, world, rank, local):
         torch.cuda.synchronize(device)
         e0 = torch.cuda.Event(enable_timing=True)
         e1 = torch.cuda.Event(enable_timing=True)
+        # A ~0.1 ms device sleep ahead of the start event: the host submits the
+        # first graph while the GPU sleeps, so the events time the steps on the
+        # device and not the first submission (which a short --steps run would
+        # otherwise spread over few steps).
+        torch.cuda._sleep(SLEEP_CYCLES)
         e0.record(stream)
         for _ in range(q_full):
             g_full.replay()
@@ -646,11 +654,14 @@ def run_rra(args, world, rank, local):
             "config": workload_config(case, desc, world),
             "timing": {"graph": f"CUDA graphs of {sets.R} rra_pipeline steps, replayed back to back",
                        "l2": f"{sets.R} rotating input sets of {sets.per_set / 2**20:.1f} MiB "
-                             f"({sets.R * sets.per_set / 2**20:.0f} MiB > L2)"},
+                             f"({sets.R * sets.per_set / 2**20:.0f} MiB > L2)",
+                       "start": "a ~0.1 ms device sleep is queued before the start event, so the events time "
+                                "the steps on the device and not the first graph's host submission"},
             "e2e": {"value": round(e2e_value, 1), "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                     "ms_per_step": round(e2e_ms / args.steps, 5),
-                    "path": "rra_pipeline_mapped (inputs and output in pinned host memory; pack + attend read the "
-                            "mask and the kept rows over the CPU-GPU link and write the output into host memory)"},
+                    "path": "rra_pipeline_mapped (inputs and output in pinned host memory; the kernel (at serving "
+                            "sizes one fused launch, else pack + attend) reads the mask and the kept rows over the "
+                            "CPU-GPU link and writes the output into host memory)"},
             "e2e_copy": e2e_copy,
             "roofline": roof,
             "kernels": kern,
