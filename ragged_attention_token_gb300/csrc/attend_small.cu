@@ -86,14 +86,22 @@ __global__ void __launch_bounds__(STHREADS)
     asm volatile("griddepcontrol.wait;" ::: "memory");
     // 1. The image's length and the start of its rows.
     if constexpr (FUSED) {
+      // All the row's mask bytes are loaded before the first ballot (N <= 256:
+      // eight per lane), so the scan waits for memory once.
       const unsigned lt = (1u << lane) - 1u;
       const uint8_t* krow = a.keep + static_cast<size_t>(b) * a.N;
+      bool flag[ATTEND_SMALL_MAX_KEYS / 32];
+#pragma unroll
+      for (int r = 0; r < ATTEND_SMALL_MAX_KEYS / 32; ++r) {
+        const int j = r * 32 + lane;
+        flag[r] = (j < a.N) && (__ldg(krow + j) != 0);
+      }
       int cnt = 0;
-      for (int j0 = 0; j0 < a.N; j0 += 32) {
-        const int j = j0 + lane;
-        const bool kept = (j < a.N) && (__ldg(krow + j) != 0);
-        const unsigned m = __ballot_sync(0xffffffffu, kept);
-        if (kept) st_shared_u16(pos + 2u * static_cast<uint32_t>(cnt + __popc(m & lt)), static_cast<uint32_t>(j));
+#pragma unroll
+      for (int r = 0; r < ATTEND_SMALL_MAX_KEYS / 32; ++r) {
+        const int j = r * 32 + lane;
+        const unsigned m = __ballot_sync(0xffffffffu, flag[r]);
+        if (flag[r]) st_shared_u16(pos + 2u * static_cast<uint32_t>(cnt + __popc(m & lt)), static_cast<uint32_t>(j));
         cnt += __popc(m);
       }
       if (lane == 0) {
