@@ -281,7 +281,7 @@ def kernel_source_sha(name):
 def pipeline_kernel_name(case, n_sms):
     """The kernel rra_pipeline launches for this workload under the automatic choice."""
     units = case.B * case.H * ((case.N + 127) // 128)
-    if units <= 2 * n_sms and case.N <= 256:
+    if units <= 4 * n_sms and case.N <= 256:
         return "attend_small_kernel (fused pipeline, small-grid form: mask scan, gather, attention, zero fill)"
     return "attend_tc_kernel (fused pipeline: mask scan, gather, attention, zero fill)"
 

@@ -418,12 +418,12 @@ RRA_API void rra_plan_destroy(rra_plan* plan);
  *                       specialisation): the shortest chain for grids of
  *                       about one unit per SM; max_seqlen (rra_pipeline: N)
  *                       up to 256, the TCGEN05 kernel beyond;
- *   RRA_ATTEND_AUTO     (default) while the grid (B * H *
- *                       ceil(max_seqlen / 128) units) fits in one wave of
- *                       two CTAs per SM and max_seqlen <= 256: rra_pipeline
- *                       TCGEN05_LATENCY, rra_attend MMA_SYNC (the shortest
- *                       chain on packed buffers at these sizes); TCGEN05
- *                       otherwise. */
+ *   RRA_ATTEND_AUTO     (default) with max_seqlen <= 256: rra_pipeline
+ *                       takes TCGEN05_LATENCY while the grid (B * H *
+ *                       ceil(max_seqlen / 128) units) is at most four per
+ *                       SM, rra_attend MMA_SYNC (the shortest chain on
+ *                       packed buffers) while it is at most two per SM;
+ *                       TCGEN05 otherwise. */
 typedef enum {
   RRA_ATTEND_TCGEN05 = 0,
   RRA_ATTEND_MMA_SYNC = 1,

@@ -145,15 +145,17 @@ AttendKernelChoice attend_choice(const DeviceState& st, int B, int H, int max_se
   if (k == RRA_ATTEND_MMA_SYNC) return KC_MMA;
   if (k == RRA_ATTEND_TCGEN05) return KC_TC;
   if (k == RRA_ATTEND_TCGEN05_LATENCY) return small_ok ? KC_TC_SMALL : KC_TC;
-  // Automatic.  While the grid fits in one wave of two CTAs per SM the call
-  // is one latency chain per CTA: the pipeline takes the small-grid tcgen05
-  // form (one launch that also scans the mask and writes the zero rows:
-  // 5.0 against 5.4 us for the warp-specialised fused kernel at serving
-  // B=4), rra_attend on packed buffers the mma.sync kernel (its
-  // register-resident chain: 3.4 against 4.1 us).  Beyond, the
+  // Automatic.  While the grid has a few units per SM each CTA is mostly
+  // one latency chain: the pipeline takes the small-grid tcgen05 form (one
+  // launch that also scans the mask and writes the zero rows) up to four
+  // units per SM (serving-like batches, N=197, H=6, fused us small / warp-
+  // specialised: B=4 4.0 / 5.3, B=32 5.8 / 6.7, B=48 7.1 / 7.4, B=64
+  // 10.1 / 8.3), rra_attend on packed buffers the mma.sync kernel up to two
+  // (its register-resident chain: 3.6 against 3.8-4.0 us).  Beyond, the
   // warp-specialised kernel.
   const long long units = static_cast<long long>(B) * H * ((max_seqlen + 127) / 128);
-  if (units <= 2LL * st.num_sms && small_ok) return pipeline ? KC_TC_SMALL : KC_MMA;
+  if (small_ok && pipeline && units <= 4LL * st.num_sms) return KC_TC_SMALL;
+  if (small_ok && !pipeline && units <= 2LL * st.num_sms) return KC_MMA;
   return KC_TC;
 }
 

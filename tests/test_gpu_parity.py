@@ -434,17 +434,20 @@ def test_attend_kernel_selector():
     rra.set_attend_kernel(prev)
 
 
-@pytest.mark.parametrize("make", [lambda: W.make_serving(4), lambda: W.make_tiny(), lambda: W.make_batched(0.8)],
-                         ids=["serving", "tiny", "large"])
+@pytest.mark.parametrize("make", [lambda: W.make_serving(4), lambda: W.make_tiny(), lambda: W.make_batched(0.8),
+                                  lambda: W.make_serving(32, seed=4321)],
+                         ids=["serving", "tiny", "large", "serving_B32"])
 def test_auto_kernel_matches_explicit(make):
-    """AUTO, while B*H*ceil(N/128) units fit in one wave of two CTAs per SM
-    (N <= 256): the pipeline runs the small-grid tcgen05 kernel and rra_attend
-    the mma.sync one; beyond, the warp-specialised kernel -- bit for bit."""
+    """AUTO with N <= 256: the pipeline runs the small-grid tcgen05 kernel
+    while B*H*ceil(N/128) units are at most four per SM, rra_attend the
+    mma.sync one while they are at most two per SM; beyond, the
+    warp-specialised kernel -- bit for bit."""
     case = make()
     units = case.B * case.H * ((case.N + 127) // 128)
     sms = torch.cuda.get_device_properties(0).multi_processor_count
+    small_pipe = units <= 4 * sms and case.N <= 256
     small = units <= 2 * sms and case.N <= 256
-    expect = rra.ATTEND_TCGEN05_LATENCY if small else rra.ATTEND_TCGEN05
+    expect = rra.ATTEND_TCGEN05_LATENCY if small_pipe else rra.ATTEND_TCGEN05
     outs = {}
     for k in (rra.ATTEND_AUTO, expect):
         prev = rra.set_attend_kernel(k)
@@ -452,6 +455,7 @@ def test_auto_kernel_matches_explicit(make):
         rra.set_attend_kernel(prev)
     a, b = outs.values()
     assert np.array_equal(bits(a), bits(b))
+    check_output(a, case.keep.numpy(), oracle_result(case)["out"])
     ref, qp, kp, vp, cu = _packed_inputs(case)
     B, N = case.B, case.N
     res = {}
