@@ -157,13 +157,9 @@ __global__ void __launch_bounds__(STHREADS)
       cp_async16(sK + swz128(r, ch), kg + off);
       cp_async16(sV + swz128(r, ch), vg + off);
     }
-    asm volatile("cp.async.wait_all;" ::: "memory");
-    fence_proxy_async();   // the copies (generic proxy) before the products read them
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-
-    // Where this thread's row goes (element offset of its output row), or -1.
+    // Where this thread's row goes (element offset of its output row), or
+    // -1; looked up while the copies are in flight, so the scatter index's
+    // load does not add a round trip before the first product.
     long long out_elem = -1;
     {
       const int i = q0 + tid;
@@ -184,6 +180,12 @@ __global__ void __launch_bounds__(STHREADS)
         out_elem = dst_row < 0 ? -1 : (dst_row * a.H + h) * HD;
       }
     }
+
+    asm volatile("cp.async.wait_all;" ::: "memory");
+    fence_proxy_async();   // the copies (generic proxy) before the products read them
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
 
     // 3. Per chunk: S, softmax, P.V.
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
