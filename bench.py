@@ -265,7 +265,7 @@ def kernel_times(case, sets, rra, stream, n_launch=None, packed=False):
 # headers it includes when it was captured, bytes).  Once any of them changes, the
 # traffic is reported as null until it is captured again.
 KERNEL_HEADERS = ("common.cuh", "tc_ptx.cuh", "softmax_tc.cuh")
-TRAFFIC = {"serving_B4": ("attend_small.cu", "2f0a1a4995924210", 421376),
+TRAFFIC = {"serving_B4": ("attend_small.cu", "9aa3be4f30069e31", 421376),
            "batched_b64_p80": ("attend_tc.cu", "be714d8c0419632c", 11919360)}
 
 
