@@ -151,8 +151,8 @@ AttendKernelChoice attend_choice(const DeviceState& st, int B, int H, int max_se
   // units per SM (serving-like batches, N=197, H=6, fused us small / warp-
   // specialised: B=4 4.0 / 5.3, B=32 5.8 / 6.7, B=48 7.1 / 7.4, B=64
   // 10.1 / 8.3), rra_attend on packed buffers the mma.sync kernel up to two
-  // (its register-resident chain: 3.6 against 3.8-4.0 us).  Beyond, the
-  // warp-specialised kernel.
+  // (its register-resident chain returns to a polling host in 10.2-10.4 us
+  // against 10.6-10.7 us at B=1-4).  Beyond, the warp-specialised kernel.
   const long long units = static_cast<long long>(B) * H * ((max_seqlen + 127) / 128);
   if (small_ok && pipeline && units <= 4LL * st.num_sms) return KC_TC_SMALL;
   if (small_ok && !pipeline && units <= 2LL * st.num_sms) return KC_MMA;
