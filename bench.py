@@ -322,8 +322,15 @@ def roofline_obj(bytes_alg, flops, us, peaks):
             "frac": round(hbm_frac, 4), "traffic": None}
 
 
+def percentile(samples, q):
+    """The q-quantile of the samples (nearest rank, no interpolation)."""
+    s = sorted(samples)
+    return s[min(len(s) - 1, int(q * len(s)))]
+
+
 def host_latency(rra, B, stream, reps=1000, warmup=100):
-    """Median host-timed µs of one rra_attend at serving batch B: + stream sync, and as rra_attend_wait."""
+    """Host-timed µs of one rra_attend at serving batch B (median; p90 for the two C-timed
+    forms): + stream sync, and as rra_attend_wait."""
     case = W.make_serving(B)
     keep, q, k, v = (x.cuda() for x in (case.keep, case.q, case.k, case.v))
     out = torch.empty_like(q)
@@ -352,7 +359,9 @@ def host_latency(rra, B, stream, reps=1000, warmup=100):
     if rra.get_device_error() != 0:
         raise RuntimeError("host_latency: a kernel recorded a device-side error")
     return {"attend_c": round(statistics.median(c_samples), 2),
+            "attend_c_p90": round(percentile(c_samples, 0.9), 2),
             "attend_wait_c": round(statistics.median(w_samples), 2),
+            "attend_wait_c_p90": round(percentile(w_samples, 0.9), 2),
             "attend_python": round(statistics.median(py), 2),
             "pipeline_graph_c": round(statistics.median(g_samples), 2),
             "null_kernel_c": round(statistics.median(null), 2)}

@@ -55,3 +55,12 @@ def test_both_arms_share_the_config():
     a = bench.workload_config(case, desc, 1)
     b = bench.workload_config(case, desc, 1)
     assert a == b and a["workload"] == desc and a["kept_tokens_per_step"] == case.kept_tokens
+
+
+def test_percentile_nearest_rank():
+    xs = list(range(1, 11))            # 1..10
+    assert bench.percentile(xs, 0.9) == 10
+    assert bench.percentile(xs, 0.5) == 6
+    assert bench.percentile(xs, 0.0) == 1
+    assert bench.percentile([3.0], 0.9) == 3.0
+    assert bench.percentile(list(reversed(xs)), 0.9) == 10   # order of the samples does not matter
