@@ -305,8 +305,10 @@ RRA_API rra_status rra_unpack(const void* op, const int32_t* dst_idx, int B, int
                               rra_dtype dtype, void* out, void* stream);
 
 /* The whole path, no host synchronisation, `out` [B, N, H, d] of out_dtype.
- * With the tcgen05 attention kernel (RRA_ATTEND_TCGEN05 or AUTO): ONE kernel launch that scans each image's keep row on the
- * device, gathers the kept Q/K/V rows straight from q/k/v (TMA gather4),
+ * With a tcgen05 attention kernel (RRA_ATTEND_TCGEN05, _TCGEN05_LATENCY or
+ * AUTO): ONE kernel launch that scans each image's keep row on the device,
+ * gathers the kept Q/K/V rows straight from q/k/v (TMA gather4 in the
+ * warp-specialised kernel, 16-byte cp.async copies in its small-grid form),
  * computes the attention and writes every output row -- kept positions get
  * the attention, pruned ones +0; the workspace is not touched.  With the
  * mma.sync kernel: rra_pack (with the row copy) then rra_attend on the
